@@ -1,0 +1,204 @@
+"""Exact tiled softmax attention for NVIDIA GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``libattn_gb300.so``.  Each function
+here has the name of the C entry point it calls and only marshals arguments:
+it checks tensor metadata, allocates outputs with PyTorch (device memory and
+streams are PyTorch's job) and passes raw pointers.  Every step of the
+computation runs in the library's CUDA kernels; there is no CPU or PyTorch
+fallback, and a missing library raises.
+
+Tensors are [B, H, N, d], contiguous.  Inputs on the CPU are accepted for the
+forward calls: they are copied to the current CUDA device on the current
+stream, and the outputs are copied back to the CPU.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_ARCH = 3
+ATTN_ERR_CUDA = 4
+ATTN_ERR_TIMEOUT = 5
+
+_DTYPES = {torch.bfloat16: 0, torch.float16: 1}
+
+__all__ = ["AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
+           "attn_fp8_quantize", "attn_fwd_fp8", "attn_get_device_status",
+           "attn_status_string", "attn_last_error", "load_library"]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        lib = _lib.load()
+        detail = lib.attn_last_error().decode()
+        super().__init__(f"{where}: {lib.attn_status_string(code).decode()} ({code})"
+                         + (f": {detail}" if detail else ""))
+        self.code = code
+
+
+def load_library():
+    """Load libattn_gb300.so (raises if it is not built)."""
+    return _lib.load()
+
+
+def _check(code: int, where: str):
+    if code != ATTN_OK:
+        raise AttnError(code, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _shape4(t, name):
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be [B, H, N, d]")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return tuple(t.shape)
+
+
+def _to_device(ts):
+    """Copy CPU inputs to the current device; report whether results go back."""
+    on_host = all(t.device.type == "cpu" for t in ts)
+    if on_host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        ts = [t.to(dev, non_blocking=True) for t in ts]
+    return ts, on_host
+
+
+def attn_status_string(code: int) -> str:
+    return _lib.load().attn_status_string(code).decode()
+
+
+def attn_last_error() -> str:
+    return _lib.load().attn_last_error().decode()
+
+
+def attn_get_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return _lib.load().attn_get_device_status(_stream(stream))
+
+
+def attn_fwd(q, k, v, causal: bool = False, softmax_scale: float | None = None,
+             o=None, lse=None, stream=None):
+    """O, LSE = attention(q, k, v) in bf16/fp16; LSE is float32 [B, H, N]."""
+    lib = _lib.load()
+    (q, k, v), host = _to_device([q, k, v])
+    B, H, N, d = _shape4(q, "q")
+    if _shape4(k, "k") != (B, H, N, d) or _shape4(v, "v") != (B, H, N, d):
+        raise ValueError("q, k, v must have the same shape")
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must all be bfloat16 or all float16")
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    code = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                        int(bool(causal)), scale, _DTYPES[q.dtype], _stream(stream))
+    _check(code, "attn_fwd")
+    if host:
+        return o.cpu(), lse.cpu()
+    return o, lse
+
+
+def attn_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(_lib.load().attn_bwd_workspace_size(B, H, N, d))
+
+
+def attn_bwd(q, k, v, o, dout, lse, causal: bool = False, softmax_scale: float | None = None,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of sum(O * dO); o and lse come from attn_fwd."""
+    lib = _lib.load()
+    (q, k, v, o, dout, lse), host = _to_device([q, k, v, o, dout, lse])
+    B, H, N, d = _shape4(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        if _shape4(t, n) != (B, H, N, d) or t.dtype != q.dtype:
+            raise ValueError(f"{n} must match q in shape and dtype")
+    if q.dtype not in _DTYPES:
+        raise ValueError("tensors must be bfloat16 or float16")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [B, H, N]")
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = attn_bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    code = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                        workspace.numel() * workspace.element_size(),
+                        B, H, N, d, int(bool(causal)), scale, _DTYPES[q.dtype], _stream(stream))
+    _check(code, "attn_bwd")
+    if host:
+        return dq.cpu(), dk.cpu(), dv.cpu()
+    return dq, dk, dv
+
+
+def attn_fp8_quantize(q, k, v, hadamard_signs=None, per_tensor: bool = False, stream=None):
+    """float32 Q, K, V -> (q8, k8, v8) uint8 e4m3 codes and float32 descales."""
+    lib = _lib.load()
+    ins = [q, k, v] + ([hadamard_signs] if hadamard_signs is not None else [])
+    ins, host = _to_device(ins)
+    q, k, v = ins[:3]
+    signs = ins[3] if hadamard_signs is not None else None
+    B, H, N, d = _shape4(q, "q")
+    for t, n in ((k, "k"), (v, "v")):
+        if _shape4(t, n) != (B, H, N, d) or t.dtype != torch.float32:
+            raise ValueError(f"{n} must match q")
+    if q.dtype != torch.float32:
+        raise ValueError("FP8 pre-pass inputs are float32")
+    if signs is not None and (signs.dtype != torch.float32 or signs.numel() != d):
+        raise ValueError("hadamard_signs must be d float32 values")
+    nblk = (N + 127) // 128
+    outs = [torch.empty((B, H, N, d), dtype=torch.uint8, device=q.device) for _ in range(3)]
+    desc = [torch.empty((B, H, nblk), dtype=torch.float32, device=q.device) for _ in range(3)]
+    code = lib.attn_fp8_quantize(_ptr(q), _ptr(k), _ptr(v), _ptr(signs),
+                                 *[_ptr(t) for t in outs], *[_ptr(t) for t in desc],
+                                 B, H, N, d, int(bool(per_tensor)), _stream(stream))
+    _check(code, "attn_fp8_quantize")
+    if host:
+        return tuple(t.cpu() for t in outs), tuple(t.cpu() for t in desc)
+    return tuple(outs), tuple(desc)
+
+
+def attn_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, causal: bool = False,
+                 softmax_scale: float | None = None, o=None, lse=None, stream=None):
+    """FP8 forward: e4m3 inputs with block descales -> O (bfloat16), LSE (float32)."""
+    lib = _lib.load()
+    (q8, k8, v8, q_descale, k_descale, v_descale), host = _to_device(
+        [q8, k8, v8, q_descale, k_descale, v_descale])
+    B, H, N, d = _shape4(q8, "q8")
+    for t, n in ((k8, "k8"), (v8, "v8")):
+        if _shape4(t, n) != (B, H, N, d) or t.dtype != torch.uint8:
+            raise ValueError(f"{n} must match q8 (uint8 e4m3 codes)")
+    nblk = (N + 127) // 128
+    for t in (q_descale, k_descale, v_descale):
+        if t.dtype != torch.float32 or tuple(t.shape) != (B, H, nblk) or not t.is_contiguous():
+            raise ValueError("descales must be contiguous float32 [B, H, ceil(N/128)]")
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    code = lib.attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_descale), _ptr(k_descale),
+                            _ptr(v_descale), _ptr(o), _ptr(lse), B, H, N, d,
+                            int(bool(causal)), scale, _stream(stream))
+    _check(code, "attn_fwd_fp8")
+    if host:
+        return o.cpu(), lse.cpu()
+    return o, lse

@@ -1,0 +1,273 @@
+// The C ABI: argument validation, device checks, tensor maps, status word.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "common.h"
+
+namespace attn {
+
+namespace {
+
+thread_local std::string g_last_error;
+
+// One status word per device; kernels record the first internal error here.
+__device__ int g_device_status;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];
+int g_arch_ok[kMaxDevices];   // 0 unknown, 1 ok, 2 wrong arch
+std::mutex g_dev_mutex;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Pure argument checks: no CUDA call is made here, so they also run on a
+// machine without a GPU.
+attn_status_t check_shape(int B, int H, int N, int d, int causal) {
+  if (B < 1 || H < 1 || N < 1) return fail(ATTN_ERR_INVALID_ARG, "B, H and N must be >= 1");
+  if (d != 64 && d != 128 && d != 256)
+    return fail(ATTN_ERR_INVALID_ARG, "d must be 64, 128 or 256");
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  const double elems = static_cast<double>(B) * H * N * d;
+  if (elems >= 2147483648.0) return fail(ATTN_ERR_INVALID_ARG, "B*H*N*d must be < 2^31");
+  return ATTN_OK;
+}
+
+attn_status_t check_ptrs(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs) {
+    if (p == nullptr) return fail(ATTN_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(p)) return fail(ATTN_ERR_INVALID_ARG, "tensor pointer not 16-byte aligned");
+  }
+  return ATTN_OK;
+}
+
+attn_status_t check_scale(float s) {
+  if (!(s > 0.f) || !std::isfinite(s))
+    return fail(ATTN_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
+  return ATTN_OK;
+}
+
+// Device checks: compute capability 10.3 and the status word address.
+attn_status_t check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device ordinal out of range");
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_arch_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+    e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+    g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    if (g_arch_ok[dev] == 1) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_device_status);
+      if (e != cudaSuccess) {
+        g_arch_ok[dev] = 0;
+        return fail_cuda(e, "cudaGetSymbolAddress(status word)");
+      }
+      g_status_ptr[dev] = static_cast<int*>(p);
+    }
+  }
+  if (g_arch_ok[dev] != 1)
+    return fail(ATTN_ERR_ARCH, "this library runs on compute capability 10.3 (GB300) only");
+  return ATTN_OK;
+}
+
+}  // namespace
+
+attn_status_t fail(attn_status_t code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+attn_status_t fail_cuda(cudaError_t err, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorName(err) + " (" +
+                 cudaGetErrorString(err) + ")";
+  return ATTN_ERR_CUDA;
+}
+
+int* device_status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  return g_status_ptr[dev];
+}
+
+attn_status_t make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
+                           uint64_t rows, uint64_t planes, uint32_t box_inner,
+                           uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {inner, rows, planes};
+  cuuint64_t strides[2] = {inner * elem_bytes, inner * rows * elem_bytes};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMapDataType dt =
+      elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  CUresult r = enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
+  return ATTN_OK;
+}
+
+attn_status_t set_smem(const void* kernel, int bytes) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+  return ATTN_OK;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported shape or mode";
+    case ATTN_ERR_ARCH: return "device is not compute capability 10.3";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "a kernel wait exceeded its time limit";
+  }
+  return "unknown status";
+}
+
+const char* attn_last_error(void) { return g_last_error.c_str(); }
+
+size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return align_up(rows * d * sizeof(float), 256) + align_up(rows * sizeof(float), 256);
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N, int d, int causal, float softmax_scale, attn_dtype_t dtype,
+                       cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if ((s = check_shape(B, H, N, d, causal)) != ATTN_OK) return s;
+  if ((s = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return s;
+  if ((s = check_scale(softmax_scale)) != ATTN_OK) return s;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_BF16 or ATTN_FP16");
+  if ((s = check_device()) != ATTN_OK) return s;
+  FwdParams p{q, k, v, o, lse, B, H, N, d, causal, softmax_scale, dtype == ATTN_FP16 ? 1 : 0};
+  return launch_fwd(p, stream);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                       int causal, float softmax_scale, attn_dtype_t dtype,
+                       cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if ((s = check_shape(B, H, N, d, causal)) != ATTN_OK) return s;
+  if ((s = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace})) != ATTN_OK) return s;
+  if ((s = check_scale(softmax_scale)) != ATTN_OK) return s;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_BF16 or ATTN_FP16");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (workspace_bytes < attn_bwd_workspace_size(B, H, N, d))
+    return fail(ATTN_ERR_INVALID_ARG, "workspace smaller than attn_bwd_workspace_size()");
+  if (d == 256) return fail(ATTN_ERR_UNSUPPORTED, "the backward pass supports d = 64 and 128");
+  if ((s = check_device()) != ATTN_OK) return s;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          align_up(rows * d * sizeof(float), 256));
+  BwdParams p{q, k, v, o, dout, lse, dq, dk, dv, dq_acc, delta, B, H, N, d, causal,
+              softmax_scale, dtype == ATTN_FP16 ? 1 : 0};
+  return launch_bwd(p, stream);
+}
+
+attn_status_t attn_fp8_quantize(const float* q, const float* k, const float* v,
+                                const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                uint8_t* v8, float* q_descale, float* k_descale,
+                                float* v_descale, int B, int H, int N, int d, int per_tensor,
+                                cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if ((s = check_shape(B, H, N, d, 0)) != ATTN_OK) return s;
+  if ((s = check_ptrs({q, k, v, q8, k8, v8, q_descale, k_descale, v_descale})) != ATTN_OK)
+    return s;
+  if (per_tensor != 0 && per_tensor != 1)
+    return fail(ATTN_ERR_INVALID_ARG, "per_tensor must be 0 or 1");
+  if (per_tensor && hadamard_signs)
+    return fail(ATTN_ERR_INVALID_ARG, "the per-tensor comparator takes no Hadamard signs");
+  if (hadamard_signs && !aligned16(hadamard_signs))
+    return fail(ATTN_ERR_INVALID_ARG, "hadamard_signs not 16-byte aligned");
+  if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
+  if ((s = check_device()) != ATTN_OK) return s;
+  Fp8QuantParams p{{q, k, v}, {q8, k8, v8}, {q_descale, k_descale, v_descale}, hadamard_signs,
+                   B, H, N, d, per_tensor};
+  return launch_fp8_quantize(p, stream);
+}
+
+attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
+                           const float* q_descale, const float* k_descale,
+                           const float* v_descale, void* o, float* lse, int B, int H, int N,
+                           int d, int causal, float softmax_scale, cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if ((s = check_shape(B, H, N, d, causal)) != ATTN_OK) return s;
+  if ((s = check_ptrs({q8, k8, v8, o, lse})) != ATTN_OK) return s;
+  if (!q_descale || !k_descale || !v_descale)
+    return fail(ATTN_ERR_INVALID_ARG, "null descale pointer");
+  if ((s = check_scale(softmax_scale)) != ATTN_OK) return s;
+  if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
+  if ((s = check_device()) != ATTN_OK) return s;
+  Fp8FwdParams p{q8, k8, v8, q_descale, k_descale, v_descale, o, lse, B, H, N, d, causal,
+                 softmax_scale};
+  return launch_fwd_fp8(p, stream);
+}
+
+attn_status_t attn_get_device_status(cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if ((s = check_device()) != ATTN_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+  int* word = device_status_word();
+  int value = 0;
+  e = cudaMemcpy(&value, word, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e, "reading the status word");
+  if (value == 0) return ATTN_OK;
+  const int zero = 0;
+  e = cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail_cuda(e, "clearing the status word");
+  static const char* roles[] = {"?", "load", "mma", "softmax", "epilogue", "reduce"};
+  const int role = (value >> 8) & 0xF;
+  return fail(ATTN_ERR_TIMEOUT, std::string("kernel wait timed out in role ") +
+                                    (role < 6 ? roles[role] : "?") + " (code " +
+                                    std::to_string(value) + ")");
+}
+
+}  // extern "C"

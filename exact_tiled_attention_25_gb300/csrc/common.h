@@ -1,0 +1,91 @@
+// Host-side internals shared by the kernel translation units and the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include "../../include/attn_gb300.h"
+
+namespace attn {
+
+// Record a detail message for attn_last_error() and return `code`.
+attn_status_t fail(attn_status_t code, const std::string& msg);
+attn_status_t fail_cuda(cudaError_t err, const char* what);
+
+// Device address of the status word of the current device.
+int* device_status_word();
+
+// 3-D tensor map over a contiguous [planes][rows][inner] array with a
+// (box_inner x box_rows x 1) box and 128-byte swizzle.  elem_bytes is 1 or 2.
+attn_status_t make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
+                           uint64_t rows, uint64_t planes, uint32_t box_inner,
+                           uint32_t box_rows);
+
+// Opt a kernel into more than 48 KB of dynamic shared memory (once per kernel).
+attn_status_t set_smem(const void* kernel, int bytes);
+
+struct FwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, H, N, d;
+  int causal;
+  float scale;
+  int fp16;   // 0 = bf16, 1 = fp16
+};
+
+struct BwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;   // [B, H, N, d] float32 scratch
+  float* delta;    // [B, H, N] float32 scratch
+  int B, H, N, d;
+  int causal;
+  float scale;
+  int fp16;
+};
+
+struct Fp8QuantParams {
+  const float* src[3];
+  uint8_t* dst[3];
+  float* descale[3];
+  const float* signs;
+  int B, H, N, d;
+  int per_tensor;
+};
+
+struct Fp8FwdParams {
+  const uint8_t* q8;
+  const uint8_t* k8;
+  const uint8_t* v8;
+  const float* q_descale;
+  const float* k_descale;
+  const float* v_descale;
+  void* o;
+  float* lse;
+  int B, H, N, d;
+  int causal;
+  float scale;
+};
+
+attn_status_t launch_fwd(const FwdParams& p, cudaStream_t stream);
+attn_status_t launch_bwd(const BwdParams& p, cudaStream_t stream);
+attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream);
+attn_status_t launch_fwd_fp8(const Fp8FwdParams& p, cudaStream_t stream);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace attn

@@ -1,0 +1,417 @@
+// BF16/FP16 attention forward on sm_103a.
+//
+// Method: "FlashAttention-3: Hopper Asynchrony and FP8 Attention" -- the query
+// tile stays on chip while key/value tiles stream through a ring of
+// shared-memory stages ("Producer-consumer asynchrony"), the running row max
+// m and sum l are updated per tile and the output numerator is rescaled when
+// m grows ("Symbol Map"; "Putting It Together", steps 4-5), and the epilogue
+// divides by l and stores L = m + log(l) ("Putting It Together", step 7).
+//
+// GB300 design (not the page's Hopper design):
+//  * One CTA owns NQ query tiles of 128 rows (NQ = 2 for d <= 128, 1 for
+//    d = 256).  Scores S_t and output accumulators O_t live in tensor memory
+//    (TMEM); the probabilities P_t are written back over S_t as 16-bit values
+//    and fed to the P V product straight from TMEM.
+//  * Warp roles: one TMA producer warp, one MMA warp whose elected thread
+//    issues every tcgen05.mma, and one softmax warpgroup per query tile whose
+//    thread i owns row i (TMEM lane i) of S_t and O_t.  The MMA thread
+//    alternates between the tiles, so while one warpgroup runs its
+//    exponentials the tensor core works on the other tile -- the same overlap
+//    the page's "Ping-pong scheduling" gets from two Hopper warpgroups.
+//  * Rescaling is lazy: the exponent reference m_ref moves only when the row
+//    max exceeds it by more than 8 (log2 units), so P <= 2^8 and most tiles
+//    skip the TMEM read-modify-write of O.  In exact arithmetic the result is
+//    the same as rescaling on every tile.
+//  * Causal: query tile i visits key tiles 0..i only and masks the diagonal
+//    tile; CTAs are launched longest-first.
+#include <cmath>
+
+#include "common.h"
+#include "sm103_prims.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int BM = 128;   // query rows per tile
+constexpr int BN = 128;   // keys per tile
+constexpr int kSmemLimit = 232448;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NQ = (D <= 128) ? 2 : 1;
+  static constexpr int CH = D / 64;                  // 128-byte column chunks per row
+  static constexpr int CHUNK_BYTES = BM * 128;       // one 128-row x 128-byte chunk
+  static constexpr int TILE_BYTES = BM * D * 2;      // a Q, K or V tile
+  static constexpr int NSLOT_FIT = (kSmemLimit - 2048 - NQ * TILE_BYTES) / TILE_BYTES;
+  static constexpr int NSLOT = NSLOT_FIT > 6 ? 6 : NSLOT_FIT;
+  static constexpr int SMEM_BYTES = 1024 + NQ * TILE_BYTES + NSLOT * TILE_BYTES;
+  static constexpr int NUM_SOFTMAX_WARPS = 4 * NQ;
+  static constexpr int LOAD_WARP = NUM_SOFTMAX_WARPS;
+  static constexpr int MMA_WARP = NUM_SOFTMAX_WARPS + 1;
+  static constexpr int THREADS = (NUM_SOFTMAX_WARPS + 2) * 32;
+  __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }
+  __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256u + static_cast<uint32_t>(D) * t; }
+  static_assert(NSLOT >= 2, "need at least two ring stages");
+  static_assert(O_COL(NQ - 1) + D <= 512, "TMEM overflow");
+  static_assert(S_COL(NQ - 1) + 128 <= 256, "S region overflow");
+};
+
+struct FwdKParams {
+  void* o;
+  float* lse;
+  int* status;
+  int N;
+  int H;
+  float scale_log2;   // softmax_scale * log2(e)
+};
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int D, bool CAUSAL, bool FP16>
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const FwdKParams kp) {
+  using C = FwdCfg<D>;
+  constexpr int NQ = C::NQ;
+  constexpr int NSLOT = C::NSLOT;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + NQ * C::TILE_BYTES;
+
+  __shared__ __align__(8) uint64_t q_full[NQ];
+  __shared__ __align__(8) uint64_t kv_full[NSLOT];
+  __shared__ __align__(8) uint64_t kv_empty[NSLOT];
+  __shared__ __align__(8) uint64_t s_full[NQ];
+  __shared__ __align__(8) uint64_t p_full[NQ];
+  __shared__ __align__(8) uint64_t o_full[NQ];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ int load_items_sh;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int g = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int bh = blockIdx.z * kp.H + blockIdx.y;
+  const int N = kp.N;
+  const int nKtot = (N + BN - 1) / BN;
+
+  int nK[NQ];
+  int nKmax = 0;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    const int qt = g * NQ + t;
+    nK[t] = (qt * BM < N) ? (CAUSAL ? min(nKtot, qt + 1) : nKtot) : 0;
+    nKmax = max(nKmax, nK[t]);
+  }
+  const int total_items = 2 * nKmax;   // K_0, V_0, K_1, V_1, ...
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < NQ; ++t) {
+      mbar_init(&q_full[t], 1);
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&o_full[t], 1);
+    }
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    load_items_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+  const Abort ab{&abort_sh, kp.status};
+
+  if (warp == C::LOAD_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      for (int t = 0; t < NQ; ++t) {
+        if (nK[t] == 0) continue;
+        mbar_arrive_expect_tx(&q_full[t], C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_3d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, &q_full[t], c * 64,
+                      (g * NQ + t) * BM, bh);
+      }
+      int it = 0;
+      bool ok = true;
+      for (int j = 0; j < nKmax && ok; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int slot = it % NSLOT;
+          const int use = it / NSLOT;
+          if (use >= 1 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, ab, kDevTimeoutLoad)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&kv_full[slot], C::TILE_BYTES);
+          uint8_t* dst = sKV + slot * C::TILE_BYTES;
+#pragma unroll
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tmV : &tmK, &kv_full[slot], c * 64,
+                        j * BN, bh);
+          ++it;
+        }
+      }
+      load_items_sh = it;
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr Elt E = FP16 ? Elt::F16 : Elt::BF16;
+      constexpr uint32_t idS = idesc_f16(E, 128, BN, false, false);
+      constexpr uint32_t idPV = idesc_f16(E, 128, D, false, true);
+      bool ok = true;
+      for (int t = 0; t < NQ && ok; ++t)
+        if (nK[t] > 0) ok = mbar_wait(&q_full[t], 0, ab, kDevTimeoutMma);
+      for (int j = 0; j <= nKmax && ok; ++j) {
+        const int itK = 2 * j;
+        const int itV = 2 * (j - 1) + 1;
+        const int slotK = itK % NSLOT;
+        const int slotV = (itV + NSLOT) % NSLOT;
+        if (j < nKmax && !mbar_wait(&kv_full[slotK], (itK / NSLOT) & 1, ab, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        if (j >= 1 && !mbar_wait(&kv_full[slotV], (itV / NSLOT) & 1, ab, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        for (int t = 0; t < NQ; ++t) {
+          if (j >= 1 && j - 1 < nK[t]) {
+            // O_t += P_t(j-1) V_{j-1}
+            if (!mbar_wait(&p_full[t], (j - 1) & 1, ab, kDevTimeoutMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t vbase = smem_u32(sKV + slotV * C::TILE_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, C::CHUNK_BYTES, 1024);
+              mma_f16_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, bdesc, idPV,
+                         (j - 1 > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (j - 1 == nK[t] - 1) mma_commit(&o_full[t]);
+          }
+          if (j < nK[t]) {
+            // S_t(j) = Q_t K_j^T
+            const uint32_t qbase = smem_u32(sQ + t * C::TILE_BYTES);
+            const uint32_t kbase = smem_u32(sKV + slotK * C::TILE_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32;
+              mma_f16_ss(tmem + C::S_COL(t), sdesc_sw128(qbase + off, 16, 1024),
+                         sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&s_full[t]);
+          }
+        }
+        if (!ok) break;
+        // hand ring slots back to the producer once the MMAs reading them finish
+        if (j >= 1 && itV + NSLOT < total_items) mma_commit(&kv_empty[slotV]);
+        if (j < nKmax && itK + NSLOT < total_items) mma_commit(&kv_empty[slotK]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp / 4;
+    const int quarter = warp % 4;
+    const int r = quarter * 32 + lane;
+    const int qt = g * NQ + t;
+    const int row_g = qt * BM + r;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + C::S_COL(t);
+    const uint32_t tO = tmem + lane_addr + C::O_COL(t);
+    const float c2 = kp.scale_log2;
+    float m_ref = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nK[t]; ++j) {
+      if (!mbar_wait(&s_full[t], j & 1, ab, kDevTimeoutSoftmax)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t sr[BN];
+#pragma unroll
+      for (int c0 = 0; c0 < BN / 32; ++c0)
+        tmem_ld32(tS + c0 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0 * 32]));
+      tmem_ld_wait();
+      const int kbase = j * BN;
+      if ((CAUSAL && j == qt) || kbase + BN > N) {
+        const int lim = (CAUSAL ? min(N, row_g + 1) : N) - kbase;
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; c += 8) {
+        mx0 = fmax3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+        mx2 = fmax3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+        mx3 = fmax3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+      }
+      const float m_new = fmaxf(m_ref, fmax3(mx0, mx1, fmaxf(mx2, mx3)));
+      // Move the exponent reference only when the max grew by more than 2^8.
+      const bool need = (m_new - m_ref) * c2 > 8.f;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2_approx((m_ref - m_new) * c2);
+        l *= alpha;
+        m_ref = m_new;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D / 32; ++c0) {
+          uint32_t o[32];
+          tmem_ld32(tO + c0 * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c0 * 32, o);
+        }
+      }
+      const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref * c2;
+      const uint64_t cc = pack2(c2, c2);
+      const uint64_t nn = pack2(neg, neg);
+      uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+      for (int c0 = 0; c0 < BN / 32; ++c0) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = c0 * 32 + 2 * i;
+          const uint64_t y = ffma2(pack2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), cc, nn);
+          const float p0 = ex2_approx(lo2(y));
+          const float p1 = ex2_approx(hi2(y));
+          if (i & 1) acc1 = fadd2(acc1, pack2(p0, p1));
+          else acc0 = fadd2(acc0, pack2(p0, p1));
+          pk[i] = FP16 ? cvt_pack_f16(p0, p1) : cvt_pack_bf16(p0, p1);
+        }
+        tmem_st16(tS + c0 * 16, pk);
+      }
+      const uint64_t acc = fadd2(acc0, acc1);
+      l += lo2(acc) + hi2(acc);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&p_full[t]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && nK[t] > 0 && mbar_wait(&o_full[t], 0, ab, kDevTimeoutEpilogue)) {
+      tc_fence_after_sync();
+      const float inv_l = 1.f / l;
+      uint16_t* orow = static_cast<uint16_t*>(kp.o) + (static_cast<size_t>(bh) * N + row_g) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 32; ++c0) {
+        uint32_t o[32];
+        tmem_ld32(tO + c0 * 32, o);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = __uint_as_float(o[2 * i]) * inv_l;
+          const float b = __uint_as_float(o[2 * i + 1]) * inv_l;
+          pk[i] = FP16 ? cvt_pack_f16(a, b) : cvt_pack_bf16(a, b);
+        }
+        if (row_g < N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (row_g < N)
+        kp.lse[static_cast<size_t>(bh) * N + row_g] =
+            (m_ref * c2 + lg2_approx(l)) * 0.69314718055994530942f;
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (abort_sh) {
+    // Let every copy and MMA this CTA issued land before the memory goes away.
+    if (warp == C::LOAD_WARP && lane == 0) {
+      for (int t = 0; t < NQ; ++t)
+        if (nK[t] > 0) mbar_wait_drain(&q_full[t], 0);
+      const int issued = load_items_sh;
+      for (int s = 0; s < NSLOT && s < issued; ++s)
+        mbar_wait_drain(&kv_full[s], ((issued - 1 - s) / NSLOT) & 1);
+    }
+    if (warp == C::MMA_WARP && lane == 0) {
+      mma_commit(&drain_bar);
+      mbar_wait_drain(&drain_bar, 0);
+    }
+    __syncthreads();
+  }
+  if (warp == C::MMA_WARP) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool FP16>
+attn_status_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = fwd_kernel<D, CAUSAL, FP16>;
+  attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
+  if (s != ATTN_OK) return s;
+  CUtensorMap tq, tk, tv;
+  const uint64_t planes = static_cast<uint64_t>(p.B) * p.H;
+  if ((s = make_tmap_3d(&tq, p.q, 2, D, p.N, planes, 64, BM)) != ATTN_OK) return s;
+  if ((s = make_tmap_3d(&tk, p.k, 2, D, p.N, planes, 64, BN)) != ATTN_OK) return s;
+  if ((s = make_tmap_3d(&tv, p.v, 2, D, p.N, planes, 64, BN)) != ATTN_OK) return s;
+  int* status = device_status_word();
+  if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
+  FwdKParams kp{p.o, p.lse, status, p.N, p.H, p.scale * 1.4426950408889634f};
+  const int rows_per_cta = BM * C::NQ;
+  dim3 grid((p.N + rows_per_cta - 1) / rows_per_cta, p.H, p.B);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, kp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "forward kernel launch");
+  return ATTN_OK;
+}
+
+template <int D>
+attn_status_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
+  if (p.causal)
+    return p.fp16 ? launch_fwd_t<D, true, true>(p, stream) : launch_fwd_t<D, true, false>(p, stream);
+  return p.fp16 ? launch_fwd_t<D, false, true>(p, stream) : launch_fwd_t<D, false, false>(p, stream);
+}
+
+}  // namespace
+
+attn_status_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
+  if (p.N > 65535 * 256 || p.H > 65535 || p.B > 65535)
+    return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
+  switch (p.d) {
+    case 64: return launch_fwd_d<64>(p, stream);
+    case 128: return launch_fwd_d<128>(p, stream);
+    case 256: return launch_fwd_d<256>(p, stream);
+  }
+  return fail(ATTN_ERR_INVALID_ARG, "d must be 64, 128 or 256");
+}
+
+}  // namespace attn

@@ -1,0 +1,164 @@
+/*
+ * attn_gb300 -- exact tiled softmax attention for one NVIDIA GB300 (sm_103a).
+ *
+ * Public C ABI of libattn_gb300.so.  Plain pointers and sizes only.
+ *
+ * What is computed.  For every batch b and head h, with S = softmax_scale * Q K^T
+ * (N x N, keys j > i set to -inf when causal != 0):
+ *     O   = softmax(S) V                        (row softmax)
+ *     LSE = m + log(l)                          (natural log; m = row max of S,
+ *                                                l = sum_j exp(S_ij - m))
+ * "FlashAttention-3: Hopper Asynchrony and FP8 Attention", section "Symbol Map"
+ * (O_i, m_i, l_i, L_i = m_i + log(l_i)) and "Putting It Together", step 7 (only O
+ * and L are written).  The result is exact attention up to floating-point
+ * rounding: S and P never reach global memory; the kernels walk key/value tiles
+ * with the online-softmax recurrence.  The causal mask is lower-triangular with
+ * top-left alignment (query i sees keys 0..i).
+ *
+ * Layout.  Every Q/K/V/O/dO/dQ/dK/dV tensor is [B, H, N, d], contiguous, d fastest
+ * ("BHND").  LSE and the FP8 descales are contiguous [B, H, N] and
+ * [B, H, ceil(N/128)] float32 arrays.  All pointers are DEVICE pointers on the
+ * current CUDA device, 16-byte aligned (a TMA requirement); the caller owns them.
+ *
+ * Supported shapes.  d in {64, 128, 256} for the forward passes, d in {64, 128}
+ * for the backward pass, d = 128 for the FP8 pass; N >= 1; B, H >= 1;
+ * B * H * N * d < 2^31.
+ *
+ * Errors.  Arguments are validated before anything is launched; a bad argument
+ * returns ATTN_ERR_INVALID_ARG, an unsupported (valid) shape ATTN_ERR_UNSUPPORTED,
+ * a device that is not compute capability 10.3 ATTN_ERR_ARCH, a failed CUDA call
+ * ATTN_ERR_CUDA (attn_last_error() then names it).  Launches are asynchronous on
+ * `stream`; results are ready when the stream has reached them.  A kernel never
+ * traps: if one of its internal waits exceeds its time limit it records the
+ * fact in a device status word and returns early, and attn_get_device_status()
+ * reports ATTN_ERR_TIMEOUT.
+ *
+ * Memory.  The library allocates no device memory per call.  It holds one
+ * 4-byte status word per device (a static device variable).  Scratch for the
+ * backward pass is supplied by the caller (attn_bwd_workspace_size()).
+ *
+ * Thread safety.  Calls may come from several host threads; the status word is
+ * shared by all calls on a device.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t in the CUDA runtime headers.  NULL = legacy default stream. */
+typedef struct CUstream_st* cudaStream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,
+  ATTN_ERR_UNSUPPORTED = 2,
+  ATTN_ERR_ARCH = 3,
+  ATTN_ERR_CUDA = 4,
+  ATTN_ERR_TIMEOUT = 5
+} attn_status_t;
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype_t;
+
+/*
+ * attn_fwd -- BF16/FP16 forward.
+ *   q, k, v : [B, H, N, d] in `dtype` (read only)
+ *   o       : [B, H, N, d] in `dtype` (written)
+ *   lse     : [B, H, N] float32 (written), natural-log LSE of the scaled,
+ *             masked scores; input to attn_bwd.
+ *   causal  : 0 or 1.   softmax_scale: > 0, finite (commonly 1/sqrt(d)).
+ * Source: "FlashAttention-3: Hopper Asynchrony and FP8 Attention", sections
+ * "Symbol Map", "Producer-consumer asynchrony", "Ping-pong scheduling",
+ * "Two-stage WGMMA-softmax pipeline", "Putting It Together".
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int H, int N, int d, int causal, float softmax_scale,
+                       attn_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * attn_bwd_workspace_size -- bytes of device scratch attn_bwd needs:
+ * a float32 dQ accumulator [B, H, N, d] and the row terms D = rowsum(dO * O)
+ * [B, H, N] float32, each 256-byte aligned.  Returns 0 for invalid sizes.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * attn_bwd -- BF16/FP16 backward: dQ, dK, dV of sum(O * dO).
+ *   q, k, v, o, dout : [B, H, N, d] in `dtype`; o and lse from attn_fwd with
+ *                      the same q, k, v, causal and softmax_scale.
+ *   lse              : [B, H, N] float32.
+ *   dq, dk, dv       : [B, H, N, d] in `dtype` (written).
+ *   workspace        : device scratch of at least attn_bwd_workspace_size()
+ *                      bytes, 256-byte aligned; its contents on entry do not
+ *                      matter and are overwritten.
+ * P and dS are recomputed from LSE ("FlashAttention-3: Hopper Asynchrony and
+ * FP8 Attention", section "Backward warp specialization"): a row-dot pre-pass
+ * D_i = dO_i . O_i, a key/value-tile-outer main kernel that accumulates dK, dV
+ * on chip and adds dQ partial tiles into the float32 accumulator, and a final
+ * conversion of dQ.
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                       int causal, float softmax_scale, attn_dtype_t dtype,
+                       cudaStream_t stream);
+
+/*
+ * attn_fp8_quantize -- FP8 e4m3 pre-pass with block scaling and incoherent
+ * processing ("FlashAttention-3: Hopper Asynchrony and FP8 Attention", section
+ * "FP8 accuracy controls").
+ *   q, k, v        : [B, H, N, d] float32 (read only); d must be 128.
+ *   hadamard_signs : d float32 values, each +1 or -1, or NULL.  When given, every
+ *                    row x of Q and of K becomes x M with M = diag(signs) H_d / sqrt(d)
+ *                    (H_d the Sylvester Hadamard matrix) before quantisation;
+ *                    V is never transformed.  (QM)(KM)^T = QK^T, so the FP8
+ *                    forward needs no knowledge of the transform.
+ *   q8, k8, v8     : [B, H, N, d] e4m3 bytes (written).
+ *   q_descale, k_descale, v_descale : [B, H, ceil(N/128)] float32 (written):
+ *                    per 128-row block, descale = amax / 448 (1 if amax = 0) and
+ *                    code = e4m3_rn_satfinite(x / descale).
+ *   per_tensor     : 0 = one scale per block; 1 = one scale per whole tensor (all
+ *                    b, h, rows; every descale entry holds it) -- the per-tensor
+ *                    comparator; hadamard_signs must then be NULL.
+ */
+attn_status_t attn_fp8_quantize(const float* q, const float* k, const float* v,
+                                const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                uint8_t* v8, float* q_descale, float* k_descale,
+                                float* v_descale, int B, int H, int N, int d, int per_tensor,
+                                cudaStream_t stream);
+
+/*
+ * attn_fwd_fp8 -- FP8 e4m3 forward on the output of attn_fp8_quantize.
+ *   q8, k8, v8 : [B, H, N, d] e4m3; d must be 128.
+ *   *_descale  : [B, H, ceil(N/128)] float32 block descales.
+ *   o          : [B, H, N, d] bfloat16 (written); lse: [B, H, N] float32 (written).
+ * Scores use the block descales of their query and key blocks; the
+ * probabilities are rounded to e4m3 for the P V product.
+ */
+attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
+                           const float* q_descale, const float* k_descale,
+                           const float* v_descale, void* o, float* lse, int B, int H, int N,
+                           int d, int causal, float softmax_scale, cudaStream_t stream);
+
+/*
+ * attn_get_device_status -- synchronises `stream`, then reads and clears the
+ * current device's status word.  ATTN_OK, ATTN_ERR_TIMEOUT (a kernel gave up
+ * on an internal wait; attn_last_error() names the role), or ATTN_ERR_CUDA.
+ */
+attn_status_t attn_get_device_status(cudaStream_t stream);
+
+/* Static description of a status code. */
+const char* attn_status_string(attn_status_t s);
+
+/* Detail of the last error returned on this host thread ("" if none). */
+const char* attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

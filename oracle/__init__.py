@@ -15,12 +15,13 @@ forms, invariants, independent library routines, finite differences or
 hand-derived fixtures under ``tests/golden/``.  No function is parity-unpinned.
 """
 from .attention import (attention_forward, attention_backward, attention_probs,
+                        attention_forward_rows,
                         attention_forward_head, attention_backward_head)
 from .fp8 import (E4M3_MAX, e4m3_encode, e4m3_decode, sylvester_hadamard,
                   incoherent_transform, quantize_e4m3_blocks, dequantize_e4m3_blocks)
 
 __all__ = [
-    "attention_forward", "attention_backward", "attention_probs",
+    "attention_forward", "attention_backward", "attention_probs", "attention_forward_rows",
     "attention_forward_head", "attention_backward_head",
     "E4M3_MAX", "e4m3_encode", "e4m3_decode", "sylvester_hadamard",
     "incoherent_transform", "quantize_e4m3_blocks", "dequantize_e4m3_blocks",

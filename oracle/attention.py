@@ -121,3 +121,28 @@ def attention_backward(q, k, v, do, scale, causal=False):
             dq[b, h], dk[b, h], dv[b, h] = attention_backward_head(
                 q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
     return dq, dk, dv
+
+
+def attention_forward_rows(q, k, v, scale, causal, rows):
+    """O and L of selected query rows of one head ([N, d] inputs).
+
+    Row i of exact attention depends only on q_i and all of k, v, so the
+    selected rows are computed one at a time from the same definition; this is
+    how outputs of very large problems are spot-checked.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    rows = np.asarray(rows, dtype=np.int64)
+    o = np.empty((rows.size, v.shape[1]))
+    lse = np.empty(rows.size)
+    for n, i in enumerate(rows):
+        s = (k @ q[i]) * scale
+        if causal:
+            s[i + 1:] = -np.inf
+        m = s.max()
+        e = np.exp(s - m)
+        l = e.sum()
+        o[n] = (e / l) @ v
+        lse[n] = m + np.log(l)
+    return o, lse

@@ -1,0 +1,71 @@
+"""Helpers shared by the GPU parity tests (CUDA path vs the CPU oracle)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# Tolerances of the forward, LSE and gradient comparisons.
+FWD_MAX_ABS = 2e-2
+FWD_RMSE = 2e-3
+LSE_ABS = 1e-3
+GRAD_REL_RMSE = 5e-3
+FP8_RMSE = 3e-2
+
+
+def lib():
+    import exact_tiled_attention_25_gb300 as attn
+    from exact_tiled_attention_25_gb300 import build
+    build.build()
+    attn.load_library()
+    return attn
+
+
+def dev():
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def check_status(attn):
+    torch.cuda.synchronize()
+    code = attn.attn_get_device_status()
+    assert code == 0, f"device status {code}: {attn.attn_last_error()}"
+
+
+def fwd_errors(o_gpu, lse_gpu, o_ref, lse_ref):
+    o = o_gpu.float().cpu().numpy().astype(np.float64)
+    lse = lse_gpu.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    diff = o - o_ref
+    return (float(np.abs(diff).max()), float(np.sqrt(np.mean(diff ** 2))),
+            float(np.abs(lse - lse_ref).max()))
+
+
+def assert_fwd_close(o_gpu, lse_gpu, o_ref, lse_ref, max_abs=FWD_MAX_ABS, rmse=FWD_RMSE,
+                     lse_abs=LSE_ABS):
+    e_max, e_rmse, e_lse = fwd_errors(o_gpu, lse_gpu, o_ref, lse_ref)
+    assert e_max <= max_abs and e_rmse <= rmse and e_lse <= lse_abs, (e_max, e_rmse, e_lse)
+    return e_max, e_rmse, e_lse
+
+
+def rel_rmse(g_gpu, g_ref):
+    g = g_gpu.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(g))
+    return float(np.sqrt(np.mean((g - g_ref) ** 2)) / np.sqrt(np.mean(g_ref ** 2)))
+
+
+def guarded(shape, dtype, fill):
+    """A tensor view with sentinel bands of 4096 bytes before and after it;
+    returns (view, check) where check() asserts the bands are untouched."""
+    n = int(np.prod(shape))
+    esize = torch.empty((), dtype=dtype).element_size()
+    pad = 4096 // esize
+    buf = torch.full((n + 2 * pad,), fill, dtype=dtype, device=dev())
+    view = buf[pad:pad + n].view(shape)
+
+    def check():
+        torch.cuda.synchronize()
+        head = buf[:pad]
+        tail = buf[pad + n:]
+        same = (lambda t: torch.all(t == fill).item()) if dtype != torch.uint8 else \
+            (lambda t: torch.all(t == fill).item())
+        assert same(head) and same(tail), "write outside the output tensor"
+    return view, check

@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_tiled_attention_25_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for expected in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_fp8_quantize",
+                     "attn_fwd_fp8", "attn_get_device_status", "attn_status_string",
+                     "attn_last_error"):
+        assert expected in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.attn_status_string(code)
+    assert lib.attn_status_string(99) == b"unknown status"
+
+
+def test_workspace_size(lib):
+    B, H, N, d = 2, 16, 4096, 128
+    rows = B * H * N
+    expect = -(-rows * d * 4 // 256) * 256 + -(-rows * 4 // 256) * 256
+    assert lib.attn_bwd_workspace_size(B, H, N, d) == expect
+    assert lib.attn_bwd_workspace_size(0, 1, 1, 64) == 0
+
+
+def _fwd(lib, q=16, k=16, v=16, o=16, l=16, B=1, H=1, N=128, d=128, causal=0, scale=0.1, dt=0):
+    return lib.attn_fwd(q, k, v, o, l, B, H, N, d, causal, scale, dt, None)
+
+
+@pytest.mark.parametrize("kwargs,why", [
+    (dict(d=96), "d"),
+    (dict(d=0), "d"),
+    (dict(N=0), "N"),
+    (dict(B=-1), "B"),
+    (dict(causal=2), "causal"),
+    (dict(scale=0.0), "scale"),
+    (dict(scale=float("inf")), "scale"),
+    (dict(q=0), "null"),
+    (dict(v=8), "aligned"),
+    (dict(dt=7), "dtype"),
+    (dict(B=65536, H=256, N=256, d=128), "2^31"),
+])
+def test_fwd_rejects_bad_arguments_without_a_gpu(lib, kwargs, why):
+    assert _fwd(lib, **kwargs) == 1          # ATTN_ERR_INVALID_ARG
+    assert why.lower() in lib.attn_last_error().decode().lower()
+
+
+def test_bwd_rejects_small_workspace(lib):
+    ws = lib.attn_bwd_workspace_size(1, 1, 128, 64)
+    code = lib.attn_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, 256, ws - 1,
+                        1, 1, 128, 64, 0, 0.125, 0, None)
+    assert code == 1 and b"workspace" in lib.attn_last_error()
+    code = lib.attn_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, 16, ws,
+                        1, 1, 128, 64, 0, 0.125, 0, None)
+    assert code == 1 and b"256-byte" in lib.attn_last_error()
+
+
+def test_fp8_quantize_rejects_bad_modes(lib):
+    code = lib.attn_fp8_quantize(16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 1, 128, 128, 1, None)
+    assert code == 1 and b"per-tensor" in lib.attn_last_error()
+    code = lib.attn_fp8_quantize(16, 16, 16, None, 16, 16, 16, 16, 16, 16, 1, 1, 128, 128, 3, None)
+    assert code == 1
+
+
+def test_unsupported_shapes_are_reported(lib):
+    ws = lib.attn_bwd_workspace_size(1, 1, 128, 256)
+    code = lib.attn_bwd(16, 16, 16, 16, 16, 16, 16, 16, 16, 256, ws,
+                        1, 1, 128, 256, 0, 0.1, 0, None)
+    assert code == 2                          # ATTN_ERR_UNSUPPORTED
+    code = lib.attn_fwd_fp8(16, 16, 16, 16, 16, 16, 16, 16, 1, 1, 128, 64, 0, 0.1, None)
+    assert code == 2
+
+
+def test_device_check_fails_loudly_without_a_gpu(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid arguments reach the device check, which must fail, not fall back
+    code = _fwd(lib)
+    assert code in (3, 4)

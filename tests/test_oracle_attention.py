@@ -207,3 +207,19 @@ def test_planted_mistakes_are_caught():
     assert not np.allclose((p * (dp - row)).T @ q, tk.grad.numpy(), atol=1e-6)
     # a transposed P in dV
     assert not np.allclose(p @ do, tv.grad.numpy(), atol=1e-6)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_sampler_matches_full_head(causal):
+    """The row-by-row oracle used for spot checks equals the batched one and
+    torch SDPA on every row."""
+    rng = np.random.default_rng(9)
+    N, d = 70, 16
+    q, k, v = (rng.standard_normal((N, d)) for _ in range(3))
+    rows = np.array([0, 1, 33, 69])
+    o_r, l_r = oracle.attention_forward_rows(q, k, v, 0.3, causal, rows)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        *(torch.from_numpy(x)[None, None] for x in (q, k, v)), is_causal=causal, scale=0.3)[0, 0]
+    np.testing.assert_allclose(o_r, ref.numpy()[rows], atol=1e-12)
+    _, l_full = oracle.attention_forward_head(q, k, v, 0.3, causal)
+    np.testing.assert_allclose(l_r, l_full[rows], atol=1e-12)
