@@ -1,0 +1,405 @@
+"""Benchmark of the attention hot path on GB300.
+
+One step = one pass of every stage of the path over the long-context workload
+B=2, H=16, N=8192, d=128 (16K tokens, the 8K/128 shape):
+  1. BF16 forward              (attn_fwd)
+  2. BF16 backward             (attn_bwd: row-dot pre-pass, main kernel, dQ conversion)
+  3. FP8 pre-pass              (attn_fp8_quantize: block scales + Hadamard on Q, K)
+  4. FP8 forward               (attn_fwd_fp8)
+Inputs are seeded synthetic N(0,1) tensors resident in HBM before timing;
+together they are larger than the 129 MB L2, so no explicit flush is done.
+
+value = algorithmic TFLOP per step / step time, with forward FLOP =
+4*B*H*N^2*d (halved if causal), backward = 2.5x forward, FP8 forward = forward.
+The pre-pass does no tensor-core work and is reported in GB/s.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--causal] [--impl reference]
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas, weak scaling); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+B, H, N, D = 2, 16, 8192, 128
+METRIC = "Attn fwd/bwd TFLOP/s (BF16, FP8) & % of GB300 dense tensor peak, N=8K d=128"
+WORKLOAD = "attention step (bf16 fwd + bf16 bwd + fp8 pre-pass + fp8 fwd), B=2 H=16 N=8192 d=128"
+
+# DRAM bytes per launch of each kernel from the ncu capture summarised in
+# profiles/ (None until a capture of the current kernel exists).
+NCU_TRAFFIC = {}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def fwd_flop(causal):
+    f = 4.0 * B * H * N * N * D
+    return f / 2 if causal else f
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].strip().lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].strip() not in ("", "[N/A]"))}
+
+
+def make_inputs(torch, dev, seed=3):
+    g = torch.Generator(device=dev).manual_seed(seed)
+    shape = (B, H, N, D)
+    q, k, v, do = (torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+                   for _ in range(4))
+    signs = torch.where(torch.rand(D, generator=g, device=dev) < 0.5, -1.0, 1.0).float()
+    return q, k, v, do, signs
+
+
+def run_ours(args, rank, world):
+    import torch
+    import exact_tiled_attention_25_gb300 as attn
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    attn.load_library()
+    stream = torch.cuda.current_stream()
+    causal = args.causal
+    scale = 1.0 / math.sqrt(D)
+    q32, k32, v32, do32, signs = make_inputs(torch, dev)
+    q, k, v, do = (t.to(torch.bfloat16) for t in (q32, k32, v32, do32))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(attn.attn_bwd_workspace_size(B, H, N, D), dtype=torch.uint8, device=dev)
+    nblk = (N + 127) // 128
+    q8, k8, v8 = (torch.empty((B, H, N, D), dtype=torch.uint8, device=dev) for _ in range(3))
+    qs, ks, vs = (torch.empty((B, H, nblk), dtype=torch.float32, device=dev) for _ in range(3))
+    o8 = torch.empty_like(q)
+    lse8 = torch.empty_like(lse)
+
+    parts = {}
+
+    def part_fwd():
+        attn.attn_fwd(q, k, v, causal=causal, softmax_scale=scale, o=o, lse=lse)
+
+    def part_bwd():
+        attn.attn_bwd(q, k, v, o, do, lse, causal=causal, softmax_scale=scale,
+                      dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    def part_quant():
+        lib = attn.load_library()
+        code = lib.attn_fp8_quantize(q32.data_ptr(), k32.data_ptr(), v32.data_ptr(),
+                                     signs.data_ptr(), q8.data_ptr(), k8.data_ptr(),
+                                     v8.data_ptr(), qs.data_ptr(), ks.data_ptr(), vs.data_ptr(),
+                                     B, H, N, D, 0, stream.cuda_stream)
+        if code:
+            raise attn.AttnError(code, "attn_fp8_quantize")
+
+    def part_fp8():
+        attn.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=causal, softmax_scale=scale,
+                          o=o8, lse=lse8)
+
+    candidates = [("fwd_bf16", part_fwd, fwd_flop(causal), 1),
+                  ("bwd_bf16", part_bwd, 2.5 * fwd_flop(causal), 3),
+                  ("fp8_prepass", part_quant, 0.0, 1),
+                  ("fwd_fp8", part_fp8, fwd_flop(causal), 1)]
+    step_parts = []
+    skipped = []
+    for name, fn, flop, launches in candidates:
+        try:
+            fn()
+            torch.cuda.synchronize()
+            step_parts.append((name, fn, flop, launches))
+        except attn.AttnError as e:
+            if e.code != attn.ATTN_ERR_UNSUPPORTED:
+                raise
+            skipped.append(name)
+    assert attn.attn_get_device_status() == 0, attn.attn_last_error()
+
+    # prepass algorithmic bytes: read 3 fp32 tensors, write 3 e4m3 tensors + descales
+    prepass_bytes = 3 * B * H * N * D * (4 + 1) + 3 * B * H * nblk * 4
+
+    for _ in range(args.warmup):
+        for _, fn, _, _ in step_parts:
+            fn()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ev = {name: [] for name, *_ in step_parts}
+    step_start = torch.cuda.Event(enable_timing=True)
+    step_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clocks:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        step_start.record(stream)
+        for _ in range(args.steps):
+            for name, fn, _, _ in step_parts:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ev[name].append((a, b))
+        step_end.record(stream)
+        torch.cuda.synchronize()
+    total_ms = step_start.elapsed_time(step_end)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert attn.attn_get_device_status() == 0, attn.attn_last_error()
+    ms_per_step = total_ms / args.steps
+    step_flop = sum(f for _, _, f, _ in step_parts)
+    value = world * step_flop / (ms_per_step * 1e-3) / 1e12
+
+    pk = peaks()
+    bf16_peak = pk["bf16_tflops_sustained"]
+    fp8_peak = 2.0 * bf16_peak     # nominal fp8:bf16 dense ratio 2
+    breakdown = {}
+    for name, _, flop, _ in step_parts:
+        times = [a.elapsed_time(b) for a, b in ev[name]]
+        avg = sum(times) / len(times)
+        entry = {"ms": round(avg, 4), "share": round(sum(times) / total_ms, 4)}
+        if flop:
+            tf = flop / (avg * 1e-3) / 1e12
+            peak = fp8_peak if name == "fwd_fp8" else bf16_peak
+            entry.update(tflops=round(tf, 1), frac_of_peak=round(tf / peak, 4))
+        else:
+            gbs = prepass_bytes / (avg * 1e-3) / 1e9
+            entry.update(gbs=round(gbs, 1), frac_of_hbm=round(gbs / pk["hbm_gbs"], 4))
+        breakdown[name] = entry
+
+    dominant = max(breakdown, key=lambda n: breakdown[n]["ms"])
+    dflop = dict((n, f) for n, _, f, _ in step_parts)[dominant]
+    if dflop:
+        roof = {"bound": "tensor", "achieved": breakdown[dominant]["tflops"],
+                "peak": fp8_peak if dominant == "fwd_fp8" else bf16_peak, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": breakdown[dominant]["gbs"], "peak": pk["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["kernel"] = dominant
+    roof["traffic"] = NCU_TRAFFIC.get(dominant)
+    roof["peak_source"] = f"{pk['source']} (bf16 sustained; fp8 = 2x bf16)"
+
+    e2e = run_e2e(args, torch, attn, dev, stream, step_parts, causal, scale, q32, k32, v32,
+                  do32, signs)
+    launches = sum(l for _, _, _, l in step_parts) * args.steps
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16+e4m3 (fp32 accumulate)", "data": "synthetic N(0,1), seeded",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D, "causal": causal,
+                   "global_batch": B * world, "seq_len": N, "parallelism": f"replicas{world}",
+                   "step": [n for n, *_ in step_parts], "not_built": skipped,
+                   "l2": "no flush: Q/K/V/dO/O (bf16) + fp32 pre-pass inputs exceed the 129 MB L2"},
+        "breakdown": breakdown,
+        "roofline": roof,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "gpu_launches": launches,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, torch, attn, dev, stream, step_parts, causal, scale, q32, k32, v32, do32,
+            signs):
+    """The same step through the public API with inputs in pinned host memory:
+    host-to-device copies of the inputs and device-to-host copies of every
+    output are inside the timed region."""
+    names = [n for n, *_ in step_parts]
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = {"q": pin(q32.to(torch.bfloat16)), "k": pin(k32.to(torch.bfloat16)),
+            "v": pin(v32.to(torch.bfloat16)), "do": pin(do32.to(torch.bfloat16))}
+    if "fp8_prepass" in names:
+        h_in.update(q32=pin(q32), k32=pin(k32), v32=pin(v32), signs=pin(signs))
+    d_in = {k_: torch.empty_like(t, device=dev) for k_, t in h_in.items()}
+    outs = {}
+
+    def step():
+        for k_, t in h_in.items():
+            d_in[k_].copy_(t, non_blocking=True)
+        res = []
+        o, lse = attn.attn_fwd(d_in["q"], d_in["k"], d_in["v"], causal=causal,
+                               softmax_scale=scale)
+        res += [o, lse]
+        if "bwd_bf16" in names:
+            res += list(attn.attn_bwd(d_in["q"], d_in["k"], d_in["v"], o, d_in["do"], lse,
+                                      causal=causal, softmax_scale=scale))
+        if "fp8_prepass" in names:
+            (q8, k8, v8), (qs, ks, vs) = attn.attn_fp8_quantize(d_in["q32"], d_in["k32"],
+                                                                d_in["v32"], d_in["signs"])
+            if "fwd_fp8" in names:
+                res += list(attn.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=causal,
+                                              softmax_scale=scale))
+        for i, t in enumerate(res):
+            if i not in outs:
+                outs[i] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            outs[i].copy_(t, non_blocking=True)
+        return res
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    flop = sum(f for _, _, f, _ in step_parts)
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    return {"value": round(flop / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def cpu_sample_problem(seed=3):
+    """One head of the timed workload (N=8192, d=128), float64 on the host."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    return [rng.standard_normal((N, D)) for _ in range(4)]
+
+
+def cpu_baseline(args, heads=1):
+    """The CPU oracle as it stands, on a bounded sample of the workload: the
+    forward and backward of `heads` head(s) at N=8192, d=128."""
+    import oracle
+    q, k, v, do = cpu_sample_problem()
+    scale = 1.0 / math.sqrt(D)
+    t0 = time.perf_counter()
+    for _ in range(heads):
+        oracle.attention_forward_head(q, k, v, scale, args.causal)
+        oracle.attention_backward_head(q, k, v, do, scale, args.causal)
+    dt = time.perf_counter() - t0
+    flop = heads * 3.5 * 4.0 * N * N * D / (2 if args.causal else 1)
+    threads = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max(i.get("num_threads", 0) for i in threadpool_info()) or threads
+    except Exception:
+        pass
+    return {"value": round(flop / dt / 1e12, 5), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{heads} head(s) of the workload, forward + backward, float64 NumPy"}
+
+
+def run_reference(args, rank):
+    """The CPU oracle timed as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    q, k, v, do = cpu_sample_problem()
+    scale = 1.0 / math.sqrt(D)
+    for _ in range(args.warmup):
+        oracle.attention_forward_head(q[:256], k, v, scale, args.causal)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention_forward_head(q, k, v, scale, args.causal)
+        oracle.attention_backward_head(q, k, v, do, scale, args.causal)
+    dt = time.perf_counter() - t0
+    flop = args.steps * 3.5 * 4.0 * N * N * D / (2 if args.causal else 1)
+    value = flop / dt / 1e12
+    threads = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic N(0,1), seeded",
+            "config": {"workload": WORKLOAD + " -- oracle sample: one head fwd+bwd per step",
+                       "B": B, "H": H, "N": N, "d": D, "causal": args.causal},
+            "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": "one head (N=8192, d=128) forward + backward per step"},
+            "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if args.steps < 1:
+            raise SystemExit("--steps must be >= 1")
+        run_reference(args, rank)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    run_ours(args, rank, world)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -162,8 +162,7 @@ const char* attn_last_error(void) { return g_last_error.c_str(); }
 
 size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * N;
-  return align_up(rows * d * sizeof(float), 256) + align_up(rows * sizeof(float), 256);
+  return bwd_workspace_layout(B, H, N, d).total;
 }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -199,12 +198,11 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
     return fail(ATTN_ERR_INVALID_ARG, "workspace smaller than attn_bwd_workspace_size()");
   if (d == 256) return fail(ATTN_ERR_UNSUPPORTED, "the backward pass supports d = 64 and 128");
   if ((s = check_device()) != ATTN_OK) return s;
-  const size_t rows = static_cast<size_t>(B) * H * N;
-  float* dq_acc = static_cast<float*>(workspace);
-  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                          align_up(rows * d * sizeof(float), 256));
-  BwdParams p{q, k, v, o, dout, lse, dq, dk, dv, dq_acc, delta, B, H, N, d, causal,
-              softmax_scale, dtype == ATTN_FP16 ? 1 : 0};
+  const BwdWorkspace w = bwd_workspace_layout(B, H, N, d);
+  char* ws = static_cast<char*>(workspace);
+  BwdParams p{q, k, v, o, dout, lse, dq, dk, dv, reinterpret_cast<float*>(ws + w.dq_acc),
+              reinterpret_cast<float*>(ws + w.lse2), reinterpret_cast<float*>(ws + w.delta),
+              B, H, N, d, causal, softmax_scale, dtype == ATTN_FP16 ? 1 : 0};
   return launch_bwd(p, stream);
 }
 

@@ -1,8 +1,541 @@
-// BF16/FP16 attention backward (placeholder until the kernels land).
+// BF16/FP16 attention backward on sm_103a.
+//
+// Method: "FlashAttention-3: Hopper Asynchrony and FP8 Attention", section
+// "Backward warp specialization": producers load K_j and V_j, then stream Q_i
+// and dO_i; consumers recompute S and P from the stored L_i, form dP, dS, dV
+// and dK; a separate writer adds each local dQ tile into global dQ.  The
+// gradient formulas are the chain rule through softmax:
+//   P = exp(scale * Q K^T - L),  dV = P^T dO,  dP = dO V^T,
+//   dS = P * (dP - D) with D_i = rowsum(dO_i * O_i),
+//   dQ = scale * dS K,  dK = scale * dS^T Q.
+//
+// Three kernels:
+//  1. prep: D = rowsum(dO * O) and L * log2(e) into 128-row padded arrays
+//     (padding: D = 0, L = +inf, so padded query rows get P = 0), and the
+//     float32 dQ accumulator is zeroed.
+//  2. main: one CTA per (key/value tile j, head, batch).  K_j and V_j stay in
+//     shared memory; dK_j and dV_j accumulate in tensor memory.  Per query tile
+//     i (causal: i >= j) the MMA thread issues, on tcgen05,
+//        dP^T = V_j dO_i^T        S^T = K_j Q_i^T
+//     the compute warpgroup (thread = key row) forms P^T and dS^T in registers
+//     and writes them back to tensor memory (operands of the next two MMAs)
+//     and dS^T to shared memory (operand of the third),
+//        dV += P^T dO_i           dK += dS^T Q_i          dQ_i = dS K_j
+//     and the reduce warpgroup (thread = query row) reads dQ_i from tensor
+//     memory and adds it into the float32 accumulator with vector reductions.
+//  3. convert: dQ = scale * accumulator, rounded to the 16-bit type.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+
 #include "common.h"
+#include "sm103_prims.cuh"
 
 namespace attn {
-attn_status_t launch_bwd(const BwdParams&, cudaStream_t) {
-  return fail(ATTN_ERR_UNSUPPORTED, "backward pass not built yet");
+namespace {
+
+constexpr int kSmemLimit = 232448;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BM = 128;                 // query rows per step
+  static constexpr int BN = 128;                 // keys per CTA
+  static constexpr int CH = D / 64;              // 128-byte chunks per row
+  static constexpr int CHUNK = 128 * 128;        // one 128-row x 128-byte chunk
+  static constexpr int TILE = 128 * D * 2;       // a K, V, Q or dO tile
+  static constexpr int NST = 2;                  // Q/dO ring stages
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TILE;
+  static constexpr int OFF_RING = 2 * TILE;      // stage s: Q at +2*TILE*s, dO at +TILE
+  static constexpr int OFF_DS = OFF_RING + NST * 2 * TILE;   // dS^T, 128 keys x 128 queries
+  static constexpr int OFF_LD = OFF_DS + 2 * CHUNK;           // per stage: L*log2e[128], D[128]
+  static constexpr int OFF_BAR = OFF_LD + NST * 1024;
+  static constexpr int NEED = OFF_BAR + 256;
+  static constexpr int SMEM_BYTES = cmin(kSmemLimit, NEED + 1024);
+  static constexpr int SLACK = SMEM_BYTES - NEED;   // room to align the base to 1024
+  static constexpr bool DQ_ALIAS = (D == 128);      // dQ shares columns with S^T
+  static constexpr uint32_t S_COL = 0;
+  static constexpr uint32_t DP_COL = 128;
+  static constexpr uint32_t DV_COL = 256;
+  static constexpr uint32_t DK_COL = 256 + D;
+  static constexpr uint32_t DQ_COL = DQ_ALIAS ? 0 : 256 + 2 * D;
+  static constexpr int THREADS = 320;            // compute WG, reduce WG, load warp, MMA warp
+  static constexpr int LOAD_WARP = 8;
+  static constexpr int MMA_WARP = 9;
+  static_assert(DQ_COL + D <= 512 && DK_COL + D <= 512, "TMEM overflow");
+  static_assert(SLACK >= 0, "shared memory overflow");
+};
+
+struct Bars {
+  uint64_t kv_full;
+  uint64_t stage_full[2];
+  uint64_t stage_empty[2];
+  uint64_t s_full;
+  uint64_t p_full;
+  uint64_t dq_full;
+  uint64_t dq_free;
+  uint64_t ds_free;
+  uint64_t dkv_full;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int load_items;
+};
+
+struct BwdKParams {
+  void* dk;
+  void* dv;
+  float* dq_acc;
+  const float* lse2;    // L * log2(e), [B*H][Npad], +inf padding
+  const float* delta;   // rowsum(dO * O), [B*H][Npad], 0 padding
+  int* status;
+  int N;
+  int Npad;
+  int H;
+  float scale;
+  float scale_log2;
+};
+
+// ------------------------------------------------------------------ prep ----
+// One group of D/8 lanes per row; each lane holds 8 consecutive elements.
+template <int D, bool FP16>
+__global__ void __launch_bounds__(256)
+    bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                    const float* __restrict__ lse, float* __restrict__ lse2,
+                    float* __restrict__ delta, float* __restrict__ dq_acc, int N, int Npad,
+                    long long total_rows_pad) {
+  constexpr int L = D / 8;
+  constexpr int ROWS_PER_WARP = 32 / L;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / L;
+  const int li = lane % L;
+  const long long warp_global = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const long long prow = warp_global * ROWS_PER_WARP + sub;   // padded row index
+  if (prow >= total_rows_pad) return;
+  const long long bh = prow / Npad;
+  const int n = static_cast<int>(prow - bh * Npad);
+  float acc = 0.f;
+  if (n < N) {
+    const long long row = bh * N + n;
+    const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[li];
+    const uint4 b = reinterpret_cast<const uint4*>(dout + row * D)[li];
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float2 fa, fb;
+      if (FP16) {
+        fa = __half22float2(*reinterpret_cast<const __half2*>(&av[e]));
+        fb = __half22float2(*reinterpret_cast<const __half2*>(&bv[e]));
+      } else {
+        fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
+        fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv[e]));
+      }
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+    float4* z = reinterpret_cast<float4*>(dq_acc + row * D) + 2 * li;
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int off = L / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (li == 0) {
+    delta[prow] = (n < N) ? acc : 0.f;
+    lse2[prow] = (n < N) ? lse[bh * N + n] * kLog2e : INFINITY;
+  }
 }
+
+// --------------------------------------------------------------- convert ----
+template <bool FP16>
+__global__ void __launch_bounds__(256)
+    bwd_convert_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq, float scale,
+                       long long n8) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    uint4 r;
+    if (FP16) {
+      r.x = cvt_pack_f16(a.x * scale, a.y * scale);
+      r.y = cvt_pack_f16(a.z * scale, a.w * scale);
+      r.z = cvt_pack_f16(b.x * scale, b.y * scale);
+      r.w = cvt_pack_f16(b.z * scale, b.w * scale);
+    } else {
+      r.x = cvt_pack_bf16(a.x * scale, a.y * scale);
+      r.y = cvt_pack_bf16(a.z * scale, a.w * scale);
+      r.z = cvt_pack_bf16(b.x * scale, b.y * scale);
+      r.w = cvt_pack_bf16(b.z * scale, b.w * scale);
+    }
+    reinterpret_cast<uint4*>(dq)[i] = r;
+  }
+}
+
+// ------------------------------------------------------------------ main ----
+template <int D, bool CAUSAL, bool FP16>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const BwdKParams kp) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+  if (pad > static_cast<uint32_t>(C::SLACK)) {
+    // Cannot place the swizzled tiles: report and leave before touching anything.
+    if (threadIdx.x == 0) atomicCAS(kp.status, 0, kDevSmemMisaligned);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
+  Bars& bars = *reinterpret_cast<Bars*>(smem + C::OFF_BAR);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int j = blockIdx.x;
+  const int bh = blockIdx.z * kp.H + blockIdx.y;
+  const int N = kp.N;
+  const int nQ = (N + C::BM - 1) / C::BM;
+  const int i0 = CAUSAL ? j : 0;
+  const int nsteps = nQ - i0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars.kv_full, 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&bars.stage_full[s], 1);
+      mbar_init(&bars.stage_empty[s], 1);
+    }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.p_full, 128);
+    mbar_init(&bars.dq_full, 1);
+    mbar_init(&bars.dq_free, 128);
+    mbar_init(&bars.ds_free, 1);
+    mbar_init(&bars.dkv_full, 1);
+    mbar_init(&bars.drain, 1);
+    bars.abort_flag = 0;
+    bars.load_items = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = bars.tmem_base;
+  const Abort ab{&bars.abort_flag, kp.status};
+
+  if (warp == C::LOAD_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmDO);
+      mbar_arrive_expect_tx(&bars.kv_full, 2 * C::TILE);
+#pragma unroll
+      for (int c = 0; c < C::CH; ++c) {
+        tma_load_3d(smem + C::OFF_K + c * C::CHUNK, &tmK, &bars.kv_full, c * 64, j * C::BN, bh);
+        tma_load_3d(smem + C::OFF_V + c * C::CHUNK, &tmV, &bars.kv_full, c * 64, j * C::BN, bh);
+      }
+      int n = 0;
+      for (; n < nsteps; ++n) {
+        const int st = n % C::NST;
+        const int use = n / C::NST;
+        if (use >= 1 && !mbar_wait(&bars.stage_empty[st], (use - 1) & 1, ab, kDevTimeoutLoad))
+          break;
+        const int i = i0 + n;
+        uint8_t* sq = smem + C::OFF_RING + st * 2 * C::TILE;
+        uint8_t* sdo = sq + C::TILE;
+        float* sld = reinterpret_cast<float*>(smem + C::OFF_LD + st * 1024);
+        mbar_arrive_expect_tx(&bars.stage_full[st], 2 * C::TILE + 1024);
+#pragma unroll
+        for (int c = 0; c < C::CH; ++c) {
+          tma_load_3d(sq + c * C::CHUNK, &tmQ, &bars.stage_full[st], c * 64, i * C::BM, bh);
+          tma_load_3d(sdo + c * C::CHUNK, &tmDO, &bars.stage_full[st], c * 64, i * C::BM, bh);
+        }
+        const size_t roff = static_cast<size_t>(bh) * kp.Npad + static_cast<size_t>(i) * C::BM;
+        bulk_load(sld, kp.lse2 + roff, 512, &bars.stage_full[st]);
+        bulk_load(sld + 128, kp.delta + roff, 512, &bars.stage_full[st]);
+      }
+      bars.load_items = n;
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr Elt E = FP16 ? Elt::F16 : Elt::BF16;
+      constexpr uint32_t idSP = idesc_f16(E, 128, 128, false, false);   // S^T and dP^T
+      constexpr uint32_t idKV = idesc_f16(E, 128, D, false, true);      // dV and dK (A in TMEM)
+      constexpr uint32_t idQ = idesc_f16(E, 128, D, true, true);        // dQ (A = dS from smem)
+      const uint32_t sK = smem_u32(smem + C::OFF_K);
+      const uint32_t sV = smem_u32(smem + C::OFF_V);
+      const uint32_t sDS = smem_u32(smem + C::OFF_DS);
+      bool ok = mbar_wait(&bars.kv_full, 0, ab, kDevTimeoutMma);
+      for (int n = 0; n < nsteps && ok; ++n) {
+        const int st = n % C::NST;
+        if (!(ok = mbar_wait(&bars.stage_full[st], (n / C::NST) & 1, ab, kDevTimeoutMma))) break;
+        tc_fence_after_sync();
+        const uint32_t sQ = smem_u32(smem + C::OFF_RING + st * 2 * C::TILE);
+        const uint32_t sDO = sQ + C::TILE;
+        // dP^T = V_j dO_i^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
+          mma_f16_ss(tmem + C::DP_COL, sdesc_sw128(sV + off, 16, 1024),
+                     sdesc_sw128(sDO + off, 16, 1024), idSP, kk > 0 ? 1u : 0u);
+        }
+        // S^T = K_j Q_i^T (when dQ shares these columns, wait until the last dQ was read)
+        if (C::DQ_ALIAS && n > 0) {
+          if (!(ok = mbar_wait(&bars.dq_free, (n - 1) & 1, ab, kDevTimeoutMma))) break;
+          tc_fence_after_sync();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
+          mma_f16_ss(tmem + C::S_COL, sdesc_sw128(sK + off, 16, 1024),
+                     sdesc_sw128(sQ + off, 16, 1024), idSP, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars.s_full);
+        if (!(ok = mbar_wait(&bars.p_full, n & 1, ab, kDevTimeoutMma))) break;
+        tc_fence_after_sync();
+        // dV += P^T dO_i ; dK += dS^T Q_i   (A operands from tensor memory)
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk) {
+          const uint64_t bdo = sdesc_sw128(sDO + kk * 16 * 128, C::CHUNK, 1024);
+          mma_f16_ts(tmem + C::DV_COL, tmem + C::S_COL + kk * 8, bdo, idKV,
+                     (n > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk) {
+          const uint64_t bq = sdesc_sw128(sQ + kk * 16 * 128, C::CHUNK, 1024);
+          mma_f16_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8, bq, idKV,
+                     (n > 0 || kk > 0) ? 1u : 0u);
+        }
+        // dQ_i = dS K_j   (A = dS^T in shared memory read MN-major)
+        if (!C::DQ_ALIAS && n > 0) {
+          if (!(ok = mbar_wait(&bars.dq_free, (n - 1) & 1, ab, kDevTimeoutMma))) break;
+          tc_fence_after_sync();
+        }
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          const uint64_t ads = sdesc_sw128(sDS + kk * 16 * 128, C::CHUNK, 1024);
+          const uint64_t bk = sdesc_sw128(sK + kk * 16 * 128, C::CHUNK, 1024);
+          mma_f16_ss(tmem + C::DQ_COL, ads, bk, idQ, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars.dq_full);
+        if (n + 1 < nsteps) mma_commit(&bars.ds_free);
+        if (n + C::NST < nsteps) mma_commit(&bars.stage_empty[st]);
+      }
+      if (ok) mma_commit(&bars.dkv_full);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ compute WG
+    const int k = threadIdx.x;                       // key row of the tile = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const int key_g = j * C::BN + k;
+    const bool key_ok = key_g < N;
+    const float c2 = kp.scale_log2;
+    const uint32_t sDSrow = smem_u32(smem + C::OFF_DS) + k * 128;
+    bool ok = true;
+    for (int n = 0; n < nsteps; ++n) {
+      const int st = n % C::NST;
+      const int i = i0 + n;
+      if (!(ok = mbar_wait(&bars.s_full, n & 1, ab, kDevTimeoutSoftmax))) break;
+      if (n > 0 && !(ok = mbar_wait(&bars.ds_free, (n - 1) & 1, ab, kDevTimeoutSoftmax))) break;
+      tc_fence_after_sync();
+      const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_LD + st * 1024);
+      const float* dvec = lse2 + 128;
+      const bool diag = CAUSAL && i == j;
+#pragma unroll
+      for (int c0 = 0; c0 < C::BM / 32; ++c0) {
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(tmem + lane_addr + C::S_COL + c0 * 32, sv);
+        tmem_ld32(tmem + lane_addr + C::DP_COL + c0 * 32, dpv);
+        tmem_ld_wait();
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int q0 = c0 * 32 + e;
+          float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), c2, -lse2[q0]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), c2, -lse2[q0 + 1]));
+          if (diag) {
+            if (k > q0) p0 = 0.f;
+            if (k > q0 + 1) p1 = 0.f;
+          }
+          if (!key_ok) {
+            p0 = 0.f;
+            p1 = 0.f;
+          }
+          const float ds0 = p0 * (__uint_as_float(dpv[e]) - dvec[q0]);
+          const float ds1 = p1 * (__uint_as_float(dpv[e + 1]) - dvec[q0 + 1]);
+          pp[e / 2] = FP16 ? cvt_pack_f16(p0, p1) : cvt_pack_bf16(p0, p1);
+          dd[e / 2] = FP16 ? cvt_pack_f16(ds0, ds1) : cvt_pack_bf16(ds0, ds1);
+        }
+        tmem_st16(tmem + lane_addr + C::S_COL + c0 * 16, pp);
+        tmem_st16(tmem + lane_addr + C::DP_COL + c0 * 16, dd);
+        // dS^T row k, queries [32 c0, 32 c0 + 32): chunk c0 / 2, 16-byte pieces
+        // (c0 % 2) * 4 .. + 3, placed with the 128-byte swizzle.
+        const uint32_t base = sDSrow + (c0 / 2) * C::CHUNK;
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {
+          const uint32_t piece = static_cast<uint32_t>((c0 % 2) * 4 + pc);
+          st_shared_v4(base + ((piece ^ (k & 7)) * 16), dd[4 * pc], dd[4 * pc + 1],
+                       dd[4 * pc + 2], dd[4 * pc + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(&bars.p_full);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && mbar_wait(&bars.dkv_full, 0, ab, kDevTimeoutEpilogue)) {
+      tc_fence_after_sync();
+      uint16_t* dvrow = static_cast<uint16_t*>(kp.dv) + (static_cast<size_t>(bh) * N + key_g) * D;
+      uint16_t* dkrow = static_cast<uint16_t*>(kp.dk) + (static_cast<size_t>(bh) * N + key_g) * D;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which ? C::DK_COL : C::DV_COL;
+        const float mul = which ? kp.scale : 1.f;
+        uint16_t* dst_row = which ? dkrow : dvrow;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D / 32; ++c0) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_addr + col + c0 * 32, v);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a = __uint_as_float(v[2 * e]) * mul;
+            const float b = __uint_as_float(v[2 * e + 1]) * mul;
+            pk[e] = FP16 ? cvt_pack_f16(a, b) : cvt_pack_bf16(a, b);
+          }
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + c0 * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ reduce WG
+    const int q = threadIdx.x - 128;                 // query row of the tile = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    for (int n = 0; n < nsteps; ++n) {
+      if (!mbar_wait(&bars.dq_full, n & 1, ab, kDevTimeoutReduce)) break;
+      tc_fence_after_sync();
+      uint32_t v[D];
+#pragma unroll
+      for (int c0 = 0; c0 < D / 32; ++c0)
+        tmem_ld32(tmem + lane_addr + C::DQ_COL + c0 * 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(&v[c0 * 32]));
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars.dq_free);
+      const int q_g = (i0 + n) * C::BM + q;
+      if (q_g < N) {
+        float* dst = kp.dq_acc + (static_cast<size_t>(bh) * N + q_g) * D;
+#pragma unroll
+        for (int e = 0; e < D; e += 4)
+          red_add_v4(dst + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                     __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (bars.abort_flag) {
+    if (warp == C::LOAD_WARP && lane == 0) {
+      mbar_wait_drain(&bars.kv_full, 0);
+      const int issued = bars.load_items;
+      for (int s = 0; s < C::NST && s < issued; ++s)
+        mbar_wait_drain(&bars.stage_full[s], ((issued - 1 - s) / C::NST) & 1);
+    }
+    if (warp == C::MMA_WARP && lane == 0) {
+      mma_commit(&bars.drain);
+      mbar_wait_drain(&bars.drain, 0);
+    }
+    __syncthreads();
+  }
+  if (warp == C::MMA_WARP) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool FP16>
+attn_status_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  const int Npad = (p.N + 127) / 128 * 128;
+  const long long rows_pad = static_cast<long long>(p.B) * p.H * Npad;
+  // 1. prep
+  {
+    constexpr int rows_per_block = 8 * (32 / (D / 8));
+    const long long blocks = (rows_pad + rows_per_block - 1) / rows_per_block;
+    bwd_prep_kernel<D, FP16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.lse, p.lse2,
+        p.delta, p.dq_acc, p.N, Npad, rows_pad);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e, "backward prep launch");
+  }
+  // 2. main
+  {
+    auto kern = bwd_main_kernel<D, CAUSAL, FP16>;
+    attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
+    if (s != ATTN_OK) return s;
+    CUtensorMap tq, tk, tv, tdo;
+    const uint64_t planes = static_cast<uint64_t>(p.B) * p.H;
+    if ((s = make_tmap_3d(&tq, p.q, 2, D, p.N, planes, 64, 128)) != ATTN_OK) return s;
+    if ((s = make_tmap_3d(&tk, p.k, 2, D, p.N, planes, 64, 128)) != ATTN_OK) return s;
+    if ((s = make_tmap_3d(&tv, p.v, 2, D, p.N, planes, 64, 128)) != ATTN_OK) return s;
+    if ((s = make_tmap_3d(&tdo, p.dout, 2, D, p.N, planes, 64, 128)) != ATTN_OK) return s;
+    int* status = device_status_word();
+    if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
+    BwdKParams kp{p.dk, p.dv, p.dq_acc, p.lse2, p.delta, status, p.N, Npad, p.H,
+                  p.scale, p.scale * kLog2e};
+    dim3 grid((p.N + 127) / 128, p.H, p.B);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, kp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e, "backward main launch");
+  }
+  // 3. convert
+  {
+    const long long n8 = static_cast<long long>(p.B) * p.H * p.N * D / 8;
+    const long long want = (n8 + 255) / 256;
+    const unsigned blocks = static_cast<unsigned>(want < 152 * 16 ? want : 152 * 16);
+    bwd_convert_kernel<FP16><<<blocks, 256, 0, stream>>>(p.dq_acc, static_cast<uint16_t*>(p.dq),
+                                                         p.scale, n8);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e, "backward convert launch");
+  }
+  return ATTN_OK;
+}
+
+template <int D>
+attn_status_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
+  if (p.causal)
+    return p.fp16 ? launch_bwd_t<D, true, true>(p, stream) : launch_bwd_t<D, true, false>(p, stream);
+  return p.fp16 ? launch_bwd_t<D, false, true>(p, stream) : launch_bwd_t<D, false, false>(p, stream);
+}
+
+}  // namespace
+
+attn_status_t launch_bwd(const BwdParams& p, cudaStream_t stream) {
+  if (p.N > 65535 * 128 || p.H > 65535 || p.B > 65535)
+    return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
+  switch (p.d) {
+    case 64: return launch_bwd_d<64>(p, stream);
+    case 128: return launch_bwd_d<128>(p, stream);
+  }
+  return fail(ATTN_ERR_UNSUPPORTED, "the backward pass supports d = 64 and 128");
+}
+
 }  // namespace attn

@@ -51,7 +51,8 @@ struct BwdParams {
   void* dk;
   void* dv;
   float* dq_acc;   // [B, H, N, d] float32 scratch
-  float* delta;    // [B, H, N] float32 scratch
+  float* lse2;     // [B, H, Npad] float32 scratch: LSE * log2(e), +inf padding
+  float* delta;    // [B, H, Npad] float32 scratch: rowsum(dO * O), 0 padding
   int B, H, N, d;
   int causal;
   float scale;
@@ -87,5 +88,21 @@ attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream);
 attn_status_t launch_fwd_fp8(const Fp8FwdParams& p, cudaStream_t stream);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Backward scratch layout: dQ accumulator, then L*log2(e) and D, each padded
+// to a multiple of 128 rows per head; every part 256-byte aligned.
+struct BwdWorkspace {
+  size_t dq_acc, lse2, delta, total;
+};
+inline BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t rows_pad = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128 * 128);
+  BwdWorkspace w;
+  w.dq_acc = 0;
+  w.lse2 = align_up(rows * d * sizeof(float), 256);
+  w.delta = w.lse2 + align_up(rows_pad * sizeof(float), 256);
+  w.total = w.delta + align_up(rows_pad * sizeof(float), 256);
+  return w;
+}
 
 }  // namespace attn

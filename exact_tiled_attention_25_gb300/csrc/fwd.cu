@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
+#pragma unroll
       for (int t = 0; t < NQ; ++t) {
         if (nK[t] == 0) continue;
         mbar_arrive_expect_tx(&q_full[t], C::TILE_BYTES);
@@ -181,8 +182,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       constexpr uint32_t idS = idesc_f16(E, 128, BN, false, false);
       constexpr uint32_t idPV = idesc_f16(E, 128, D, false, true);
       bool ok = true;
-      for (int t = 0; t < NQ && ok; ++t)
-        if (nK[t] > 0) ok = mbar_wait(&q_full[t], 0, ab, kDevTimeoutMma);
+#pragma unroll
+      for (int t = 0; t < NQ; ++t)
+        if (ok && nK[t] > 0) ok = mbar_wait(&q_full[t], 0, ab, kDevTimeoutMma);
       for (int j = 0; j <= nKmax && ok; ++j) {
         const int itK = 2 * j;
         const int itV = 2 * (j - 1) + 1;
@@ -197,6 +199,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           break;
         }
         tc_fence_after_sync();
+#pragma unroll
         for (int t = 0; t < NQ; ++t) {
           if (j >= 1 && j - 1 < nK[t]) {
             // O_t += P_t(j-1) V_{j-1}
@@ -239,6 +242,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const int quarter = warp % 4;
     const int r = quarter * 32 + lane;
     const int qt = g * NQ + t;
+    // key tiles of this warpgroup's query tile (a scalar: no runtime-indexed array)
+    const int my_nK = (qt * BM < N) ? (CAUSAL ? min(nKtot, qt + 1) : nKtot) : 0;
     const int row_g = qt * BM + r;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::S_COL(t);
@@ -247,7 +252,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nK[t]; ++j) {
+    for (int j = 0; j < my_nK; ++j) {
       if (!mbar_wait(&s_full[t], j & 1, ab, kDevTimeoutSoftmax)) {
         ok = false;
         break;
@@ -282,17 +287,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         l *= alpha;
         m_ref = m_new;
       }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-        for (int c0 = 0; c0 < D / 32; ++c0) {
-          uint32_t o[32];
-          tmem_ld32(tO + c0 * 32, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + c0 * 32, o);
-        }
-      }
       const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref * c2;
       const uint64_t cc = pack2(c2, c2);
       const uint64_t nn = pack2(neg, neg);
@@ -314,12 +308,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       const uint64_t acc = fadd2(acc0, acc1);
       l += lo2(acc) + hi2(acc);
+      // Rescale this row of O after the scores are consumed (fewer live
+      // registers); the P V product of this step is issued only after the
+      // arrive below, and the previous one finished before S_t(j) did.
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D / 32; ++c0) {
+          uint32_t o[32];
+          tmem_ld32(tO + c0 * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c0 * 32, o);
+        }
+      }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&p_full[t]);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && nK[t] > 0 && mbar_wait(&o_full[t], 0, ab, kDevTimeoutEpilogue)) {
+    if (ok && my_nK > 0 && mbar_wait(&o_full[t], 0, ab, kDevTimeoutEpilogue)) {
       tc_fence_after_sync();
       const float inv_l = 1.f / l;
       uint16_t* orow = static_cast<uint16_t*>(kp.o) + (static_cast<size_t>(bh) * N + row_g) * D;
@@ -354,6 +362,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   if (abort_sh) {
     // Let every copy and MMA this CTA issued land before the memory goes away.
     if (warp == C::LOAD_WARP && lane == 0) {
+#pragma unroll
       for (int t = 0; t < NQ; ++t)
         if (nK[t] > 0) mbar_wait_drain(&q_full[t], 0);
       const int issued = load_items_sh;

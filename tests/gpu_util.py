@@ -46,10 +46,13 @@ def assert_fwd_close(o_gpu, lse_gpu, o_ref, lse_ref, max_abs=FWD_MAX_ABS, rmse=F
     return e_max, e_rmse, e_lse
 
 
-def rel_rmse(g_gpu, g_ref):
+def rel_rmse(g_gpu, g_ref, floor=1e-4):
+    """RMSE(g - g_ref) / RMS(g_ref).  The denominator is floored at `floor`
+    because some gradients are exactly zero (e.g. dQ and dK with a single key),
+    where only float32 rounding residue remains on the GPU."""
     g = g_gpu.float().cpu().numpy().astype(np.float64)
     assert np.all(np.isfinite(g))
-    return float(np.sqrt(np.mean((g - g_ref) ** 2)) / np.sqrt(np.mean(g_ref ** 2)))
+    return float(np.sqrt(np.mean((g - g_ref) ** 2)) / max(np.sqrt(np.mean(g_ref ** 2)), floor))
 
 
 def guarded(shape, dtype, fill):

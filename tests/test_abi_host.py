@@ -43,10 +43,13 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    B, H, N, d = 2, 16, 4096, 128
-    rows = B * H * N
-    expect = -(-rows * d * 4 // 256) * 256 + -(-rows * 4 // 256) * 256
-    assert lib.attn_bwd_workspace_size(B, H, N, d) == expect
+    up = lambda x: -(-x // 256) * 256
+    for B, H, N, d in ((2, 16, 4096, 128), (1, 3, 300, 64)):
+        rows = B * H * N
+        rows_pad = B * H * (-(-N // 128) * 128)
+        # float32 dQ accumulator + two float32 row vectors padded to 128 rows per head
+        expect = up(rows * d * 4) + 2 * up(rows_pad * 4)
+        assert lib.attn_bwd_workspace_size(B, H, N, d) == expect
     assert lib.attn_bwd_workspace_size(0, 1, 1, 64) == 0
 
 
