@@ -109,6 +109,28 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        cudaStream_t stream);
 
 /*
+ * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for code that
+ * may not call cudaMalloc (or any allocating routine) itself, such as a
+ * runtime without its own device allocator.  Arguments are those of attn_bwd
+ * without the workspace: the scratch comes from a 64 MiB array built into the
+ * library (held on every GPU that loads the library until the process exits).
+ *   - Problems whose attn_bwd_workspace_size() exceeds 64 MiB are rejected with
+ *     ATTN_ERR_INVALID_ARG and a message naming the sizes.
+ *   - No device memory is allocated or freed by this call.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream
+ *     capture.
+ *   - Every call shares the one array.  Calls whose work overlaps on the GPU
+ *     (different streams, or different host threads on the same device) race on
+ *     it; serialise them.  Each call clears what must start at zero itself.
+ */
+attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                               const void* dout, const float* lse, void* dq, void* dk,
+                               void* dv, int B, int H, int N, int d, int causal,
+                               float softmax_scale, attn_dtype_t dtype, cudaStream_t stream);
+
+/*
  * attn_fp8_quantize -- FP8 e4m3 pre-pass with block scaling and incoherent
  * processing ("FlashAttention-3: Hopper Asynchrony and FP8 Attention", section
  * "FP8 accuracy controls").
