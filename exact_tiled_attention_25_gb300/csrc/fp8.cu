@@ -1,11 +1,522 @@
-// FP8 pre-pass and forward (placeholder until the kernels land).
+// FP8 (e4m3) path on sm_103a: the quantisation pre-pass and the FP8 forward.
+//
+// Method: "FlashAttention-3: Hopper Asynchrony and FP8 Attention", section "FP8
+// accuracy controls": block quantisation keeps one scale per Q, K or V block,
+// and incoherent processing multiplies Q and K by the same orthogonal matrix
+// M = diag(s) H_d / sqrt(d) before quantisation, so (QM)(KM)^T = QK^T and the
+// forward kernel needs no knowledge of M.
+//
+// Pre-pass (d = 128): one CTA per (128-row block, head, tensor).  A warp holds
+// a row as 32 lanes x 4 values; the Walsh-Hadamard butterfly runs two stages
+// inside each lane and five across lanes with xor shuffles.  The block amax
+// gives descale = amax / 448 and codes = e4m3_rn_satfinite(x / descale).
+// Per-tensor mode (the comparator) runs amax, reduce and quantise kernels.
+//
+// Forward (d = 128): the BF16 forward's structure with tcgen05.mma
+// kind::f8f6f4 (32-element K steps).  Scores use c_j = scale * log2(e) * dq_i *
+// dk_j, folded into the single FMA before exp2.  The per-block V descales are
+// folded into the exponent as log2(dv_j / dv_max) (dv_max = largest V descale
+// of the head), so P dv_j / dv_max is what is rounded to e4m3 for the P V
+// product; the row sum l accumulates the unscaled P, and the epilogue
+// multiplies O by dv_max / l.  The page's FP8 layout steps ("FP8 layout
+// conformance": V transpose, accumulator byte permutation) are not needed:
+// V is read as an MN-major operand and P goes through tensor memory.
+#include <cmath>
+
 #include "common.h"
+#include "sm103_prims.cuh"
 
 namespace attn {
-attn_status_t launch_fp8_quantize(const Fp8QuantParams&, cudaStream_t) {
-  return fail(ATTN_ERR_UNSUPPORTED, "FP8 pre-pass not built yet");
+namespace {
+
+constexpr int kSmemLimit = 232448;
+constexpr float kE4m3Max = 448.f;
+
+// ============================================================== pre-pass ====
+// Mode: 0 = fused block mode (amax + quantise), 1 = block amax only (into
+// descale), 2 = quantise with the descale already in place.
+template <int MODE>
+__global__ void __launch_bounds__(256)
+    fp8_quant_kernel(const float* __restrict__ src0, const float* __restrict__ src1,
+                     const float* __restrict__ src2, uint8_t* __restrict__ dst0,
+                     uint8_t* __restrict__ dst1, uint8_t* __restrict__ dst2,
+                     float* __restrict__ desc0, float* __restrict__ desc1,
+                     float* __restrict__ desc2, const float* __restrict__ signs, int N,
+                     int nblk) {
+  constexpr int D = 128;
+  const int which = blockIdx.z;
+  const float* src = which == 0 ? src0 : (which == 1 ? src1 : src2);
+  uint8_t* dst = which == 0 ? dst0 : (which == 1 ? dst1 : dst2);
+  float* desc = which == 0 ? desc0 : (which == 1 ? desc1 : desc2);
+  const bool hadamard = signs != nullptr && which < 2;
+  const int blk = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  __shared__ float warp_max[8];
+
+  float4 x[16];   // 16 rows per warp, 4 columns per lane
+  float amax = 0.f;
+  float4 s4 = make_float4(1.f, 1.f, 1.f, 1.f);
+  if (hadamard) s4 = reinterpret_cast<const float4*>(signs)[lane];
+  const float inv_sqrt_d = 0.08838834764831845f;   // 1 / sqrt(128)
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int row = blk * 128 + warp * 16 + r;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < N) v = reinterpret_cast<const float4*>(src + (static_cast<size_t>(bh) * N + row) * D)[lane];
+    if (hadamard) {
+      v.x *= s4.x; v.y *= s4.y; v.z *= s4.z; v.w *= s4.w;
+      // stages of span 1 and 2 inside the lane (columns 4*lane .. 4*lane+3)
+      float a = v.x + v.y, b = v.x - v.y, c = v.z + v.w, e = v.z - v.w;
+      v = make_float4(a + c, b + e, a - c, b - e);
+      // stages of span 4 .. 64 across lanes (lane distance 1 .. 16)
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const float ox = __shfl_xor_sync(0xffffffffu, v.x, m);
+        const float oy = __shfl_xor_sync(0xffffffffu, v.y, m);
+        const float oz = __shfl_xor_sync(0xffffffffu, v.z, m);
+        const float ow = __shfl_xor_sync(0xffffffffu, v.w, m);
+        if (lane & m) {
+          v = make_float4(ox - v.x, oy - v.y, oz - v.z, ow - v.w);
+        } else {
+          v = make_float4(v.x + ox, v.y + oy, v.z + oz, v.w + ow);
+        }
+      }
+      v.x *= inv_sqrt_d; v.y *= inv_sqrt_d; v.z *= inv_sqrt_d; v.w *= inv_sqrt_d;
+    }
+    x[r] = v;
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+
+  float descale;
+  if (MODE == 2) {
+    descale = desc[static_cast<size_t>(bh) * nblk + blk];
+  } else {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) warp_max[warp] = amax;
+    __syncthreads();
+    float bmax = warp_max[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) bmax = fmaxf(bmax, warp_max[w]);
+    if (MODE == 1) {
+      if (threadIdx.x == 0) desc[static_cast<size_t>(bh) * nblk + blk] = bmax;
+      return;
+    }
+    descale = bmax > 0.f ? __fdiv_rn(bmax, kE4m3Max) : 1.f;
+    if (threadIdx.x == 0) desc[static_cast<size_t>(bh) * nblk + blk] = descale;
+  }
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int row = blk * 128 + warp * 16 + r;
+    if (row < N) {
+      const float4 v = x[r];
+      const uint32_t packed = cvt_pack_e4m3x4(__fdiv_rn(v.x, descale), __fdiv_rn(v.y, descale),
+                                              __fdiv_rn(v.z, descale), __fdiv_rn(v.w, descale));
+      reinterpret_cast<uint32_t*>(dst + (static_cast<size_t>(bh) * N + row) * D)[lane] = packed;
+    }
+  }
 }
-attn_status_t launch_fwd_fp8(const Fp8FwdParams&, cudaStream_t) {
-  return fail(ATTN_ERR_UNSUPPORTED, "FP8 forward not built yet");
+
+// Per-tensor mode: one CTA per tensor reduces the block amaxes and writes the
+// single descale into every entry.
+__global__ void __launch_bounds__(256)
+    fp8_tensor_scale_kernel(float* __restrict__ desc0, float* __restrict__ desc1,
+                            float* __restrict__ desc2, long long count) {
+  float* desc = blockIdx.x == 0 ? desc0 : (blockIdx.x == 1 ? desc1 : desc2);
+  __shared__ float warp_max[8];
+  float m = 0.f;
+  for (long long i = threadIdx.x; i < count; i += blockDim.x) m = fmaxf(m, desc[i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x / 32] = m;
+  __syncthreads();
+  float gmax = warp_max[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) gmax = fmaxf(gmax, warp_max[w]);
+  const float descale = gmax > 0.f ? __fdiv_rn(gmax, kE4m3Max) : 1.f;
+  __syncthreads();
+  for (long long i = threadIdx.x; i < count; i += blockDim.x) desc[i] = descale;
 }
+
+// =============================================================== forward ====
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int D8 = 128;
+constexpr int NQ8 = 2;
+constexpr int TILE8 = BM * D8;            // 16 KB: one 128-byte row per token
+constexpr int NSLOT8 = 8;
+constexpr int SMEM8 = 1024 + NQ8 * TILE8 + NSLOT8 * TILE8;
+constexpr int THREADS8 = (4 * NQ8 + 2) * 32;
+constexpr int LOAD_WARP8 = 4 * NQ8;
+constexpr int MMA_WARP8 = 4 * NQ8 + 1;
+__host__ __device__ constexpr uint32_t s_col8(int t) { return 128u * t; }
+__host__ __device__ constexpr uint32_t o_col8(int t) { return 256u + 128u * t; }
+static_assert(SMEM8 <= kSmemLimit - 512, "shared memory");
+
+struct Fp8KParams {
+  const float* q_descale;
+  const float* k_descale;
+  const float* v_descale;
+  void* o;
+  float* lse;
+  int* status;
+  int N;
+  int H;
+  int nblk;
+  float scale_log2;
+};
+
+__device__ __forceinline__ float lg2_approx8(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(THREADS8, 1)
+    fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const Fp8KParams kp) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + NQ8 * TILE8;
+
+  __shared__ __align__(8) uint64_t q_full[NQ8];
+  __shared__ __align__(8) uint64_t kv_full[NSLOT8];
+  __shared__ __align__(8) uint64_t kv_empty[NSLOT8];
+  __shared__ __align__(8) uint64_t s_full[NQ8];
+  __shared__ __align__(8) uint64_t p_full[NQ8];
+  __shared__ __align__(8) uint64_t o_full[NQ8];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ int load_items_sh;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int g = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int bh = blockIdx.z * kp.H + blockIdx.y;
+  const int N = kp.N;
+  const int nKtot = (N + BN - 1) / BN;
+  int nK[NQ8];
+  int nKmax = 0;
+#pragma unroll
+  for (int t = 0; t < NQ8; ++t) {
+    const int qt = g * NQ8 + t;
+    nK[t] = (qt * BM < N) ? (CAUSAL ? min(nKtot, qt + 1) : nKtot) : 0;
+    nKmax = max(nKmax, nK[t]);
+  }
+  const int total_items = 2 * nKmax;
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < NQ8; ++t) {
+      mbar_init(&q_full[t], 1);
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&o_full[t], 1);
+    }
+    for (int s = 0; s < NSLOT8; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    load_items_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == MMA_WARP8) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+  const Abort ab{&abort_sh, kp.status};
+
+  if (warp == LOAD_WARP8) {
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+#pragma unroll
+      for (int t = 0; t < NQ8; ++t) {
+        if (nK[t] == 0) continue;
+        mbar_arrive_expect_tx(&q_full[t], TILE8);
+        tma_load_3d(sQ + t * TILE8, &tmQ, &q_full[t], 0, (g * NQ8 + t) * BM, bh);
+      }
+      int it = 0;
+      bool ok = true;
+      for (int j = 0; j < nKmax && ok; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int slot = it % NSLOT8;
+          const int use = it / NSLOT8;
+          if (use >= 1 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, ab, kDevTimeoutLoad)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&kv_full[slot], TILE8);
+          tma_load_3d(sKV + slot * TILE8, kv ? &tmV : &tmK, &kv_full[slot], 0, j * BN, bh);
+          ++it;
+        }
+      }
+      load_items_sh = it;
+    }
+  } else if (warp == MMA_WARP8) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_e4m3(128, BN, false, false);
+      constexpr uint32_t idPV = idesc_e4m3(128, D8, false, true);
+      bool ok = true;
+#pragma unroll
+      for (int t = 0; t < NQ8; ++t)
+        if (ok && nK[t] > 0) ok = mbar_wait(&q_full[t], 0, ab, kDevTimeoutMma);
+      for (int j = 0; j <= nKmax && ok; ++j) {
+        const int itK = 2 * j;
+        const int itV = 2 * (j - 1) + 1;
+        const int slotK = itK % NSLOT8;
+        const int slotV = (itV + NSLOT8) % NSLOT8;
+        if (j < nKmax && !mbar_wait(&kv_full[slotK], (itK / NSLOT8) & 1, ab, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        if (j >= 1 && !mbar_wait(&kv_full[slotV], (itV / NSLOT8) & 1, ab, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int t = 0; t < NQ8; ++t) {
+          if (j >= 1 && j - 1 < nK[t]) {
+            if (!mbar_wait(&p_full[t], (j - 1) & 1, ab, kDevTimeoutMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t vbase = smem_u32(sKV + slotV * TILE8);
+#pragma unroll
+            for (int kk = 0; kk < BN / 32; ++kk) {
+              const uint64_t bdesc = sdesc_sw128(vbase + kk * 32 * 128, TILE8, 1024);
+              mma_f8_ts(tmem + o_col8(t), tmem + s_col8(t) + kk * 8, bdesc, idPV,
+                        (j - 1 > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (j - 1 == nK[t] - 1) mma_commit(&o_full[t]);
+          }
+          if (j < nK[t]) {
+            const uint32_t qbase = smem_u32(sQ + t * TILE8);
+            const uint32_t kbase = smem_u32(sKV + slotK * TILE8);
+#pragma unroll
+            for (int kk = 0; kk < D8 / 32; ++kk) {
+              mma_f8_ss(tmem + s_col8(t), sdesc_sw128(qbase + kk * 32, 16, 1024),
+                        sdesc_sw128(kbase + kk * 32, 16, 1024), idS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&s_full[t]);
+          }
+        }
+        if (!ok) break;
+        if (j >= 1 && itV + NSLOT8 < total_items) mma_commit(&kv_empty[slotV]);
+        if (j < nKmax && itK + NSLOT8 < total_items) mma_commit(&kv_empty[slotK]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp / 4;
+    const int quarter = warp % 4;
+    const int r = quarter * 32 + lane;
+    const int qt = g * NQ8 + t;
+    const int my_nK = (qt * BM < N) ? (CAUSAL ? min(nKtot, qt + 1) : nKtot) : 0;
+    const int row_g = qt * BM + r;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + s_col8(t);
+    const uint32_t tO = tmem + lane_addr + o_col8(t);
+    const float* kdesc = kp.k_descale + static_cast<size_t>(bh) * kp.nblk;
+    const float* vdesc = kp.v_descale + static_cast<size_t>(bh) * kp.nblk;
+    float dv_max = 0.f;
+    for (int b = 0; b < kp.nblk; ++b) dv_max = fmaxf(dv_max, vdesc[b]);
+    const float c_q = (my_nK > 0) ? kp.scale_log2 * kp.q_descale[static_cast<size_t>(bh) * kp.nblk + qt] : 0.f;
+    float m_ref = -INFINITY;   // in log2 units of the scaled scores
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < my_nK; ++j) {
+      const float cj = c_q * kdesc[j];
+      const float ratio = vdesc[j] / dv_max;              // in (0, 1]
+      const float lg_ratio = lg2_approx8(ratio);
+      if (!mbar_wait(&s_full[t], j & 1, ab, kDevTimeoutSoftmax)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t sr[BN];
+#pragma unroll
+      for (int c0 = 0; c0 < BN / 32; ++c0)
+        tmem_ld32(tS + c0 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0 * 32]));
+      tmem_ld_wait();
+      const int kbase = j * BN;
+      if ((CAUSAL && j == qt) || kbase + BN > N) {
+        const int lim = (CAUSAL ? min(N, row_g + 1) : N) - kbase;
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; c += 8) {
+        mx0 = fmax3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+        mx2 = fmax3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+        mx3 = fmax3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+      }
+      const float m_new = fmaxf(m_ref, fmax3(mx0, mx1, fmaxf(mx2, mx3)) * cj);
+      const bool need = (m_new - m_ref) > 8.f;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2_approx(m_ref - m_new);
+        l *= alpha;
+        m_ref = m_new;
+      }
+      // exponent offset: -m_ref (the running reference) + log2(dv_j / dv_max)
+      const float off = ((m_ref == -INFINITY) ? 0.f : -m_ref) + lg_ratio;
+      const uint64_t cc = pack2(cj, cj);
+      const uint64_t nn = pack2(off, off);
+      uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+      for (int c0 = 0; c0 < BN / 32; ++c0) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 * 32 + 4 * i;
+          const uint64_t y0 = ffma2(pack2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), cc, nn);
+          const uint64_t y1 = ffma2(pack2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), cc, nn);
+          const float p0 = ex2_approx(lo2(y0));
+          const float p1 = ex2_approx(hi2(y0));
+          const float p2 = ex2_approx(lo2(y1));
+          const float p3 = ex2_approx(hi2(y1));
+          acc0 = fadd2(acc0, pack2(p0, p1));
+          acc1 = fadd2(acc1, pack2(p2, p3));
+          pk[i] = cvt_pack_e4m3x4(p0, p1, p2, p3);
+        }
+        tmem_st_x8(tS + c0 * 8, pk);
+      }
+      const uint64_t acc = fadd2(acc0, acc1);
+      l += (lo2(acc) + hi2(acc)) / ratio;                   // sum of the unscaled P
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D8 / 32; ++c0) {
+          uint32_t o[32];
+          tmem_ld32(tO + c0 * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c0 * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&p_full[t]);
+    }
+    if (ok && my_nK > 0 && mbar_wait(&o_full[t], 0, ab, kDevTimeoutEpilogue)) {
+      tc_fence_after_sync();
+      const float mul = dv_max / l;
+      uint16_t* orow = static_cast<uint16_t*>(kp.o) + (static_cast<size_t>(bh) * N + row_g) * D8;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D8 / 32; ++c0) {
+        uint32_t o[32];
+        tmem_ld32(tO + c0 * 32, o);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = cvt_pack_bf16(__uint_as_float(o[2 * i]) * mul, __uint_as_float(o[2 * i + 1]) * mul);
+        if (row_g < N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (row_g < N)
+        kp.lse[static_cast<size_t>(bh) * N + row_g] = (m_ref + lg2_approx8(l)) * 0.69314718055994530942f;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (abort_sh) {
+    if (warp == LOAD_WARP8 && lane == 0) {
+#pragma unroll
+      for (int t = 0; t < NQ8; ++t)
+        if (nK[t] > 0) mbar_wait_drain(&q_full[t], 0);
+      const int issued = load_items_sh;
+      for (int s = 0; s < NSLOT8 && s < issued; ++s)
+        mbar_wait_drain(&kv_full[s], ((issued - 1 - s) / NSLOT8) & 1);
+    }
+    if (warp == MMA_WARP8 && lane == 0) {
+      mma_commit(&drain_bar);
+      mbar_wait_drain(&drain_bar, 0);
+    }
+    __syncthreads();
+  }
+  if (warp == MMA_WARP8) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) {
+  if (p.d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
+  const int nblk = (p.N + 127) / 128;
+  if (p.B * p.H > 65535 || nblk > 2147483647 / 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
+  dim3 grid(nblk, p.B * p.H, 3);
+  if (!p.per_tensor) {
+    fp8_quant_kernel<0><<<grid, 256, 0, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1],
+                                                  p.dst[2], p.descale[0], p.descale[1],
+                                                  p.descale[2], p.signs, p.N, nblk);
+  } else {
+    fp8_quant_kernel<1><<<grid, 256, 0, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1],
+                                                  p.dst[2], p.descale[0], p.descale[1],
+                                                  p.descale[2], nullptr, p.N, nblk);
+    fp8_tensor_scale_kernel<<<3, 256, 0, stream>>>(p.descale[0], p.descale[1], p.descale[2],
+                                                   static_cast<long long>(p.B) * p.H * nblk);
+    fp8_quant_kernel<2><<<grid, 256, 0, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1],
+                                                  p.dst[2], p.descale[0], p.descale[1],
+                                                  p.descale[2], nullptr, p.N, nblk);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "FP8 pre-pass launch");
+  return ATTN_OK;
+}
+
+template <bool CAUSAL>
+attn_status_t launch_fwd_fp8_t(const Fp8FwdParams& p, cudaStream_t stream) {
+  auto kern = fwd_fp8_kernel<CAUSAL>;
+  attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), SMEM8);
+  if (s != ATTN_OK) return s;
+  CUtensorMap tq, tk, tv;
+  const uint64_t planes = static_cast<uint64_t>(p.B) * p.H;
+  if ((s = make_tmap_3d(&tq, p.q8, 1, D8, p.N, planes, 128, BM)) != ATTN_OK) return s;
+  if ((s = make_tmap_3d(&tk, p.k8, 1, D8, p.N, planes, 128, BN)) != ATTN_OK) return s;
+  if ((s = make_tmap_3d(&tv, p.v8, 1, D8, p.N, planes, 128, BN)) != ATTN_OK) return s;
+  int* status = device_status_word();
+  if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
+  Fp8KParams kp{p.q_descale, p.k_descale, p.v_descale, p.o, p.lse, status, p.N, p.H,
+                (p.N + 127) / 128, p.scale * 1.4426950408889634f};
+  dim3 grid((p.N + BM * NQ8 - 1) / (BM * NQ8), p.H, p.B);
+  kern<<<grid, THREADS8, SMEM8, stream>>>(tq, tk, tv, kp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "FP8 forward launch");
+  return ATTN_OK;
+}
+
+attn_status_t launch_fwd_fp8(const Fp8FwdParams& p, cudaStream_t stream) {
+  if (p.d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
+  if (p.N > 65535 * 256 || p.H > 65535 || p.B > 65535)
+    return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
+  return p.causal ? launch_fwd_fp8_t<true>(p, stream) : launch_fwd_fp8_t<false>(p, stream);
+}
+
 }  // namespace attn

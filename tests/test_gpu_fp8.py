@@ -1,0 +1,109 @@
+"""FP8 path parity: the e4m3 pre-pass against the oracle quantiser, and the FP8
+forward against exact float64 attention (on the original float32 inputs and on
+the dequantised inputs)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_util import FP8_RMSE, check_status, dev, lib
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def attn():
+    return lib()
+
+
+def _quant(attn, xs, signs=None, per_tensor=False):
+    g = [torch.from_numpy(x).to(dev()) for x in xs]
+    s = None if signs is None else torch.from_numpy(signs).to(dev())
+    codes, desc = attn.attn_fp8_quantize(*g, hadamard_signs=s, per_tensor=per_tensor)
+    check_status(attn)
+    return [c.cpu().numpy() for c in codes], [d.cpu().numpy() for d in desc]
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 300, 128), (2, 3, 256, 128), (1, 1, 1, 128)])
+@pytest.mark.parametrize("per_tensor", [False, True])
+def test_quantiser_bit_exact_without_hadamard(attn, shape, per_tensor):
+    xs = workloads.normal_with_outliers(11, shape, 3)
+    codes, desc = _quant(attn, xs, per_tensor=per_tensor)
+    for x, c, d in zip(xs, codes, desc):
+        rc, rd = oracle.quantize_e4m3_blocks(x, per_tensor=per_tensor)
+        np.testing.assert_array_equal(d, rd)
+        np.testing.assert_array_equal(c, rc)
+
+
+def test_quantiser_with_hadamard(attn):
+    """The GPU transform runs in float32, the oracle's in float64: descales agree
+    to float32 rounding and codes differ by at most one e4m3 step, rarely."""
+    shape = (1, 4, 700, 128)
+    xs = workloads.normal_with_outliers(12, shape, 3)
+    signs = workloads.random_signs(5, 128)
+    codes, desc = _quant(attn, xs, signs)
+    for which, (x, c, d) in enumerate(zip(xs, codes, desc)):
+        rc, rd = oracle.quantize_e4m3_blocks(x, signs=signs if which < 2 else None)
+        np.testing.assert_allclose(d, rd, rtol=2e-6)
+        if which == 2:
+            np.testing.assert_array_equal(c, rc)          # V is not transformed
+            continue
+        got = oracle.e4m3_decode(c)
+        ref = oracle.e4m3_decode(rc)
+        diff = np.abs(got - ref)
+        step = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -6))) - 3)
+        assert np.all(diff <= step * 1.0001)
+        assert np.mean(c != rc) < 1e-3
+
+
+def _fp8_forward(attn, q, k, v, signs, per_tensor, causal):
+    gq, gk, gv = (torch.from_numpy(x).to(dev()) for x in (q, k, v))
+    s = None if signs is None else torch.from_numpy(signs).to(dev())
+    (q8, k8, v8), (qd, kd, vd) = attn.attn_fp8_quantize(gq, gk, gv, hadamard_signs=s,
+                                                        per_tensor=per_tensor)
+    o, lse = attn.attn_fwd_fp8(q8, k8, v8, qd, kd, vd, causal=causal,
+                               softmax_scale=1 / np.sqrt(q.shape[-1]))
+    check_status(attn)
+    return (o, lse), [t.cpu().numpy() for t in (q8, k8, v8, qd, kd, vd)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 100, 129, 300, 640])
+def test_fp8_forward_matches_dequantised_oracle(attn, N, causal):
+    """Against exact attention on the dequantised e4m3 inputs, the only error
+    left is the kernel's own: P rounded to e4m3 for the P V product and float32
+    accumulation."""
+    B, H, d = 1, 2, 128
+    q, k, v = workloads.normal_with_outliers(40 + N, (B, H, N, d), 3)
+    signs = workloads.random_signs(5, d)
+    (o, lse), (q8, k8, v8, qd, kd, vd) = _fp8_forward(attn, q, k, v, signs, False, causal)
+    dq_, dk_, dv_ = (oracle.dequantize_e4m3_blocks(c, s) for c, s in ((q8, qd), (k8, kd), (v8, vd)))
+    ref_o, ref_l = oracle.attention_forward(dq_, dk_, dv_, 1 / np.sqrt(d), causal)
+    got = o.float().cpu().numpy()
+    diff = got - ref_o
+    assert np.sqrt(np.mean(diff ** 2)) <= 1e-2 * max(1.0, np.sqrt(np.mean(ref_o ** 2)))
+    assert np.abs(diff).max() <= 0.25 * max(1.0, np.abs(ref_o).max())
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=2e-3)
+
+
+def test_fp8_outlier_config_rmse(attn):
+    """The outlier-stress problem at full size (B=2, H=16, N=4096, d=128): RMSE
+    of the FP8 output against exact float64 attention on the original float32
+    inputs, on sampled heads, for per-tensor, block, and block + Hadamard."""
+    w = workloads.FP8_FWD
+    q, k, v = workloads.normal_with_outliers(w.seed, (w.B, w.H, w.N, w.d), 3)
+    signs = workloads.random_signs(workloads.FP8_HADAMARD_SIGN_SEED, w.d)
+    heads = [(0, 0), (1, 9), (0, 15)]
+    refs = {bh: oracle.attention_forward_head(q[bh], k[bh], v[bh], w.scale, w.causal)[0]
+            for bh in heads}
+    rmse = {}
+    for name, sg, pt in (("per_tensor", None, True), ("block", None, False),
+                         ("block_hadamard", signs, False)):
+        (o, _), _ = _fp8_forward(attn, q, k, v, sg, pt, w.causal)
+        got = o.float().cpu().numpy()
+        err = np.concatenate([(got[bh] - refs[bh]).ravel() for bh in heads])
+        rmse[name] = float(np.sqrt(np.mean(err ** 2)))
+    print("fp8 rmse", rmse)
+    assert rmse["block"] <= FP8_RMSE and rmse["block_hadamard"] <= FP8_RMSE
+    assert rmse["block_hadamard"] < rmse["per_tensor"]
