@@ -16,13 +16,16 @@
 //  2. main: one CTA per (key/value tile j, head, batch).  K_j and V_j stay in
 //     shared memory; dK_j and dV_j accumulate in tensor memory.  Per query tile
 //     i (causal: i >= j) the MMA thread issues, on tcgen05,
-//        dP^T = V_j dO_i^T        S^T = K_j Q_i^T
-//     the compute warpgroup (thread = key row) forms P^T and dS^T in registers
-//     and writes them back to tensor memory (operands of the next two MMAs)
-//     and dS^T to shared memory (operand of the third),
-//        dV += P^T dO_i           dK += dS^T Q_i          dQ_i = dS K_j
-//     and the reduce warpgroup (thread = query row) reads dQ_i from tensor
-//     memory and adds it into the float32 accumulator with vector reductions.
+//        S^T = K_j Q_i^T, then dP^T = V_j dO_i^T,
+//     the compute warpgroup (thread = key row) forms P^T while dP^T runs and
+//     writes it back to tensor memory, so
+//        dV += P^T dO_i
+//     runs while the same warpgroup forms dS^T = P^T (dP^T - D) (tensor memory
+//     for dK, shared memory for dQ), then
+//        dK += dS^T Q_i,   dQ_i = dS K_j  (at d = 128 as dQ_i^T = K_j^T dS^T)
+//     and the reduce warpgroup reads dQ_i from tensor memory and adds it into
+//     the float32 accumulator.  At d = 128, dQ_i^T has one head dimension per
+//     TMEM lane, so each warp-wide reduction covers a whole 128-byte line.
 //  3. convert: dQ = scale * accumulator, rounded to the 16-bit type.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -57,12 +60,15 @@ struct BwdCfg {
   static constexpr int NEED = OFF_BAR + 256;
   static constexpr int SMEM_BYTES = cmin(kSmemLimit, NEED + 1024);
   static constexpr int SLACK = SMEM_BYTES - NEED;   // room to align the base to 1024
-  static constexpr bool DQ_ALIAS = (D == 128);      // dQ shares columns with S^T
+  // TMEM columns: S^T/P^T [0,128), dP^T/dS^T [128,256), dV, dK.  At d = 128
+  // there is no room left, so dQ^T reuses the dP^T columns (after dK has read
+  // dS^T there); at d = 64 dQ has its own columns.
+  static constexpr bool DQ_T = (D == 128);          // dQ computed transposed, in the dP columns
   static constexpr uint32_t S_COL = 0;
   static constexpr uint32_t DP_COL = 128;
   static constexpr uint32_t DV_COL = 256;
   static constexpr uint32_t DK_COL = 256 + D;
-  static constexpr uint32_t DQ_COL = DQ_ALIAS ? 0 : 256 + 2 * D;
+  static constexpr uint32_t DQ_COL = DQ_T ? DP_COL : 256 + 2 * D;
   static constexpr int THREADS = 320;            // compute WG, reduce WG, load warp, MMA warp
   static constexpr int LOAD_WARP = 8;
   static constexpr int MMA_WARP = 9;
@@ -75,7 +81,9 @@ struct Bars {
   uint64_t stage_full[2];
   uint64_t stage_empty[2];
   uint64_t s_full;
-  uint64_t p_full;
+  uint64_t dp_full;
+  uint64_t p_ready;
+  uint64_t ds_ready;
   uint64_t dq_full;
   uint64_t dq_free;
   uint64_t ds_free;
@@ -209,7 +217,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_init(&bars.stage_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.p_full, 128);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.p_ready, 128);
+    mbar_init(&bars.ds_ready, 128);
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_free, 128);
     mbar_init(&bars.ds_free, 1);
@@ -270,7 +280,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       constexpr Elt E = FP16 ? Elt::F16 : Elt::BF16;
       constexpr uint32_t idSP = idesc_f16(E, 128, 128, false, false);   // S^T and dP^T
       constexpr uint32_t idKV = idesc_f16(E, 128, D, false, true);      // dV and dK (A in TMEM)
-      constexpr uint32_t idQ = idesc_f16(E, 128, D, true, true);        // dQ (A = dS from smem)
+      // dQ: rows = queries (d = 64) or, transposed, rows = head dim (d = 128);
+      // both operands MN-major from shared memory
+      constexpr uint32_t idQ = idesc_f16(E, 128, C::DQ_T ? 128 : D, true, true);
       const uint32_t sK = smem_u32(smem + C::OFF_K);
       const uint32_t sV = smem_u32(smem + C::OFF_V);
       const uint32_t sDS = smem_u32(smem + C::OFF_DS);
@@ -281,50 +293,65 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tc_fence_after_sync();
         const uint32_t sQ = smem_u32(smem + C::OFF_RING + st * 2 * C::TILE);
         const uint32_t sDO = sQ + C::TILE;
-        // dP^T = V_j dO_i^T
+        // Base descriptors of this step (K-major: lbo unused, sbo 1024; MN-major:
+        // lbo = distance between 64-element slabs, sbo 1024); every MMA below
+        // uses one of these advanced by a compile-time byte offset.
+        const uint64_t kK = opaque(sdesc_sw128(sK, 16, 1024));
+        const uint64_t kV = opaque(sdesc_sw128(sV, 16, 1024));
+        const uint64_t kQ = opaque(sdesc_sw128(sQ, 16, 1024));
+        const uint64_t kDO = opaque(sdesc_sw128(sDO, 16, 1024));
+        // S^T = K_j Q_i^T  (its columns held P^T of the last step, read by the
+        // dV MMA issued before this one)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          mma_f16_ss(tmem + C::DP_COL, sdesc_sw128(sV + off, 16, 1024),
-                     sdesc_sw128(sDO + off, 16, 1024), idSP, kk > 0 ? 1u : 0u);
-        }
-        // S^T = K_j Q_i^T (when dQ shares these columns, wait until the last dQ was read)
-        if (C::DQ_ALIAS && n > 0) {
-          if (!(ok = mbar_wait(&bars.dq_free, (n - 1) & 1, ab, kDevTimeoutMma))) break;
-          tc_fence_after_sync();
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          mma_f16_ss(tmem + C::S_COL, sdesc_sw128(sK + off, 16, 1024),
-                     sdesc_sw128(sQ + off, 16, 1024), idSP, kk > 0 ? 1u : 0u);
+          mma_f16_ss(tmem + C::S_COL, sdesc_add(kK, off), sdesc_add(kQ, off), idSP,
+                     kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars.s_full);
-        if (!(ok = mbar_wait(&bars.p_full, n & 1, ab, kDevTimeoutMma))) break;
-        tc_fence_after_sync();
-        // dV += P^T dO_i ; dK += dS^T Q_i   (A operands from tensor memory)
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk) {
-          const uint64_t bdo = sdesc_sw128(sDO + kk * 16 * 128, C::CHUNK, 1024);
-          mma_f16_ts(tmem + C::DV_COL, tmem + C::S_COL + kk * 8, bdo, idKV,
-                     (n > 0 || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk) {
-          const uint64_t bq = sdesc_sw128(sQ + kk * 16 * 128, C::CHUNK, 1024);
-          mma_f16_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8, bq, idKV,
-                     (n > 0 || kk > 0) ? 1u : 0u);
-        }
-        // dQ_i = dS K_j   (A = dS^T in shared memory read MN-major)
-        if (!C::DQ_ALIAS && n > 0) {
+        // dP^T = V_j dO_i^T  (at d = 128 these columns held the last dQ^T)
+        if (C::DQ_T && n > 0) {
           if (!(ok = mbar_wait(&bars.dq_free, (n - 1) & 1, ab, kDevTimeoutMma))) break;
           tc_fence_after_sync();
         }
 #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
+          mma_f16_ss(tmem + C::DP_COL, sdesc_add(kV, off), sdesc_add(kDO, off), idSP,
+                     kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars.dp_full);
+        // dV += P^T dO_i  (A = P^T from tensor memory)
+        if (!(ok = mbar_wait(&bars.p_ready, n & 1, ab, kDevTimeoutMma))) break;
+        tc_fence_after_sync();
+        const uint64_t mDO = opaque(sdesc_sw128(sDO, C::CHUNK, 1024));
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          mma_f16_ts(tmem + C::DV_COL, tmem + C::S_COL + kk * 8, sdesc_add(mDO, kk * 16 * 128),
+                     idKV, (n > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q_i  (A = dS^T from tensor memory)
+        if (!(ok = mbar_wait(&bars.ds_ready, n & 1, ab, kDevTimeoutMma))) break;
+        tc_fence_after_sync();
+        const uint64_t mQ = opaque(sdesc_sw128(sQ, C::CHUNK, 1024));
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          mma_f16_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8, sdesc_add(mQ, kk * 16 * 128),
+                     idKV, (n > 0 || kk > 0) ? 1u : 0u);
+        // dQ_i = dS K_j (d = 64), or dQ_i^T = K_j^T dS^T (d = 128)
+        if (!C::DQ_T && n > 0) {
+          if (!(ok = mbar_wait(&bars.dq_free, (n - 1) & 1, ab, kDevTimeoutMma))) break;
+          tc_fence_after_sync();
+        }
+        const uint64_t mDS = opaque(sdesc_sw128(sDS, C::CHUNK, 1024));
+        const uint64_t mK = opaque(sdesc_sw128(sK, C::CHUNK, 1024));
+#pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
-          const uint64_t ads = sdesc_sw128(sDS + kk * 16 * 128, C::CHUNK, 1024);
-          const uint64_t bk = sdesc_sw128(sK + kk * 16 * 128, C::CHUNK, 1024);
-          mma_f16_ss(tmem + C::DQ_COL, ads, bk, idQ, kk > 0 ? 1u : 0u);
+          const uint64_t dds = sdesc_add(mDS, kk * 16 * 128);
+          const uint64_t dk = sdesc_add(mK, kk * 16 * 128);
+          if (C::DQ_T)
+            mma_f16_ss(tmem + C::DQ_COL, dk, dds, idQ, kk > 0 ? 1u : 0u);
+          else
+            mma_f16_ss(tmem + C::DQ_COL, dds, dk, idQ, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars.dq_full);
         if (n + 1 < nsteps) mma_commit(&bars.ds_free);
@@ -344,38 +371,74 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     for (int n = 0; n < nsteps; ++n) {
       const int st = n % C::NST;
       const int i = i0 + n;
-      if (!(ok = mbar_wait(&bars.s_full, n & 1, ab, kDevTimeoutSoftmax))) break;
-      if (n > 0 && !(ok = mbar_wait(&bars.ds_free, (n - 1) & 1, ab, kDevTimeoutSoftmax))) break;
-      tc_fence_after_sync();
-      const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_LD + st * 1024);
-      const float* dvec = lse2 + 128;
+      const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + st * 1024);
+      const float4* dvec4 = lse4 + 32;
       const bool diag = CAUSAL && i == j;
+      // phase A: P^T = exp2(S^T c - L log2 e), written back over S^T as 16-bit
+      if (!(ok = mbar_wait(&bars.s_full, n & 1, ab, kDevTimeoutSoftmax))) break;
+      tc_fence_after_sync();
+      uint32_t pb[C::BM / 2];
 #pragma unroll
       for (int c0 = 0; c0 < C::BM / 32; ++c0) {
-        uint32_t sv[32], dpv[32];
+        uint32_t sv[32];
         tmem_ld32(tmem + lane_addr + C::S_COL + c0 * 32, sv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const int q0 = c0 * 32 + e;
+          const float4 l4 = lse4[q0 / 4];
+          float p[4];
+          p[0] = ex2_approx(fmaf(__uint_as_float(sv[e + 0]), c2, -l4.x));
+          p[1] = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), c2, -l4.y));
+          p[2] = ex2_approx(fmaf(__uint_as_float(sv[e + 2]), c2, -l4.z));
+          p[3] = ex2_approx(fmaf(__uint_as_float(sv[e + 3]), c2, -l4.w));
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (diag && k > q0 + u) p[u] = 0.f;
+            if (!key_ok) p[u] = 0.f;
+          }
+          pb[q0 / 2] = FP16 ? cvt_pack_f16(p[0], p[1]) : cvt_pack_bf16(p[0], p[1]);
+          pb[q0 / 2 + 1] = FP16 ? cvt_pack_f16(p[2], p[3]) : cvt_pack_bf16(p[2], p[3]);
+        }
+        tmem_st16(tmem + lane_addr + C::S_COL + c0 * 16,
+                  *reinterpret_cast<const uint32_t(*)[16]>(&pb[c0 * 16]));
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars.p_ready);
+      // phase B: dS^T = P^T (dP^T - D), from the 16-bit P^T kept in registers
+      if (!(ok = mbar_wait(&bars.dp_full, n & 1, ab, kDevTimeoutSoftmax))) break;
+      if (n > 0 && !(ok = mbar_wait(&bars.ds_free, (n - 1) & 1, ab, kDevTimeoutSoftmax))) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int c0 = 0; c0 < C::BM / 32; ++c0) {
+        uint32_t dpv[32];
         tmem_ld32(tmem + lane_addr + C::DP_COL + c0 * 32, dpv);
         tmem_ld_wait();
-        uint32_t pp[16], dd[16];
+        uint32_t dd[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
+        for (int e = 0; e < 32; e += 4) {
           const int q0 = c0 * 32 + e;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), c2, -lse2[q0]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), c2, -lse2[q0 + 1]));
-          if (diag) {
-            if (k > q0) p0 = 0.f;
-            if (k > q0 + 1) p1 = 0.f;
+          const float4 d4 = dvec4[q0 / 4];
+          // unpack here, not earlier: keeps 64 packed registers live instead of 128 floats
+          const uint32_t pw0 = opaque32(pb[q0 / 2]);
+          const uint32_t pw1 = opaque32(pb[q0 / 2 + 1]);
+          float2 pa, pc;
+          if (FP16) {
+            pa = __half22float2(*reinterpret_cast<const __half2*>(&pw0));
+            pc = __half22float2(*reinterpret_cast<const __half2*>(&pw1));
+          } else {
+            // a bf16 value is the upper half of the float32 with the same bits
+            pa = make_float2(__uint_as_float(pw0 << 16), __uint_as_float(pw0 & 0xffff0000u));
+            pc = make_float2(__uint_as_float(pw1 << 16), __uint_as_float(pw1 & 0xffff0000u));
           }
-          if (!key_ok) {
-            p0 = 0.f;
-            p1 = 0.f;
-          }
-          const float ds0 = p0 * (__uint_as_float(dpv[e]) - dvec[q0]);
-          const float ds1 = p1 * (__uint_as_float(dpv[e + 1]) - dvec[q0 + 1]);
-          pp[e / 2] = FP16 ? cvt_pack_f16(p0, p1) : cvt_pack_bf16(p0, p1);
+          const float ds0 = pa.x * (__uint_as_float(dpv[e + 0]) - d4.x);
+          const float ds1 = pa.y * (__uint_as_float(dpv[e + 1]) - d4.y);
+          const float ds2 = pc.x * (__uint_as_float(dpv[e + 2]) - d4.z);
+          const float ds3 = pc.y * (__uint_as_float(dpv[e + 3]) - d4.w);
           dd[e / 2] = FP16 ? cvt_pack_f16(ds0, ds1) : cvt_pack_bf16(ds0, ds1);
+          dd[e / 2 + 1] = FP16 ? cvt_pack_f16(ds2, ds3) : cvt_pack_bf16(ds2, ds3);
         }
-        tmem_st16(tmem + lane_addr + C::S_COL + c0 * 16, pp);
         tmem_st16(tmem + lane_addr + C::DP_COL + c0 * 16, dd);
         // dS^T row k, queries [32 c0, 32 c0 + 32): chunk c0 / 2, 16-byte pieces
         // (c0 % 2) * 4 .. + 3, placed with the 128-byte swizzle.
@@ -390,7 +453,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before_sync();
-      mbar_arrive(&bars.p_full);
+      mbar_arrive(&bars.ds_ready);
     }
     // ------------------------------------------------------------ epilogue
     if (ok && mbar_wait(&bars.dkv_full, 0, ab, kDevTimeoutEpilogue)) {
@@ -425,26 +488,56 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ reduce WG
-    const int q = threadIdx.x - 128;                 // query row of the tile = TMEM lane
+    const int r = threadIdx.x - 128;                 // TMEM lane: query (d = 64) or head dim (d = 128)
     const uint32_t lane_addr = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    constexpr int NCOL = C::DQ_T ? C::BM : D;       // columns of the dQ tile in TMEM
     for (int n = 0; n < nsteps; ++n) {
       if (!mbar_wait(&bars.dq_full, n & 1, ab, kDevTimeoutReduce)) break;
       tc_fence_after_sync();
-      uint32_t v[D];
+      const int q_base = (i0 + n) * C::BM;
+      if (C::DQ_T) {
+        // lane r = head-dim index; column q = query q_base + q: the warp's 32
+        // lanes cover 32 consecutive floats of one dQ row.  Columns are read
+        // 32 at a time; the tile is released after the last read.
+        float* col = kp.dq_acc + (static_cast<size_t>(bh) * N + q_base) * D + r;
+        const bool full = q_base + C::BM <= N;
+#pragma unroll 1
+        for (int c0 = 0; c0 < C::BM / 32; ++c0) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_addr + C::DQ_COL + c0 * 32, v);
+          tmem_ld_wait();
+          if (c0 == C::BM / 32 - 1) {
+            tc_fence_before_sync();
+            mbar_arrive(&bars.dq_free);
+          }
+          float* cq = col + static_cast<size_t>(c0 * 32) * D;
+          if (full) {
 #pragma unroll
-      for (int c0 = 0; c0 < D / 32; ++c0)
-        tmem_ld32(tmem + lane_addr + C::DQ_COL + c0 * 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(&v[c0 * 32]));
-      tmem_ld_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&bars.dq_free);
-      const int q_g = (i0 + n) * C::BM + q;
-      if (q_g < N) {
-        float* dst = kp.dq_acc + (static_cast<size_t>(bh) * N + q_g) * D;
+            for (int q = 0; q < 32; ++q) red_add_f32(cq + q * D, __uint_as_float(v[q]));
+          } else {
 #pragma unroll
-        for (int e = 0; e < D; e += 4)
-          red_add_v4(dst + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                     __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            for (int q = 0; q < 32; ++q)
+              if (q_base + c0 * 32 + q < N) red_add_f32(cq + q * D, __uint_as_float(v[q]));
+          }
+        }
+      } else {
+        uint32_t v[NCOL];
+#pragma unroll
+        for (int c0 = 0; c0 < NCOL / 32; ++c0)
+          tmem_ld32(tmem + lane_addr + C::DQ_COL + c0 * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(&v[c0 * 32]));
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&bars.dq_free);
+        // lane r = query; its D values are one contiguous dQ row
+        const int q_g = q_base + r;
+        if (q_g < N) {
+          float* dst = kp.dq_acc + (static_cast<size_t>(bh) * N + q_g) * D;
+#pragma unroll
+          for (int e = 0; e < D; e += 4)
+            red_add_v4(dst + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                       __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+        }
       }
     }
   }

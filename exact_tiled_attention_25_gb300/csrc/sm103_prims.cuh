@@ -199,6 +199,25 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// Descriptor of the same operand `byte_off` bytes further on.  The start
+// address field holds address >> 4 in 14 bits, and every shared-memory address
+// here is below 256 KB, so the add cannot carry into the next field.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t byte_off) {
+  return desc + (byte_off >> 4);
+}
+
+// Hide a value from loop-invariant code motion, so descriptors derived from it
+// are formed right before use instead of all being kept live in registers.
+__device__ __forceinline__ uint64_t opaque(uint64_t v) {
+  asm volatile("mov.b64 %0, %0;" : "+l"(v));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t opaque32(uint32_t v) {
+  asm volatile("mov.b32 %0, %0;" : "+r"(v));
+  return v;
+}
+
 // Instruction descriptors.  D is always fp32.  M = 128 (cta_group::1).
 // a_mn / b_mn: operand is MN-major (1) or K-major (0).
 enum class Elt : uint32_t { F16 = 0, BF16 = 1 };
@@ -350,6 +369,10 @@ __device__ __forceinline__ void red_add_v4(float* gptr, float a, float b, float 
   asm volatile("red.global.add.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(gptr), "f"(a), "f"(b), "f"(c),
                "f"(d)
                : "memory");
+}
+
+__device__ __forceinline__ void red_add_f32(float* gptr, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gptr), "f"(a) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c,
