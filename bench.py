@@ -35,9 +35,17 @@ B, H, N, D = 2, 16, 8192, 128
 METRIC = "Attn fwd/bwd TFLOP/s (BF16, FP8) & % of GB300 dense tensor peak, N=8K d=128"
 WORKLOAD = "attention step (bf16 fwd + bf16 bwd + fp8 pre-pass + fp8 fwd), B=2 H=16 N=8192 d=128"
 
-# DRAM bytes per launch of each kernel from the ncu capture summarised in
-# profiles/ (None until a capture of the current kernel exists).
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) per launch of each stage's main kernel, from the
+# ncu captures summarised in profiles/*_b2h16n8192d128.md (non-causal).  An
+# entry is removed whenever its kernel changes after the capture.
+NCU_TRAFFIC = {
+    "fwd_bf16": 249_590_016,      # fwd_kernel: 201.8 MB read + 47.8 MB write
+    "bwd_bf16": 626_711_040,      # bwd_main_kernel: 404.9 MB read + 221.8 MB write
+    "fwd_fp8": 133_623_040,       # fwd_fp8_kernel: 100.8 MB read + 32.9 MB write
+    "fp8_prepass": 484_918_528,   # fp8_quant_kernel: 402.7 MB read + 82.2 MB write
+}
+KERNEL_OF = {"fwd_bf16": "fwd_kernel", "bwd_bf16": "bwd_main_kernel (timed as the whole attn_bwd call)",
+             "fwd_fp8": "fwd_fp8_kernel", "fp8_prepass": "fp8_quant_kernel"}
 
 
 def peaks():
@@ -233,8 +241,9 @@ def run_ours(args, rank, world):
         roof = {"bound": "hbm", "achieved": breakdown[dominant]["gbs"], "peak": pk["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["kernel"] = dominant
-    roof["traffic"] = NCU_TRAFFIC.get(dominant)
+    roof["kernel"] = KERNEL_OF[dominant]
+    roof["traffic"] = None if causal else NCU_TRAFFIC.get(dominant)
+    roof["traffic_unit"] = "bytes per launch (ncu dram read + write)"
     roof["peak_source"] = f"{pk['source']} (bf16 sustained; fp8 = 2x bf16)"
 
     e2e = run_e2e(args, torch, attn, dev, stream, step_parts, causal, scale, q32, k32, v32,
@@ -321,7 +330,7 @@ def cpu_sample_problem(seed=3):
     return [rng.standard_normal((N, D)) for _ in range(4)]
 
 
-def cpu_baseline(args, heads=1):
+def cpu_baseline(args, heads=8):
     """The CPU oracle as it stands, on a bounded sample of the workload: the
     forward and backward of `heads` head(s) at N=8192, d=128."""
     import oracle
@@ -378,7 +387,7 @@ def run_reference(args, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
