@@ -286,22 +286,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const uint32_t sK = smem_u32(smem + C::OFF_K);
       const uint32_t sV = smem_u32(smem + C::OFF_V);
       const uint32_t sDS = smem_u32(smem + C::OFF_DS);
-      bool ok = mbar_wait(&bars.kv_full, 0, ab, kDevTimeoutMma);
-      for (int n = 0; n < nsteps && ok; ++n) {
-        const int st = n % C::NST;
-        if (!(ok = mbar_wait(&bars.stage_full[st], (n / C::NST) & 1, ab, kDevTimeoutMma))) break;
-        tc_fence_after_sync();
-        const uint32_t sQ = smem_u32(smem + C::OFF_RING + st * 2 * C::TILE);
-        const uint32_t sDO = sQ + C::TILE;
-        // Base descriptors of this step (K-major: lbo unused, sbo 1024; MN-major:
-        // lbo = distance between 64-element slabs, sbo 1024); every MMA below
-        // uses one of these advanced by a compile-time byte offset.
+      const uint64_t mK = opaque(sdesc_sw128(sK, C::CHUNK, 1024));
+      const uint64_t mDS = opaque(sdesc_sw128(sDS, C::CHUNK, 1024));
+      // S^T(i) = K_j Q_i^T into the S^T columns
+      auto issue_s = [&](uint32_t sQ) {
         const uint64_t kK = opaque(sdesc_sw128(sK, 16, 1024));
-        const uint64_t kV = opaque(sdesc_sw128(sV, 16, 1024));
         const uint64_t kQ = opaque(sdesc_sw128(sQ, 16, 1024));
-        const uint64_t kDO = opaque(sdesc_sw128(sDO, 16, 1024));
-        // S^T = K_j Q_i^T  (its columns held P^T of the last step, read by the
-        // dV MMA issued before this one)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
@@ -309,11 +299,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                      kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars.s_full);
-        // dP^T = V_j dO_i^T  (at d = 128 these columns held the last dQ^T)
-        if (C::DQ_T && n > 0) {
-          if (!(ok = mbar_wait(&bars.dq_free, (n - 1) & 1, ab, kDevTimeoutMma))) break;
-          tc_fence_after_sync();
-        }
+      };
+      // dP^T(i) = V_j dO_i^T into the dP^T columns
+      auto issue_dp = [&](uint32_t sDO) {
+        const uint64_t kV = opaque(sdesc_sw128(sV, 16, 1024));
+        const uint64_t kDO = opaque(sdesc_sw128(sDO, 16, 1024));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
@@ -321,6 +311,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                      kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars.dp_full);
+      };
+      auto stage_q = [&](int n) { return smem_u32(smem + C::OFF_RING + (n % C::NST) * 2 * C::TILE); };
+      // Issue order per step n (each MMA waits only for what it reads):
+      //   dV(n)  [P^T(n) ready]      S^T(n+1)  [stage n+1 loaded]
+      //   dK(n)  [dS^T(n) ready]     dQ(n)
+      //   dP^T(n+1)  [dQ(n) read out of the dP^T columns when they are shared]
+      // so the compute warpgroup's dS phase of step n runs under S^T(n+1) and its
+      // P phase of step n+1 runs under dK(n) and dQ(n).
+      bool ok = mbar_wait(&bars.kv_full, 0, ab, kDevTimeoutMma) &&
+                mbar_wait(&bars.stage_full[0], 0, ab, kDevTimeoutMma);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_s(stage_q(0));
+        issue_dp(stage_q(0) + C::TILE);
+      }
+      for (int n = 0; n < nsteps && ok; ++n) {
+        const int st = n % C::NST;
+        const uint32_t sQ = stage_q(n);
+        const uint32_t sDO = sQ + C::TILE;
         // dV += P^T dO_i  (A = P^T from tensor memory)
         if (!(ok = mbar_wait(&bars.p_ready, n & 1, ab, kDevTimeoutMma))) break;
         tc_fence_after_sync();
@@ -329,6 +338,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int kk = 0; kk < C::BM / 16; ++kk)
           mma_f16_ts(tmem + C::DV_COL, tmem + C::S_COL + kk * 8, sdesc_add(mDO, kk * 16 * 128),
                      idKV, (n > 0 || kk > 0) ? 1u : 0u);
+        // S^T of the next step (its columns now only hold P^T(n), read by dV above)
+        if (n + 1 < nsteps) {
+          if (!(ok = mbar_wait(&bars.stage_full[(n + 1) % C::NST], ((n + 1) / C::NST) & 1, ab,
+                               kDevTimeoutMma)))
+            break;
+          tc_fence_after_sync();
+          issue_s(stage_q(n + 1));
+        }
         // dK += dS^T Q_i  (A = dS^T from tensor memory)
         if (!(ok = mbar_wait(&bars.ds_ready, n & 1, ab, kDevTimeoutMma))) break;
         tc_fence_after_sync();
@@ -337,13 +354,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int kk = 0; kk < C::BM / 16; ++kk)
           mma_f16_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8, sdesc_add(mQ, kk * 16 * 128),
                      idKV, (n > 0 || kk > 0) ? 1u : 0u);
-        // dQ_i = dS K_j (d = 64), or dQ_i^T = K_j^T dS^T (d = 128)
+        // dQ_i = dS K_j (d = 64), or dQ_i^T = K_j^T dS^T (d = 128, into the dP^T columns)
         if (!C::DQ_T && n > 0) {
           if (!(ok = mbar_wait(&bars.dq_free, (n - 1) & 1, ab, kDevTimeoutMma))) break;
           tc_fence_after_sync();
         }
-        const uint64_t mDS = opaque(sdesc_sw128(sDS, C::CHUNK, 1024));
-        const uint64_t mK = opaque(sdesc_sw128(sK, C::CHUNK, 1024));
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
           const uint64_t dds = sdesc_add(mDS, kk * 16 * 128);
@@ -356,6 +371,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         mma_commit(&bars.dq_full);
         if (n + 1 < nsteps) mma_commit(&bars.ds_free);
         if (n + C::NST < nsteps) mma_commit(&bars.stage_empty[st]);
+        // dP^T of the next step
+        if (n + 1 < nsteps) {
+          if (C::DQ_T) {
+            if (!(ok = mbar_wait(&bars.dq_free, n & 1, ab, kDevTimeoutMma))) break;
+            tc_fence_after_sync();
+          }
+          issue_dp(stage_q(n + 1) + C::TILE);
+        }
       }
       if (ok) mma_commit(&bars.dkv_full);
     }
@@ -497,28 +520,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const int q_base = (i0 + n) * C::BM;
       if (C::DQ_T) {
         // lane r = head-dim index; column q = query q_base + q: the warp's 32
-        // lanes cover 32 consecutive floats of one dQ row.  Columns are read
-        // 32 at a time; the tile is released after the last read.
+        // lanes cover 32 consecutive floats of one dQ row.  All columns are read
+        // first so the tile is handed back before the reductions are issued.
+        uint32_t v[C::BM];
+#pragma unroll
+        for (int c0 = 0; c0 < C::BM / 32; ++c0)
+          tmem_ld32(tmem + lane_addr + C::DQ_COL + c0 * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(&v[c0 * 32]));
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&bars.dq_free);
         float* col = kp.dq_acc + (static_cast<size_t>(bh) * N + q_base) * D + r;
-        const bool full = q_base + C::BM <= N;
-#pragma unroll 1
-        for (int c0 = 0; c0 < C::BM / 32; ++c0) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_addr + C::DQ_COL + c0 * 32, v);
-          tmem_ld_wait();
-          if (c0 == C::BM / 32 - 1) {
-            tc_fence_before_sync();
-            mbar_arrive(&bars.dq_free);
-          }
-          float* cq = col + static_cast<size_t>(c0 * 32) * D;
-          if (full) {
+        if (q_base + C::BM <= N) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q) red_add_f32(cq + q * D, __uint_as_float(v[q]));
-          } else {
+          for (int q = 0; q < C::BM; ++q) red_add_f32(col + q * D, __uint_as_float(v[q]));
+        } else {
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-              if (q_base + c0 * 32 + q < N) red_add_f32(cq + q * D, __uint_as_float(v[q]));
-          }
+          for (int q = 0; q < C::BM; ++q)
+            if (q_base + q < N) red_add_f32(col + q * D, __uint_as_float(v[q]));
         }
       } else {
         uint32_t v[NCOL];
