@@ -69,9 +69,18 @@ struct BwdCfg {
   static constexpr uint32_t DV_COL = 256;
   static constexpr uint32_t DK_COL = 256 + D;
   static constexpr uint32_t DQ_COL = DQ_T ? DP_COL : 256 + 2 * D;
-  static constexpr int THREADS = 320;            // compute WG, reduce WG, load warp, MMA warp
-  static constexpr int LOAD_WARP = 8;
-  static constexpr int MMA_WARP = 9;
+  // Warps 0-7: two compute warpgroups (one per half of the 128 query columns);
+  // warps 8-15: two reduce warpgroups (one per half of the dQ tile's columns);
+  // warp 16: TMA producer; warp 17: MMA issuer.
+  static constexpr int THREADS = 576;
+  static constexpr int LOAD_WARP = 16;
+  static constexpr int MMA_WARP = 17;
+  // Packed 16-bit P^T / dS^T of query half h sit in columns [64 h, 64 h + 32) of
+  // the S^T / dP^T region, inside the half's own fp32 columns, so each
+  // warpgroup overwrites only scores it has already read.
+  __host__ __device__ static constexpr uint32_t half_col(int kk) {
+    return 64u * static_cast<uint32_t>(kk / 4) + 8u * static_cast<uint32_t>(kk % 4);
+  }
   static_assert(DQ_COL + D <= 512 && DK_COL + D <= 512, "TMEM overflow");
   static_assert(SLACK >= 0, "shared memory overflow");
 };
@@ -218,10 +227,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.p_ready, 128);
-    mbar_init(&bars.ds_ready, 128);
+    mbar_init(&bars.p_ready, 256);
+    mbar_init(&bars.ds_ready, 256);
     mbar_init(&bars.dq_full, 1);
-    mbar_init(&bars.dq_free, 128);
+    mbar_init(&bars.dq_free, 256);
     mbar_init(&bars.ds_free, 1);
     mbar_init(&bars.dkv_full, 1);
     mbar_init(&bars.drain, 1);
@@ -314,11 +323,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       };
       auto stage_q = [&](int n) { return smem_u32(smem + C::OFF_RING + (n % C::NST) * 2 * C::TILE); };
       // Issue order per step n (each MMA waits only for what it reads):
-      //   dV(n)  [P^T(n) ready]      S^T(n+1)  [stage n+1 loaded]
-      //   dK(n)  [dS^T(n) ready]     dQ(n)
-      //   dP^T(n+1)  [dQ(n) read out of the dP^T columns when they are shared]
-      // so the compute warpgroup's dS phase of step n runs under S^T(n+1) and its
-      // P phase of step n+1 runs under dK(n) and dQ(n).
+      //   dV(n) [P^T(n) ready]   dP^T(n) [n > 0; at d = 128 after dQ(n-1) was read
+      //   out of the shared columns]   S^T(n+1) [stage n+1 loaded]
+      //   dK(n) [dS^T(n) ready]   dQ(n)
+      // so reading dQ(n-1) out of tensor memory overlaps dV(n), the dS phase of
+      // step n overlaps S^T(n+1), and the P phase of step n+1 overlaps dK(n), dQ(n).
       bool ok = mbar_wait(&bars.kv_full, 0, ab, kDevTimeoutMma) &&
                 mbar_wait(&bars.stage_full[0], 0, ab, kDevTimeoutMma);
       if (ok) {
@@ -336,8 +345,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const uint64_t mDO = opaque(sdesc_sw128(sDO, C::CHUNK, 1024));
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_f16_ts(tmem + C::DV_COL, tmem + C::S_COL + kk * 8, sdesc_add(mDO, kk * 16 * 128),
+          mma_f16_ts(tmem + C::DV_COL, tmem + C::S_COL + C::half_col(kk), sdesc_add(mDO, kk * 16 * 128),
                      idKV, (n > 0 || kk > 0) ? 1u : 0u);
+        // dP^T of this step (step 0's was issued with S^T(0))
+        if (n > 0) {
+          if (C::DQ_T) {
+            if (!(ok = mbar_wait(&bars.dq_free, (n - 1) & 1, ab, kDevTimeoutMma))) break;
+            tc_fence_after_sync();
+          }
+          issue_dp(sDO);
+        }
         // S^T of the next step (its columns now only hold P^T(n), read by dV above)
         if (n + 1 < nsteps) {
           if (!(ok = mbar_wait(&bars.stage_full[(n + 1) % C::NST], ((n + 1) / C::NST) & 1, ab,
@@ -346,14 +363,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tc_fence_after_sync();
           issue_s(stage_q(n + 1));
         }
-        // dK += dS^T Q_i  (A = dS^T from tensor memory)
+        // dK += dS^T Q_i  (A = dS^T from tensor memory); the stage is free after it
         if (!(ok = mbar_wait(&bars.ds_ready, n & 1, ab, kDevTimeoutMma))) break;
         tc_fence_after_sync();
         const uint64_t mQ = opaque(sdesc_sw128(sQ, C::CHUNK, 1024));
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_f16_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8, sdesc_add(mQ, kk * 16 * 128),
+          mma_f16_ts(tmem + C::DK_COL, tmem + C::DP_COL + C::half_col(kk), sdesc_add(mQ, kk * 16 * 128),
                      idKV, (n > 0 || kk > 0) ? 1u : 0u);
+        if (n + C::NST < nsteps) mma_commit(&bars.stage_empty[st]);
         // dQ_i = dS K_j (d = 64), or dQ_i^T = K_j^T dS^T (d = 128, into the dP^T columns)
         if (!C::DQ_T && n > 0) {
           if (!(ok = mbar_wait(&bars.dq_free, (n - 1) & 1, ab, kDevTimeoutMma))) break;
@@ -370,26 +388,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         mma_commit(&bars.dq_full);
         if (n + 1 < nsteps) mma_commit(&bars.ds_free);
-        if (n + C::NST < nsteps) mma_commit(&bars.stage_empty[st]);
-        // dP^T of the next step
-        if (n + 1 < nsteps) {
-          if (C::DQ_T) {
-            if (!(ok = mbar_wait(&bars.dq_free, n & 1, ab, kDevTimeoutMma))) break;
-            tc_fence_after_sync();
-          }
-          issue_dp(stage_q(n + 1) + C::TILE);
-        }
       }
       if (ok) mma_commit(&bars.dkv_full);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ compute WG
-    const int k = threadIdx.x;                       // key row of the tile = TMEM lane
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ compute WGs
+    const int h = warp >> 2;                         // query half: columns [64 h, 64 h + 64)
+    const int quarter = warp & 3;
+    const int k = quarter * 32 + lane;               // key row of the tile = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const int key_g = j * C::BN + k;
     const bool key_ok = key_g < N;
     const float c2 = kp.scale_log2;
-    const uint32_t sDSrow = smem_u32(smem + C::OFF_DS) + k * 128;
+    const uint32_t sDSrow = smem_u32(smem + C::OFF_DS) + h * C::CHUNK + k * 128;
     bool ok = true;
     for (int n = 0; n < nsteps; ++n) {
       const int st = n % C::NST;
@@ -397,18 +408,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + st * 1024);
       const float4* dvec4 = lse4 + 32;
       const bool diag = CAUSAL && i == j;
-      // phase A: P^T = exp2(S^T c - L log2 e), written back over S^T as 16-bit
+      // phase A: P^T = exp2(S^T c - L log2 e), written back as 16-bit
       if (!(ok = mbar_wait(&bars.s_full, n & 1, ab, kDevTimeoutSoftmax))) break;
       tc_fence_after_sync();
-      uint32_t pb[C::BM / 2];
+      uint32_t pb[32];                               // this half's P^T, packed pairs
 #pragma unroll
-      for (int c0 = 0; c0 < C::BM / 32; ++c0) {
-        uint32_t sv[32];
-        tmem_ld32(tmem + lane_addr + C::S_COL + c0 * 32, sv);
+      for (int c = 0; c < 4; ++c) {
+        const int qb = 64 * h + 16 * c;
+        uint32_t sv[16];
+        tmem_ld16(tmem + lane_addr + C::S_COL + qb, sv);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const int q0 = c0 * 32 + e;
+        for (int e = 0; e < 16; e += 4) {
+          const int q0 = qb + e;
           const float4 l4 = lse4[q0 / 4];
           float p[4];
           p[0] = ex2_approx(fmaf(__uint_as_float(sv[e + 0]), c2, -l4.x));
@@ -420,11 +432,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             if (diag && k > q0 + u) p[u] = 0.f;
             if (!key_ok) p[u] = 0.f;
           }
-          pb[q0 / 2] = FP16 ? cvt_pack_f16(p[0], p[1]) : cvt_pack_bf16(p[0], p[1]);
-          pb[q0 / 2 + 1] = FP16 ? cvt_pack_f16(p[2], p[3]) : cvt_pack_bf16(p[2], p[3]);
+          pb[(16 * c + e) / 2] = FP16 ? cvt_pack_f16(p[0], p[1]) : cvt_pack_bf16(p[0], p[1]);
+          pb[(16 * c + e) / 2 + 1] = FP16 ? cvt_pack_f16(p[2], p[3]) : cvt_pack_bf16(p[2], p[3]);
         }
-        tmem_st16(tmem + lane_addr + C::S_COL + c0 * 16,
-                  *reinterpret_cast<const uint32_t(*)[16]>(&pb[c0 * 16]));
+        tmem_st_x8(tmem + lane_addr + C::S_COL + 64 * h + 8 * c,
+                   *reinterpret_cast<const uint32_t(*)[8]>(&pb[8 * c]));
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -434,18 +446,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (n > 0 && !(ok = mbar_wait(&bars.ds_free, (n - 1) & 1, ab, kDevTimeoutSoftmax))) break;
       tc_fence_after_sync();
 #pragma unroll
-      for (int c0 = 0; c0 < C::BM / 32; ++c0) {
-        uint32_t dpv[32];
-        tmem_ld32(tmem + lane_addr + C::DP_COL + c0 * 32, dpv);
+      for (int c = 0; c < 4; ++c) {
+        const int qb = 64 * h + 16 * c;
+        uint32_t dpv[16];
+        tmem_ld16(tmem + lane_addr + C::DP_COL + qb, dpv);
         tmem_ld_wait();
-        uint32_t dd[16];
+        uint32_t dd[8];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const int q0 = c0 * 32 + e;
+        for (int e = 0; e < 16; e += 4) {
+          const int q0 = qb + e;
           const float4 d4 = dvec4[q0 / 4];
-          // unpack here, not earlier: keeps 64 packed registers live instead of 128 floats
-          const uint32_t pw0 = opaque32(pb[q0 / 2]);
-          const uint32_t pw1 = opaque32(pb[q0 / 2 + 1]);
+          // unpack here, not earlier: keeps packed registers live instead of floats
+          const uint32_t pw0 = opaque32(pb[(16 * c + e) / 2]);
+          const uint32_t pw1 = opaque32(pb[(16 * c + e) / 2 + 1]);
           float2 pa, pc;
           if (FP16) {
             pa = __half22float2(*reinterpret_cast<const __half2*>(&pw0));
@@ -462,14 +475,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           dd[e / 2] = FP16 ? cvt_pack_f16(ds0, ds1) : cvt_pack_bf16(ds0, ds1);
           dd[e / 2 + 1] = FP16 ? cvt_pack_f16(ds2, ds3) : cvt_pack_bf16(ds2, ds3);
         }
-        tmem_st16(tmem + lane_addr + C::DP_COL + c0 * 16, dd);
-        // dS^T row k, queries [32 c0, 32 c0 + 32): chunk c0 / 2, 16-byte pieces
-        // (c0 % 2) * 4 .. + 3, placed with the 128-byte swizzle.
-        const uint32_t base = sDSrow + (c0 / 2) * C::CHUNK;
+        tmem_st_x8(tmem + lane_addr + C::DP_COL + 64 * h + 8 * c, dd);
+        // dS^T row k, queries [qb, qb + 16) = 16-byte pieces 2c and 2c + 1 of
+        // chunk h, placed with the 128-byte swizzle
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
-          const uint32_t piece = static_cast<uint32_t>((c0 % 2) * 4 + pc);
-          st_shared_v4(base + ((piece ^ (k & 7)) * 16), dd[4 * pc], dd[4 * pc + 1],
+        for (int pc = 0; pc < 2; ++pc) {
+          const uint32_t piece = static_cast<uint32_t>(2 * c + pc);
+          st_shared_v4(sDSrow + ((piece ^ (k & 7)) * 16), dd[4 * pc], dd[4 * pc + 1],
                        dd[4 * pc + 2], dd[4 * pc + 3]);
         }
       }
@@ -479,81 +491,75 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_arrive(&bars.ds_ready);
     }
     // ------------------------------------------------------------ epilogue
+    // half 0 stores dV, half 1 stores dK (scaled by softmax_scale)
     if (ok && mbar_wait(&bars.dkv_full, 0, ab, kDevTimeoutEpilogue)) {
       tc_fence_after_sync();
-      uint16_t* dvrow = static_cast<uint16_t*>(kp.dv) + (static_cast<size_t>(bh) * N + key_g) * D;
-      uint16_t* dkrow = static_cast<uint16_t*>(kp.dk) + (static_cast<size_t>(bh) * N + key_g) * D;
+      const uint32_t col = h ? C::DK_COL : C::DV_COL;
+      const float mul = h ? kp.scale : 1.f;
+      uint16_t* dst_row = static_cast<uint16_t*>(h ? kp.dk : kp.dv) +
+                          (static_cast<size_t>(bh) * N + key_g) * D;
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which ? C::DK_COL : C::DV_COL;
-        const float mul = which ? kp.scale : 1.f;
-        uint16_t* dst_row = which ? dkrow : dvrow;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D / 32; ++c0) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_addr + col + c0 * 32, v);
-          tmem_ld_wait();
-          uint32_t pk[16];
+      for (int c0 = 0; c0 < D / 32; ++c0) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_addr + col + c0 * 32, v);
+        tmem_ld_wait();
+        uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float a = __uint_as_float(v[2 * e]) * mul;
-            const float b = __uint_as_float(v[2 * e + 1]) * mul;
-            pk[e] = FP16 ? cvt_pack_f16(a, b) : cvt_pack_bf16(a, b);
-          }
-          if (key_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(dst_row + c0 * 32);
+        for (int e = 0; e < 16; ++e) {
+          const float a = __uint_as_float(v[2 * e]) * mul;
+          const float b = __uint_as_float(v[2 * e + 1]) * mul;
+          pk[e] = FP16 ? cvt_pack_f16(a, b) : cvt_pack_bf16(a, b);
+        }
+        if (key_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + c0 * 32);
 #pragma unroll
-            for (int x = 0; x < 4; ++x)
-              dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
-          }
+          for (int x = 0; x < 4; ++x)
+            dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
         }
       }
     }
   } else {
-    // ------------------------------------------------------------ dQ reduce WG
-    const int r = threadIdx.x - 128;                 // TMEM lane: query (d = 64) or head dim (d = 128)
-    const uint32_t lane_addr = static_cast<uint32_t>((warp - 4) * 32) << 16;
-    constexpr int NCOL = C::DQ_T ? C::BM : D;       // columns of the dQ tile in TMEM
+    // ------------------------------------------------------------ dQ reduce WGs
+    // TMEM lane r: head-dim index (d = 128, transposed tile) or query (d = 64).
+    // Reduce warpgroup g handles half the tile's columns.
+    const int g = (warp - 8) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    constexpr int HC = (C::DQ_T ? C::BM : D) / 2;    // columns per reduce warpgroup
     for (int n = 0; n < nsteps; ++n) {
       if (!mbar_wait(&bars.dq_full, n & 1, ab, kDevTimeoutReduce)) break;
       tc_fence_after_sync();
+      // read this half of the tile, hand the columns back, then reduce
+      uint32_t v[HC];
+#pragma unroll
+      for (int c0 = 0; c0 < HC / 32; ++c0)
+        tmem_ld32(tmem + lane_addr + C::DQ_COL + g * HC + c0 * 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(&v[c0 * 32]));
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars.dq_free);
       const int q_base = (i0 + n) * C::BM;
       if (C::DQ_T) {
-        // lane r = head-dim index; column q = query q_base + q: the warp's 32
-        // lanes cover 32 consecutive floats of one dQ row.  All columns are read
-        // first so the tile is handed back before the reductions are issued.
-        uint32_t v[C::BM];
+        // column q = query q_base + g HC + q: the warp's 32 lanes cover 32
+        // consecutive floats of one dQ row (one 128-byte line per reduction)
+        const int q0 = q_base + g * HC;
+        float* col = kp.dq_acc + (static_cast<size_t>(bh) * N + q0) * D + r;
+        if (q0 + HC <= N) {
 #pragma unroll
-        for (int c0 = 0; c0 < C::BM / 32; ++c0)
-          tmem_ld32(tmem + lane_addr + C::DQ_COL + c0 * 32,
-                    *reinterpret_cast<uint32_t(*)[32]>(&v[c0 * 32]));
-        tmem_ld_wait();
-        tc_fence_before_sync();
-        mbar_arrive(&bars.dq_free);
-        float* col = kp.dq_acc + (static_cast<size_t>(bh) * N + q_base) * D + r;
-        if (q_base + C::BM <= N) {
-#pragma unroll
-          for (int q = 0; q < C::BM; ++q) red_add_f32(col + q * D, __uint_as_float(v[q]));
+          for (int q = 0; q < HC; ++q) red_add_f32(col + q * D, __uint_as_float(v[q]));
         } else {
 #pragma unroll
-          for (int q = 0; q < C::BM; ++q)
-            if (q_base + q < N) red_add_f32(col + q * D, __uint_as_float(v[q]));
+          for (int q = 0; q < HC; ++q)
+            if (q0 + q < N) red_add_f32(col + q * D, __uint_as_float(v[q]));
         }
       } else {
-        uint32_t v[NCOL];
-#pragma unroll
-        for (int c0 = 0; c0 < NCOL / 32; ++c0)
-          tmem_ld32(tmem + lane_addr + C::DQ_COL + c0 * 32,
-                    *reinterpret_cast<uint32_t(*)[32]>(&v[c0 * 32]));
-        tmem_ld_wait();
-        tc_fence_before_sync();
-        mbar_arrive(&bars.dq_free);
-        // lane r = query; its D values are one contiguous dQ row
+        // lane r = query; columns g HC .. g HC + HC of its dQ row
         const int q_g = q_base + r;
         if (q_g < N) {
-          float* dst = kp.dq_acc + (static_cast<size_t>(bh) * N + q_g) * D;
+          float* dst = kp.dq_acc + (static_cast<size_t>(bh) * N + q_g) * D + g * HC;
 #pragma unroll
-          for (int e = 0; e < D; e += 4)
+          for (int e = 0; e < HC; e += 4)
             red_add_v4(dst + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
                        __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
         }
