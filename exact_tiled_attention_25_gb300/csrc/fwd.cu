@@ -181,6 +181,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       constexpr Elt E = FP16 ? Elt::F16 : Elt::BF16;
       constexpr uint32_t idS = idesc_f16(E, 128, BN, false, false);
       constexpr uint32_t idPV = idesc_f16(E, 128, D, false, true);
+      const uint64_t qdesc0 = sdesc_sw128(smem_u32(sQ), 16, 1024);            // K-major Q
+      const uint64_t kvdesc0 = sdesc_sw128(smem_u32(sKV), 16, 1024);          // K-major K
+      const uint64_t vdesc0 = sdesc_sw128(smem_u32(sKV), C::CHUNK_BYTES, 1024);  // MN-major V
       bool ok = true;
 #pragma unroll
       for (int t = 0; t < NQ; ++t)
@@ -199,6 +202,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           break;
         }
         tc_fence_after_sync();
+        // base descriptors of this iteration's K_j and V_{j-1} slots; every MMA
+        // below adds a compile-time byte offset to one of them
+        const uint64_t kdesc = opaque(sdesc_add(kvdesc0, slotK * C::TILE_BYTES));
+        const uint64_t vdesc = opaque(sdesc_add(vdesc0, slotV * C::TILE_BYTES));
 #pragma unroll
         for (int t = 0; t < NQ; ++t) {
           if (j >= 1 && j - 1 < nK[t]) {
@@ -208,24 +215,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               break;
             }
             tc_fence_after_sync();
-            const uint32_t vbase = smem_u32(sKV + slotV * C::TILE_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, C::CHUNK_BYTES, 1024);
-              mma_f16_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, bdesc, idPV,
-                         (j - 1 > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_f16_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8,
+                         sdesc_add(vdesc, kk * 16 * 128), idPV, (j - 1 > 0 || kk > 0) ? 1u : 0u);
             if (j - 1 == nK[t] - 1) mma_commit(&o_full[t]);
           }
           if (j < nK[t]) {
             // S_t(j) = Q_t K_j^T
-            const uint32_t qbase = smem_u32(sQ + t * C::TILE_BYTES);
-            const uint32_t kbase = smem_u32(sKV + slotK * C::TILE_BYTES);
+            const uint64_t qdesc = sdesc_add(qdesc0, t * C::TILE_BYTES);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32;
-              mma_f16_ss(tmem + C::S_COL(t), sdesc_sw128(qbase + off, 16, 1024),
-                         sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+              mma_f16_ss(tmem + C::S_COL(t), sdesc_add(qdesc, off), sdesc_add(kdesc, off), idS,
+                         kk > 0 ? 1u : 0u);
             }
             mma_commit(&s_full[t]);
           }
@@ -270,15 +273,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int c = 0; c < BN; ++c)
           if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      // row max as a tree of 3-input maxima (short dependency chains)
+      float mx[16];
 #pragma unroll
-      for (int c = 0; c < BN; c += 8) {
-        mx0 = fmax3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
-        mx1 = fmax3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-        mx2 = fmax3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-        mx3 = fmax3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
-      }
-      const float m_new = fmaxf(m_ref, fmax3(mx0, mx1, fmaxf(mx2, mx3)));
+      for (int u = 0; u < 16; ++u)
+        mx[u] = fmax3(__uint_as_float(sr[8 * u]), __uint_as_float(sr[8 * u + 1]),
+                      fmax3(__uint_as_float(sr[8 * u + 2]), __uint_as_float(sr[8 * u + 3]),
+                            fmax3(__uint_as_float(sr[8 * u + 4]), __uint_as_float(sr[8 * u + 5]),
+                                  fmaxf(__uint_as_float(sr[8 * u + 6]), __uint_as_float(sr[8 * u + 7])))));
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], mx[u + 8]);
+      const float m_new = fmaxf(m_ref, fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                             fmaxf(mx[6], mx[7])));
       // Move the exponent reference only when the max grew by more than 2^8.
       const bool need = (m_new - m_ref) * c2 > 8.f;
       float alpha = 1.f;
