@@ -112,6 +112,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     nKmax = max(nKmax, nK[t]);
   }
   const int total_items = 2 * nKmax;   // K_0, V_0, K_1, V_1, ...
+  // The last query tile with work runs every key tile; when its S(j) completes,
+  // all MMAs reading K_j and V_{j-1} (of every tile) have completed, so its
+  // softmax warpgroup hands those ring slots back to the producer.
+  const int t_rel = (nK[NQ - 1] == nKmax) ? NQ - 1 : 0;
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < NQ; ++t) {
@@ -189,31 +193,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int t = 0; t < NQ; ++t)
         if (ok && nK[t] > 0) ok = mbar_wait(&q_full[t], 0, ab, kDevTimeoutMma);
       for (int j = 0; j <= nKmax && ok; ++j) {
-        const int itK = 2 * j;
-        const int itV = 2 * (j - 1) + 1;
+        const int itK = 2 * j;          // ring item of K_j
+        const int itV = 2 * j - 1;      // ring item of V_{j-1}
         const int slotK = itK % NSLOT;
         const int slotV = (itV + NSLOT) % NSLOT;
-        if (j < nKmax && !mbar_wait(&kv_full[slotK], (itK / NSLOT) & 1, ab, kDevTimeoutMma)) {
-          ok = false;
-          break;
-        }
-        if (j >= 1 && !mbar_wait(&kv_full[slotV], (itV / NSLOT) & 1, ab, kDevTimeoutMma)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        // base descriptors of this iteration's K_j and V_{j-1} slots; every MMA
-        // below adds a compile-time byte offset to one of them
-        const uint64_t kdesc = opaque(sdesc_add(kvdesc0, slotK * C::TILE_BYTES));
-        const uint64_t vdesc = opaque(sdesc_add(vdesc0, slotV * C::TILE_BYTES));
+        bool haveK = false, haveV = false;
+        uint64_t kdesc = 0, vdesc = 0;
 #pragma unroll
         for (int t = 0; t < NQ; ++t) {
           if (j >= 1 && j - 1 < nK[t]) {
             // O_t += P_t(j-1) V_{j-1}
-            if (!mbar_wait(&p_full[t], (j - 1) & 1, ab, kDevTimeoutMma)) {
-              ok = false;
-              break;
+            if (!haveV) {
+              if (!(ok = mbar_wait(&kv_full[slotV], (itV / NSLOT) & 1, ab, kDevTimeoutMma))) break;
+              vdesc = opaque(sdesc_add(vdesc0, slotV * C::TILE_BYTES));
+              haveV = true;
             }
+            if (!(ok = mbar_wait(&p_full[t], (j - 1) & 1, ab, kDevTimeoutMma))) break;
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
@@ -223,6 +218,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
           if (j < nK[t]) {
             // S_t(j) = Q_t K_j^T
+            if (!haveK) {
+              if (!(ok = mbar_wait(&kv_full[slotK], (itK / NSLOT) & 1, ab, kDevTimeoutMma))) break;
+              tc_fence_after_sync();
+              kdesc = opaque(sdesc_add(kvdesc0, slotK * C::TILE_BYTES));
+              haveK = true;
+            }
             const uint64_t qdesc = sdesc_add(qdesc0, t * C::TILE_BYTES);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -234,9 +235,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
         }
         if (!ok) break;
-        // hand ring slots back to the producer once the MMAs reading them finish
-        if (j >= 1 && itV + NSLOT < total_items) mma_commit(&kv_empty[slotV]);
-        if (j < nKmax && itK + NSLOT < total_items) mma_commit(&kv_empty[slotK]);
       }
     }
   } else {
@@ -261,6 +259,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         break;
       }
       tc_fence_after_sync();
+      if (t == t_rel && r == 0) {
+        // release only slots the producer refills
+        if (2 * j + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j) % NSLOT]);
+        if (j >= 1 && 2 * j - 1 + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j - 1) % NSLOT]);
+      }
       uint32_t sr[BN];
 #pragma unroll
       for (int c0 = 0; c0 < BN / 32; ++c0)
