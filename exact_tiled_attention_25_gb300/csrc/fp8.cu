@@ -210,6 +210,10 @@ __global__ void __launch_bounds__(THREADS8, 1)
     nKmax = max(nKmax, nK[t]);
   }
   const int total_items = 2 * nKmax;
+  // The last query tile with work runs every key tile; when its S(j) completes,
+  // all MMAs reading K_j and V_{j-1} have completed, so its softmax warpgroup
+  // hands those ring slots back to the producer.
+  const int t_rel = (nK[NQ8 - 1] == nKmax) ? NQ8 - 1 : 0;
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < NQ8; ++t) {
@@ -269,55 +273,54 @@ __global__ void __launch_bounds__(THREADS8, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_e4m3(128, BN, false, false);
       constexpr uint32_t idPV = idesc_e4m3(128, D8, false, true);
+      const uint64_t qdesc0 = sdesc_sw128(smem_u32(sQ), 16, 1024);     // K-major Q
+      const uint64_t kdesc0 = sdesc_sw128(smem_u32(sKV), 16, 1024);    // K-major K
+      const uint64_t vdesc0 = sdesc_sw128(smem_u32(sKV), TILE8, 1024); // MN-major V
       bool ok = true;
 #pragma unroll
       for (int t = 0; t < NQ8; ++t)
         if (ok && nK[t] > 0) ok = mbar_wait(&q_full[t], 0, ab, kDevTimeoutMma);
       for (int j = 0; j <= nKmax && ok; ++j) {
-        const int itK = 2 * j;
-        const int itV = 2 * (j - 1) + 1;
+        const int itK = 2 * j;          // ring item of K_j
+        const int itV = 2 * j - 1;      // ring item of V_{j-1}
         const int slotK = itK % NSLOT8;
         const int slotV = (itV + NSLOT8) % NSLOT8;
-        if (j < nKmax && !mbar_wait(&kv_full[slotK], (itK / NSLOT8) & 1, ab, kDevTimeoutMma)) {
-          ok = false;
-          break;
-        }
-        if (j >= 1 && !mbar_wait(&kv_full[slotV], (itV / NSLOT8) & 1, ab, kDevTimeoutMma)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
+        bool haveK = false, haveV = false;
+        uint64_t kdesc = 0, vdesc = 0;
 #pragma unroll
         for (int t = 0; t < NQ8; ++t) {
           if (j >= 1 && j - 1 < nK[t]) {
-            if (!mbar_wait(&p_full[t], (j - 1) & 1, ab, kDevTimeoutMma)) {
-              ok = false;
-              break;
+            // O_t += P_t(j-1) V_{j-1}
+            if (!haveV) {
+              if (!(ok = mbar_wait(&kv_full[slotV], (itV / NSLOT8) & 1, ab, kDevTimeoutMma))) break;
+              vdesc = opaque(sdesc_add(vdesc0, slotV * TILE8));
+              haveV = true;
             }
+            if (!(ok = mbar_wait(&p_full[t], (j - 1) & 1, ab, kDevTimeoutMma))) break;
             tc_fence_after_sync();
-            const uint32_t vbase = smem_u32(sKV + slotV * TILE8);
 #pragma unroll
-            for (int kk = 0; kk < BN / 32; ++kk) {
-              const uint64_t bdesc = sdesc_sw128(vbase + kk * 32 * 128, TILE8, 1024);
-              mma_f8_ts(tmem + o_col8(t), tmem + s_col8(t) + kk * 8, bdesc, idPV,
-                        (j - 1 > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < BN / 32; ++kk)
+              mma_f8_ts(tmem + o_col8(t), tmem + s_col8(t) + kk * 8, sdesc_add(vdesc, kk * 32 * 128),
+                        idPV, (j - 1 > 0 || kk > 0) ? 1u : 0u);
             if (j - 1 == nK[t] - 1) mma_commit(&o_full[t]);
           }
           if (j < nK[t]) {
-            const uint32_t qbase = smem_u32(sQ + t * TILE8);
-            const uint32_t kbase = smem_u32(sKV + slotK * TILE8);
-#pragma unroll
-            for (int kk = 0; kk < D8 / 32; ++kk) {
-              mma_f8_ss(tmem + s_col8(t), sdesc_sw128(qbase + kk * 32, 16, 1024),
-                        sdesc_sw128(kbase + kk * 32, 16, 1024), idS, kk > 0 ? 1u : 0u);
+            // S_t(j) = Q_t K_j^T
+            if (!haveK) {
+              if (!(ok = mbar_wait(&kv_full[slotK], (itK / NSLOT8) & 1, ab, kDevTimeoutMma))) break;
+              tc_fence_after_sync();
+              kdesc = opaque(sdesc_add(kdesc0, slotK * TILE8));
+              haveK = true;
             }
+            const uint64_t qdesc = sdesc_add(qdesc0, t * TILE8);
+#pragma unroll
+            for (int kk = 0; kk < D8 / 32; ++kk)
+              mma_f8_ss(tmem + s_col8(t), sdesc_add(qdesc, kk * 32), sdesc_add(kdesc, kk * 32), idS,
+                        kk > 0 ? 1u : 0u);
             mma_commit(&s_full[t]);
           }
         }
         if (!ok) break;
-        if (j >= 1 && itV + NSLOT8 < total_items) mma_commit(&kv_empty[slotV]);
-        if (j < nKmax && itK + NSLOT8 < total_items) mma_commit(&kv_empty[slotK]);
       }
     }
   } else {
@@ -348,6 +351,10 @@ __global__ void __launch_bounds__(THREADS8, 1)
         break;
       }
       tc_fence_after_sync();
+      if (t == t_rel && r == 0) {
+        if (2 * j + NSLOT8 < total_items) mbar_arrive(&kv_empty[(2 * j) % NSLOT8]);
+        if (j >= 1 && 2 * j - 1 + NSLOT8 < total_items) mbar_arrive(&kv_empty[(2 * j - 1) % NSLOT8]);
+      }
       uint32_t sr[BN];
 #pragma unroll
       for (int c0 = 0; c0 < BN / 32; ++c0)
@@ -360,15 +367,17 @@ __global__ void __launch_bounds__(THREADS8, 1)
         for (int c = 0; c < BN; ++c)
           if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      float mx[16];
 #pragma unroll
-      for (int c = 0; c < BN; c += 8) {
-        mx0 = fmax3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
-        mx1 = fmax3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-        mx2 = fmax3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-        mx3 = fmax3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
-      }
-      const float m_new = fmaxf(m_ref, fmax3(mx0, mx1, fmaxf(mx2, mx3)) * cj);
+      for (int u = 0; u < 16; ++u)
+        mx[u] = fmax3(__uint_as_float(sr[8 * u]), __uint_as_float(sr[8 * u + 1]),
+                      fmax3(__uint_as_float(sr[8 * u + 2]), __uint_as_float(sr[8 * u + 3]),
+                            fmax3(__uint_as_float(sr[8 * u + 4]), __uint_as_float(sr[8 * u + 5]),
+                                  fmaxf(__uint_as_float(sr[8 * u + 6]), __uint_as_float(sr[8 * u + 7])))));
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], mx[u + 8]);
+      const float m_new = fmaxf(m_ref, fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                             fmaxf(mx[6], mx[7])) * cj);
       const bool need = (m_new - m_ref) > 8.f;
       float alpha = 1.f;
       if (need) {
