@@ -95,7 +95,6 @@ struct Bars {
   uint64_t ds_ready;
   uint64_t dq_full;
   uint64_t dq_free;
-  uint64_t ds_free;
   uint64_t dkv_full;
   uint64_t drain;
   uint32_t tmem_base;
@@ -231,7 +230,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(&bars.ds_ready, 256);
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_free, 256);
-    mbar_init(&bars.ds_free, 1);
     mbar_init(&bars.dkv_full, 1);
     mbar_init(&bars.drain, 1);
     bars.abort_flag = 0;
@@ -387,7 +385,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             mma_f16_ss(tmem + C::DQ_COL, dds, dk, idQ, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars.dq_full);
-        if (n + 1 < nsteps) mma_commit(&bars.ds_free);
       }
       if (ok) mma_commit(&bars.dkv_full);
     }
@@ -442,8 +439,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(&bars.p_ready);
       // phase B: dS^T = P^T (dP^T - D), from the 16-bit P^T kept in registers
+      // dP^T(n) is issued after dQ(n-1), so its completion also means dQ(n-1)
+      // has finished reading the dS^T buffer that this phase overwrites
       if (!(ok = mbar_wait(&bars.dp_full, n & 1, ab, kDevTimeoutSoftmax))) break;
-      if (n > 0 && !(ok = mbar_wait(&bars.ds_free, (n - 1) & 1, ab, kDevTimeoutSoftmax))) break;
       tc_fence_after_sync();
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
