@@ -211,8 +211,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int j = blockIdx.x;
-  const int bh = blockIdx.z * kp.H + blockIdx.y;
+  // Causal: a 1-D grid ordered by work, key tile 0 (which meets every query
+  // tile) of every head first.  Non-causal: (tile, head, batch).
+  const int ntiles = (kp.N + C::BN - 1) / C::BN;
+  const int j = CAUSAL ? static_cast<int>(blockIdx.x / (gridDim.x / ntiles)) : static_cast<int>(blockIdx.x);
+  const int bh = CAUSAL ? static_cast<int>(blockIdx.x % (gridDim.x / ntiles))
+                        : static_cast<int>(blockIdx.z * kp.H + blockIdx.y);
   const int N = kp.N;
   const int nQ = (N + C::BM - 1) / C::BM;
   const int i0 = CAUSAL ? j : 0;
@@ -617,7 +621,8 @@ attn_status_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
     if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
     BwdKParams kp{p.dk, p.dv, p.dq_acc, p.lse2, p.delta, status, p.N, Npad, p.H,
                   p.scale, p.scale * kLog2e};
-    dim3 grid((p.N + 127) / 128, p.H, p.B);
+    const unsigned ntiles = static_cast<unsigned>((p.N + 127) / 128);
+    const dim3 grid = CAUSAL ? dim3(ntiles * p.H * p.B, 1, 1) : dim3(ntiles, p.H, p.B);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e, "backward main launch");

@@ -197,8 +197,15 @@ __global__ void __launch_bounds__(THREADS8, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int g = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int bh = blockIdx.z * kp.H + blockIdx.y;
+  // Causal: a 1-D grid ordered by work, heaviest query-tile groups (largest
+  // g, which visit the most key tiles) of every head first, so the last wave
+  // holds the short ones.  Non-causal: (group, head, batch) keeps a head's
+  // CTAs together for K/V reuse in L2.
+  const int npairs = (kp.N + BM * NQ8 - 1) / (BM * NQ8);
+  const int g = CAUSAL ? npairs - 1 - static_cast<int>(blockIdx.x / (gridDim.x / npairs))
+                       : static_cast<int>(blockIdx.x);
+  const int bh = CAUSAL ? static_cast<int>(blockIdx.x % (gridDim.x / npairs))
+                        : static_cast<int>(blockIdx.z * kp.H + blockIdx.y);
   const int N = kp.N;
   const int nKtot = (N + BN - 1) / BN;
   int nK[NQ8];
@@ -514,7 +521,8 @@ attn_status_t launch_fwd_fp8_t(const Fp8FwdParams& p, cudaStream_t stream) {
   if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
   Fp8KParams kp{p.q_descale, p.k_descale, p.v_descale, p.o, p.lse, status, p.N, p.H,
                 (p.N + 127) / 128, p.scale * 1.4426950408889634f};
-  dim3 grid((p.N + BM * NQ8 - 1) / (BM * NQ8), p.H, p.B);
+  const unsigned npairs = static_cast<unsigned>((p.N + BM * NQ8 - 1) / (BM * NQ8));
+  const dim3 grid = CAUSAL ? dim3(npairs * p.H * p.B, 1, 1) : dim3(npairs, p.H, p.B);
   kern<<<grid, THREADS8, SMEM8, stream>>>(tq, tk, tv, kp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "FP8 forward launch");
