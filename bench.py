@@ -106,6 +106,20 @@ class ClockSampler:
                 "power_w_max": max(float(r[3]) for r in rows if r[3].strip() not in ("", "[N/A]"))}
 
 
+def max_over_ranks(value, device):
+    """Largest value over all ranks (the slowest rank's time defines the job)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(step_flop, ms_per_step, world):
+    """Whole-job throughput: every rank runs one replica of the step (weak
+    scaling), so the job does world * step_flop in the slowest rank's time."""
+    return world * step_flop / (ms_per_step * 1e-3) / 1e12
+
+
 def make_inputs(torch, dev, seed=3):
     g = torch.Generator(device=dev).manual_seed(seed)
     shape = (B, H, N, D)
@@ -204,13 +218,11 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
     total_ms = step_start.elapsed_time(step_end)
     if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
     assert attn.attn_get_device_status() == 0, attn.attn_last_error()
     ms_per_step = total_ms / args.steps
     step_flop = sum(f for _, _, f, _ in step_parts)
-    value = world * step_flop / (ms_per_step * 1e-3) / 1e12
+    value = aggregate_tflops(step_flop, ms_per_step, world)
 
     pk = peaks()
     bf16_peak = pk["bf16_tflops_sustained"]
@@ -245,6 +257,7 @@ def run_ours(args, rank, world):
 
     e2e = run_e2e(args, torch, attn, dev, stream, step_parts, causal, scale, q32, k32, v32,
                   do32, signs)
+    sweep = run_sweep(torch, attn, dev, stream, causal) if args.sweep else None
     launches = sum(l for _, _, _, l in step_parts) * args.steps
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -261,6 +274,8 @@ def run_ours(args, rank, world):
         "e2e": e2e,
         "gpu_launches": launches,
     }
+    if sweep is not None:
+        line["headdim_sweep"] = sweep
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(args)
         print(json.dumps(line), flush=True)
@@ -318,6 +333,41 @@ def run_e2e(args, torch, attn, dev, stream, step_parts, causal, scale, q32, k32,
     d2h = sum(t.numel() * t.element_size() for t in outs.values())
     return {"value": round(flop / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_sweep(torch, attn, dev, stream, causal, steps=20, warmup=3):
+    """Head-dimension sweep of the long-context workload at 16K tokens and
+    H*d = 2048: BF16 forward at d = 64, 128, 256 and backward at d = 64, 128
+    (TFLOP/s, CUDA events, inputs resident in HBM)."""
+    out = {}
+    for d, h in ((64, 32), (128, 16), (256, 8)):
+        g = torch.Generator(device=dev).manual_seed(7)
+        q, k, v, do = (torch.randn((B, h, N, d), generator=g, device=dev).to(torch.bfloat16)
+                       for _ in range(4))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, h, N), dtype=torch.float32, device=dev)
+        flop = 4.0 * B * h * N * N * d / (2 if causal else 1)
+        fns = [("fwd", lambda: attn.attn_fwd(q, k, v, causal=causal, o=o, lse=lse), flop)]
+        if d <= 128:
+            ws = torch.empty(attn.attn_bwd_workspace_size(B, h, N, d), dtype=torch.uint8, device=dev)
+            dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+            fns.append(("bwd", lambda: attn.attn_bwd(q, k, v, o, do, lse, causal=causal, dq=dq,
+                                                     dk=dk, dv=dv, workspace=ws), 2.5 * flop))
+        for name, fn, fl in fns:
+            for _ in range(warmup):
+                fn()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(steps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / steps
+            out[f"{name}_d{d}_h{h}"] = {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1)}
+        del q, k, v, do, o, lse
+    assert attn.attn_get_device_status() == 0, attn.attn_last_error()
+    return out
 
 
 def cpu_sample_problem(seed=3):
@@ -387,6 +437,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false",
+                    help="skip the head-dimension sweep")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))

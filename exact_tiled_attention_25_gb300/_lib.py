@@ -33,6 +33,7 @@ SIGNATURES = {
     "attn_fwd_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,
                              c_void_p]),
+    "attn_selftest_wait_timeout": (c_int, [ctypes.c_uint, c_void_p]),
     "attn_get_device_status": (c_int, [c_void_p]),
     "attn_status_string": (c_char_p, [c_int]),
     "attn_last_error": (c_char_p, []),

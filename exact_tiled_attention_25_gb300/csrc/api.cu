@@ -5,6 +5,7 @@
 #include <string>
 
 #include "common.h"
+#include "sm103_prims.cuh"
 
 namespace attn {
 
@@ -140,6 +141,20 @@ attn_status_t set_smem(const void* kernel, int bytes) {
   return ATTN_OK;
 }
 
+// One thread waits on a barrier that nothing arrives on, through the same
+// bounded wait every kernel uses; the wait gives up after limit_ns and the
+// kernel records the timeout in the status word and returns.
+__global__ void selftest_wait_kernel(int* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  const Abort ab{&abort_flag, status};
+  mbar_wait_limit(&bar, 0, ab, kDevTimeoutSelftest, limit_ns);
+}
+
 }  // namespace attn
 
 using namespace attn;
@@ -247,6 +262,19 @@ attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* 
   return launch_fwd_fp8(p, stream);
 }
 
+attn_status_t attn_selftest_wait_timeout(unsigned limit_us, cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(ATTN_ERR_INVALID_ARG, "limit_us must be in [1, 1000000]");
+  if ((s = check_device()) != ATTN_OK) return s;
+  int* status = device_status_word();
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(status, static_cast<uint64_t>(limit_us) * 1000ull);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "self-test launch");
+  return ATTN_OK;
+}
+
 attn_status_t attn_get_device_status(cudaStream_t stream) {
   g_last_error.clear();
   attn_status_t s;
@@ -261,10 +289,12 @@ attn_status_t attn_get_device_status(cudaStream_t stream) {
   const int zero = 0;
   e = cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return fail_cuda(e, "clearing the status word");
-  static const char* roles[] = {"?", "load", "mma", "softmax", "epilogue", "reduce"};
+  static const char* roles[] = {"?",        "load",   "mma",
+                                "softmax",  "epilogue", "reduce",
+                                "shared-memory alignment", "self-test"};
   const int role = (value >> 8) & 0xF;
   return fail(ATTN_ERR_TIMEOUT, std::string("kernel wait timed out in role ") +
-                                    (role < 6 ? roles[role] : "?") + " (code " +
+                                    (role < 8 ? roles[role] : "?") + " (code " +
                                     std::to_string(value) + ")");
 }
 

@@ -24,6 +24,7 @@ enum : int {
   kDevTimeoutEpilogue = 0x400,
   kDevTimeoutReduce = 0x500,
   kDevSmemMisaligned = 0x600,  // dynamic shared memory not 1024-byte aligned
+  kDevTimeoutSelftest = 0x700, // the wait of attn_selftest_wait_timeout
 };
 
 // Wall-clock budget for any single barrier wait (nanoseconds).  Every
@@ -102,18 +103,23 @@ __device__ __forceinline__ void raise_abort(const Abort& ab, int code) {
   atomicCAS(ab.status, 0, code);
 }
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Abort& ab,
-                                          int code) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, const Abort& ab,
+                                                int code, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*ab.flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       raise_abort(ab, code);
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Abort& ab,
+                                          int code) {
+  return mbar_wait_limit(bar, parity, ab, code, kWaitLimitNs);
 }
 
 // Wait used only while tearing down after an abort: short limit, no status.

@@ -174,6 +174,19 @@ attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* 
  */
 attn_status_t attn_get_device_status(cudaStream_t stream);
 
+/*
+ * attn_selftest_wait_timeout -- diagnostic for the failure path every kernel
+ * shares.  Launches one thread that waits, through the kernels' bounded
+ * barrier wait, on a barrier nothing ever arrives on; after limit_us
+ * microseconds (1 .. 1000000) the wait gives up and records a timeout in the
+ * status word, and the kernel returns normally.  A following
+ * attn_get_device_status() then returns ATTN_ERR_TIMEOUT (role "self-test")
+ * and clears the word; the CUDA context stays usable.  Section "Where It
+ * Breaks" of "FlashAttention-3: Hopper Asynchrony and FP8 Attention" lists
+ * failure modes but no recovery mechanism; this is the library's own.
+ */
+attn_status_t attn_selftest_wait_timeout(unsigned limit_us, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* attn_status_string(attn_status_t s);
 

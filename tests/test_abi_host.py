@@ -108,3 +108,8 @@ def test_device_check_fails_loudly_without_a_gpu(lib):
     # valid arguments reach the device check, which must fail, not fall back
     code = _fwd(lib)
     assert code in (3, 4)
+
+
+def test_selftest_rejects_bad_limits(lib):
+    assert lib.attn_selftest_wait_timeout(0, None) == 1
+    assert lib.attn_selftest_wait_timeout(2000000, None) == 1
