@@ -42,15 +42,24 @@ struct FwdCfg {
   static constexpr int CH = D / 64;                  // 128-byte column chunks per row
   static constexpr int CHUNK_BYTES = BM * 128;       // one 128-row x 128-byte chunk
   static constexpr int TILE_BYTES = BM * D * 2;      // a Q, K or V tile
-  static constexpr int NSLOT_FIT = (kSmemLimit - 2048 - NQ * TILE_BYTES) / TILE_BYTES;
+  // row-statistics exchange between the two warps of a row (static shared memory)
+  static constexpr int XCH_BYTES = 2 * NQ * 2 * 128 * 4;
+  static constexpr int NSLOT_FIT = (kSmemLimit - 2048 - XCH_BYTES - NQ * TILE_BYTES) / TILE_BYTES;
   static constexpr int NSLOT = NSLOT_FIT > 6 ? 6 : NSLOT_FIT;
   static constexpr int SMEM_BYTES = 1024 + NQ * TILE_BYTES + NSLOT * TILE_BYTES;
-  static constexpr int NUM_SOFTMAX_WARPS = 4 * NQ;
+  // Two softmax warpgroups per query tile: each row of S is split between two
+  // warps (key columns [0, 64) and [64, 128)).
+  static constexpr int NUM_SOFTMAX_WARPS = 8 * NQ;
   static constexpr int LOAD_WARP = NUM_SOFTMAX_WARPS;
   static constexpr int MMA_WARP = NUM_SOFTMAX_WARPS + 1;
   static constexpr int THREADS = (NUM_SOFTMAX_WARPS + 2) * 32;
   __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256u + static_cast<uint32_t>(D) * t; }
+  // TMEM column of the packed 16-bit P for keys [16 kk, 16 kk + 16): each half
+  // of the row writes its P inside its own score columns
+  __host__ __device__ static constexpr uint32_t P_COL(int kk) {
+    return 64u * static_cast<uint32_t>(kk / 4) + 8u * static_cast<uint32_t>(kk % 4);
+  }
   static_assert(NSLOT >= 2, "need at least two ring stages");
   static_assert(O_COL(NQ - 1) + D <= 512, "TMEM overflow");
   static_assert(S_COL(NQ - 1) + 128 <= 256, "S region overflow");
@@ -95,6 +104,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ int load_items_sh;
+  __shared__ float xch[2][NQ][2][128];   // [step parity][tile][half][row]
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -128,7 +138,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     for (int t = 0; t < NQ; ++t) {
       mbar_init(&q_full[t], 1);
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 128);
+      mbar_init(&p_full[t], 256);
       mbar_init(&o_full[t], 1);
     }
     for (int s = 0; s < NSLOT; ++s) {
@@ -219,7 +229,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-              mma_f16_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8,
+              mma_f16_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + C::P_COL(kk),
                          sdesc_add(vdesc, kk * 16 * 128), idPV, (j - 1 > 0 || kk > 0) ? 1u : 0u);
             if (j - 1 == nK[t] - 1) mma_commit(&o_full[t]);
           }
@@ -246,19 +256,24 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = warp / 4;
+    // Warp w: query tile t = w / 8, key half h = (w / 4) % 2, rows of its TMEM
+    // lane quarter.  The two warps of a row exchange their partial row max
+    // once per step through shared memory (named barrier per warp pair).
+    const int t = warp / 8;
+    const int h = (warp / 4) & 1;
     const int quarter = warp % 4;
     const int r = quarter * 32 + lane;
+    const uint32_t pair_bar = 1 + t * 4 + quarter;
     const int qt = g * NQ + t;
     // key tiles of this warpgroup's query tile (a scalar: no runtime-indexed array)
     const int my_nK = (qt * BM < N) ? (CAUSAL ? min(nKtot, qt + 1) : nKtot) : 0;
     const int row_g = qt * BM + r;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_addr + C::S_COL(t);
-    const uint32_t tO = tmem + lane_addr + C::O_COL(t);
+    const uint32_t tS = tmem + lane_addr + C::S_COL(t) + 64 * h;     // this half's scores
+    const uint32_t tO = tmem + lane_addr + C::O_COL(t) + (D / 2) * h; // this half's O columns
     const float c2 = kp.scale_log2;
     float m_ref = -INFINITY;
-    float l = 0.f;
+    float l = 0.f;                       // this half's share of the row sum
     bool ok = true;
     for (int j = 0; j < my_nK; ++j) {
       if (!mbar_wait(&s_full[t], j & 1, ab, kDevTimeoutSoftmax)) {
@@ -266,36 +281,37 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         break;
       }
       tc_fence_after_sync();
-      if (t == t_rel && r == 0) {
+      if (t == t_rel && h == 0 && r == 0) {
         // release only slots the producer refills
         if (2 * j + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j) % NSLOT]);
         if (j >= 1 && 2 * j - 1 + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j - 1) % NSLOT]);
       }
-      uint32_t sr[BN];
-#pragma unroll
-      for (int c0 = 0; c0 < BN / 32; ++c0)
-        tmem_ld32(tS + c0 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0 * 32]));
+      uint32_t sr[64];
+      tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_ld_wait();
-      const int kbase = j * BN;
-      if ((CAUSAL && j == qt) || kbase + BN > N) {
+      const int kbase = j * BN + 64 * h;
+      if ((CAUSAL && j == qt) || kbase + 64 > N) {
         const int lim = (CAUSAL ? min(N, row_g + 1) : N) - kbase;
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      // row max as a tree of 3-input maxima (short dependency chains)
-      float mx[16];
+      // this half's max as a tree of 3-input maxima, then the row max
+      float mx[8];
 #pragma unroll
-      for (int u = 0; u < 16; ++u)
+      for (int u = 0; u < 8; ++u)
         mx[u] = fmax3(__uint_as_float(sr[8 * u]), __uint_as_float(sr[8 * u + 1]),
                       fmax3(__uint_as_float(sr[8 * u + 2]), __uint_as_float(sr[8 * u + 3]),
                             fmax3(__uint_as_float(sr[8 * u + 4]), __uint_as_float(sr[8 * u + 5]),
                                   fmaxf(__uint_as_float(sr[8 * u + 6]), __uint_as_float(sr[8 * u + 7])))));
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], mx[u + 8]);
-      const float m_new = fmaxf(m_ref, fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                             fmaxf(mx[6], mx[7])));
-      // Move the exponent reference only when the max grew by more than 2^8.
+      const float m_half = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7]));
+      xch[j & 1][t][h][r] = m_half;
+      named_bar_sync(pair_bar, 64);
+      const float m_new = fmaxf(m_ref, fmaxf(m_half, xch[j & 1][t][h ^ 1][r]));
+      // Move the exponent reference only when the max grew by more than 2^8
+      // (both halves of a row take the same decision).
       const bool need = (m_new - m_ref) * c2 > 8.f;
       float alpha = 1.f;
       if (need) {
@@ -308,7 +324,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const uint64_t nn = pack2(neg, neg);
       uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
-      for (int c0 = 0; c0 < BN / 32; ++c0) {
+      for (int c0 = 0; c0 < 2; ++c0) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -320,16 +336,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           else acc0 = fadd2(acc0, pack2(p0, p1));
           pk[i] = FP16 ? cvt_pack_f16(p0, p1) : cvt_pack_bf16(p0, p1);
         }
+        // packed P of keys [64 h + 32 c0, +32) -> columns [64 h + 16 c0, +16)
         tmem_st16(tS + c0 * 16, pk);
       }
       const uint64_t acc = fadd2(acc0, acc1);
       l += lo2(acc) + hi2(acc);
-      // Rescale this row of O after the scores are consumed (fewer live
-      // registers); the P V product of this step is issued only after the
-      // arrive below, and the previous one finished before S_t(j) did.
+      // Rescale this half's columns of O (the P V product of this step is
+      // issued only after the arrive below; the previous one finished before
+      // S_t(j) did).
       if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < D / 32; ++c0) {
+        for (int c0 = 0; c0 < D / 64; ++c0) {
           uint32_t o[32];
           tmem_ld32(tO + c0 * 32, o);
           tmem_ld_wait();
@@ -345,10 +362,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // ------------------------------------------------------------ epilogue
     if (ok && my_nK > 0 && mbar_wait(&o_full[t], 0, ab, kDevTimeoutEpilogue)) {
       tc_fence_after_sync();
-      const float inv_l = 1.f / l;
-      uint16_t* orow = static_cast<uint16_t*>(kp.o) + (static_cast<size_t>(bh) * N + row_g) * D;
+      // row sum = both halves' shares (buffer of parity my_nK & 1 is free: its
+      // last readers passed this pair's barrier of step my_nK - 1)
+      xch[my_nK & 1][t][h][r] = l;
+      named_bar_sync(pair_bar, 64);
+      const float l_row = l + xch[my_nK & 1][t][h ^ 1][r];
+      const float inv_l = 1.f / l_row;
+      uint16_t* orow = static_cast<uint16_t*>(kp.o) + (static_cast<size_t>(bh) * N + row_g) * D +
+                       (D / 2) * h;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D / 32; ++c0) {
+      for (int c0 = 0; c0 < D / 64; ++c0) {
         uint32_t o[32];
         tmem_ld32(tO + c0 * 32, o);
         tmem_ld_wait();
@@ -366,9 +389,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
-      if (row_g < N)
+      if (h == 0 && row_g < N)
         kp.lse[static_cast<size_t>(bh) * N + row_g] =
-            (m_ref * c2 + lg2_approx(l)) * 0.69314718055994530942f;
+            (m_ref * c2 + lg2_approx(l_row)) * 0.69314718055994530942f;
     }
   }
 
