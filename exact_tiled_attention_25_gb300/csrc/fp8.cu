@@ -12,8 +12,8 @@
 // gives descale = amax / 448 and codes = e4m3_rn_satfinite(x / descale).
 // Per-tensor mode (the comparator) runs amax, reduce and quantise kernels.
 //
-// Forward (d = 128): the BF16 forward's structure with tcgen05.mma
-// kind::f8f6f4 (32-element K steps).  Scores use c_j = scale * log2(e) * dq_i *
+// Forward (d = 128): the BF16 forward's structure (two softmax warps per row)
+// with tcgen05.mma kind::f8f6f4 (32-element K steps).  Scores use c_j = scale * log2(e) * dq_i *
 // dk_j, folded into the single FMA before exp2.  The per-block V descales are
 // folded into the exponent as log2(dv_j / dv_max) (dv_max = largest V descale
 // of the head), so P dv_j / dv_max is what is rounded to e4m3 for the P V
@@ -148,11 +148,18 @@ constexpr int NQ8 = 2;
 constexpr int TILE8 = BM * D8;            // 16 KB: one 128-byte row per token
 constexpr int NSLOT8 = 8;
 constexpr int SMEM8 = 1024 + NQ8 * TILE8 + NSLOT8 * TILE8;
-constexpr int THREADS8 = (4 * NQ8 + 2) * 32;
-constexpr int LOAD_WARP8 = 4 * NQ8;
-constexpr int MMA_WARP8 = 4 * NQ8 + 1;
+// Two softmax warpgroups per query tile: each row of S is split between two
+// warps (key columns [0, 64) and [64, 128)).
+constexpr int THREADS8 = (8 * NQ8 + 2) * 32;
+constexpr int LOAD_WARP8 = 8 * NQ8;
+constexpr int MMA_WARP8 = 8 * NQ8 + 1;
 __host__ __device__ constexpr uint32_t s_col8(int t) { return 128u * t; }
 __host__ __device__ constexpr uint32_t o_col8(int t) { return 256u + 128u * t; }
+// TMEM column of the packed e4m3 P for keys [32 kk, 32 kk + 32): each half of
+// the row writes its P inside its own score columns
+__host__ __device__ constexpr uint32_t p_col8(int kk) {
+  return 64u * static_cast<uint32_t>(kk / 2) + 8u * static_cast<uint32_t>(kk % 2);
+}
 static_assert(SMEM8 <= kSmemLimit - 512, "shared memory");
 
 struct Fp8KParams {
@@ -194,6 +201,7 @@ __global__ void __launch_bounds__(THREADS8, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ int load_items_sh;
+  __shared__ float xch[2][NQ8][2][128];   // [step parity][tile][half][row]
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(THREADS8, 1)
     for (int t = 0; t < NQ8; ++t) {
       mbar_init(&q_full[t], 1);
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 128);
+      mbar_init(&p_full[t], 256);
       mbar_init(&o_full[t], 1);
     }
     for (int s = 0; s < NSLOT8; ++s) {
@@ -307,7 +315,7 @@ __global__ void __launch_bounds__(THREADS8, 1)
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < BN / 32; ++kk)
-              mma_f8_ts(tmem + o_col8(t), tmem + s_col8(t) + kk * 8, sdesc_add(vdesc, kk * 32 * 128),
+              mma_f8_ts(tmem + o_col8(t), tmem + s_col8(t) + p_col8(kk), sdesc_add(vdesc, kk * 32 * 128),
                         idPV, (j - 1 > 0 || kk > 0) ? 1u : 0u);
             if (j - 1 == nK[t] - 1) mma_commit(&o_full[t]);
           }
@@ -332,22 +340,27 @@ __global__ void __launch_bounds__(THREADS8, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = warp / 4;
+    // Warp w: query tile t = w / 8, key half h = (w / 4) % 2, rows of its TMEM
+    // lane quarter.  The two warps of a row exchange their partial row max
+    // once per step through shared memory (named barrier per warp pair).
+    const int t = warp / 8;
+    const int h = (warp / 4) & 1;
     const int quarter = warp % 4;
     const int r = quarter * 32 + lane;
+    const uint32_t pair_bar = 1 + t * 4 + quarter;
     const int qt = g * NQ8 + t;
     const int my_nK = (qt * BM < N) ? (CAUSAL ? min(nKtot, qt + 1) : nKtot) : 0;
     const int row_g = qt * BM + r;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_addr + s_col8(t);
-    const uint32_t tO = tmem + lane_addr + o_col8(t);
+    const uint32_t tS = tmem + lane_addr + s_col8(t) + 64 * h;       // this half's scores
+    const uint32_t tO = tmem + lane_addr + o_col8(t) + (D8 / 2) * h;  // this half's O columns
     const float* kdesc = kp.k_descale + static_cast<size_t>(bh) * kp.nblk;
     const float* vdesc = kp.v_descale + static_cast<size_t>(bh) * kp.nblk;
     float dv_max = 0.f;
     for (int b = 0; b < kp.nblk; ++b) dv_max = fmaxf(dv_max, vdesc[b]);
     const float c_q = (my_nK > 0) ? kp.scale_log2 * kp.q_descale[static_cast<size_t>(bh) * kp.nblk + qt] : 0.f;
     float m_ref = -INFINITY;   // in log2 units of the scaled scores
-    float l = 0.f;
+    float l = 0.f;             // this half's share of the row sum
     bool ok = true;
     for (int j = 0; j < my_nK; ++j) {
       const float cj = c_q * kdesc[j];
@@ -358,33 +371,34 @@ __global__ void __launch_bounds__(THREADS8, 1)
         break;
       }
       tc_fence_after_sync();
-      if (t == t_rel && r == 0) {
+      if (t == t_rel && h == 0 && r == 0) {
         if (2 * j + NSLOT8 < total_items) mbar_arrive(&kv_empty[(2 * j) % NSLOT8]);
         if (j >= 1 && 2 * j - 1 + NSLOT8 < total_items) mbar_arrive(&kv_empty[(2 * j - 1) % NSLOT8]);
       }
-      uint32_t sr[BN];
-#pragma unroll
-      for (int c0 = 0; c0 < BN / 32; ++c0)
-        tmem_ld32(tS + c0 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0 * 32]));
+      uint32_t sr[64];
+      tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_ld_wait();
-      const int kbase = j * BN;
-      if ((CAUSAL && j == qt) || kbase + BN > N) {
+      const int kbase = j * BN + 64 * h;
+      if ((CAUSAL && j == qt) || kbase + 64 > N) {
         const int lim = (CAUSAL ? min(N, row_g + 1) : N) - kbase;
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      float mx[16];
+      float mx[8];
 #pragma unroll
-      for (int u = 0; u < 16; ++u)
+      for (int u = 0; u < 8; ++u)
         mx[u] = fmax3(__uint_as_float(sr[8 * u]), __uint_as_float(sr[8 * u + 1]),
                       fmax3(__uint_as_float(sr[8 * u + 2]), __uint_as_float(sr[8 * u + 3]),
                             fmax3(__uint_as_float(sr[8 * u + 4]), __uint_as_float(sr[8 * u + 5]),
                                   fmaxf(__uint_as_float(sr[8 * u + 6]), __uint_as_float(sr[8 * u + 7])))));
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], mx[u + 8]);
-      const float m_new = fmaxf(m_ref, fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                             fmaxf(mx[6], mx[7])) * cj);
+      const float m_half = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7])) * cj;
+      xch[j & 1][t][h][r] = m_half;
+      named_bar_sync(pair_bar, 64);
+      const float m_new = fmaxf(m_ref, fmaxf(m_half, xch[j & 1][t][h ^ 1][r]));
+      // both halves of a row take the same decision
       const bool need = (m_new - m_ref) > 8.f;
       float alpha = 1.f;
       if (need) {
@@ -398,7 +412,7 @@ __global__ void __launch_bounds__(THREADS8, 1)
       const uint64_t nn = pack2(off, off);
       uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
-      for (int c0 = 0; c0 < BN / 32; ++c0) {
+      for (int c0 = 0; c0 < 2; ++c0) {
         uint32_t pk[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -413,13 +427,16 @@ __global__ void __launch_bounds__(THREADS8, 1)
           acc1 = fadd2(acc1, pack2(p2, p3));
           pk[i] = cvt_pack_e4m3x4(p0, p1, p2, p3);
         }
+        // packed P of keys [64 h + 32 c0, +32) -> columns [64 h + 8 c0, +8)
         tmem_st_x8(tS + c0 * 8, pk);
       }
       const uint64_t acc = fadd2(acc0, acc1);
       l += (lo2(acc) + hi2(acc)) / ratio;                   // sum of the unscaled P
+      // Rescale this half's columns of O (this step's P V product is issued
+      // only after the arrive below; the previous one finished before S_t(j)).
       if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < D8 / 32; ++c0) {
+        for (int c0 = 0; c0 < D8 / 64; ++c0) {
           uint32_t o[32];
           tmem_ld32(tO + c0 * 32, o);
           tmem_ld_wait();
@@ -434,10 +451,16 @@ __global__ void __launch_bounds__(THREADS8, 1)
     }
     if (ok && my_nK > 0 && mbar_wait(&o_full[t], 0, ab, kDevTimeoutEpilogue)) {
       tc_fence_after_sync();
-      const float mul = dv_max / l;
-      uint16_t* orow = static_cast<uint16_t*>(kp.o) + (static_cast<size_t>(bh) * N + row_g) * D8;
+      // row sum = both halves' shares (buffer of parity my_nK & 1 is free: its
+      // last readers passed this pair's barrier of step my_nK - 1)
+      xch[my_nK & 1][t][h][r] = l;
+      named_bar_sync(pair_bar, 64);
+      const float l_row = l + xch[my_nK & 1][t][h ^ 1][r];
+      const float mul = dv_max / l_row;
+      uint16_t* orow = static_cast<uint16_t*>(kp.o) + (static_cast<size_t>(bh) * N + row_g) * D8 +
+                       (D8 / 2) * h;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D8 / 32; ++c0) {
+      for (int c0 = 0; c0 < D8 / 64; ++c0) {
         uint32_t o[32];
         tmem_ld32(tO + c0 * 32, o);
         tmem_ld_wait();
@@ -452,8 +475,8 @@ __global__ void __launch_bounds__(THREADS8, 1)
             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
-      if (row_g < N)
-        kp.lse[static_cast<size_t>(bh) * N + row_g] = (m_ref + lg2_approx8(l)) * 0.69314718055994530942f;
+      if (h == 0 && row_g < N)
+        kp.lse[static_cast<size_t>(bh) * N + row_g] = (m_ref + lg2_approx8(l_row)) * 0.69314718055994530942f;
     }
   }
 

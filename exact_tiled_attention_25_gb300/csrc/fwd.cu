@@ -13,9 +13,11 @@
 //    (TMEM); the probabilities P_t are written back over S_t as 16-bit values
 //    and fed to the P V product straight from TMEM.
 //  * Warp roles: one TMA producer warp, one MMA warp whose elected thread
-//    issues every tcgen05.mma, and one softmax warpgroup per query tile whose
-//    thread i owns row i (TMEM lane i) of S_t and O_t.  The MMA thread
-//    alternates between the tiles, so while one warpgroup runs its
+//    issues every tcgen05.mma, and two softmax warpgroups per query tile: a
+//    warp owns 32 rows (one TMEM lane quarter) and one half of the key
+//    columns, so each row is split across two warps that swap partial maxima
+//    once per step and add their row-sum shares at the end.  The MMA thread
+//    alternates between the tiles, so while one tile's softmax runs its
 //    exponentials the tensor core works on the other tile -- the same overlap
 //    the page's "Ping-pong scheduling" gets from two Hopper warpgroups.
 //  * Rescaling is lazy: the exponent reference m_ref moves only when the row
