@@ -278,7 +278,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     float l = 0.f;                       // this half's share of the row sum
     bool ok = true;
     for (int j = 0; j < my_nK; ++j) {
-      if (!mbar_wait(&s_full[t], j & 1, ab, kDevTimeoutSoftmax)) {
+      // A warp that gives up (decided for the whole warp: the TMEM loads below
+      // are warp-collective) still arrives at this step's pair barrier, where
+      // its partner may be waiting; the partner then fails its next wait too,
+      // since this warp never signals p_full again.
+      if (__any_sync(0xffffffffu, !mbar_wait(&s_full[t], j & 1, ab, kDevTimeoutSoftmax))) {
+        named_bar_arrive(pair_bar, 64);
         ok = false;
         break;
       }
@@ -362,7 +367,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_arrive(&p_full[t]);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && my_nK > 0 && mbar_wait(&o_full[t], 0, ab, kDevTimeoutEpilogue)) {
+    bool out_ok = ok && my_nK > 0;
+    if (out_ok && __any_sync(0xffffffffu, !mbar_wait(&o_full[t], 0, ab, kDevTimeoutEpilogue))) {
+      named_bar_arrive(pair_bar, 64);   // release the partner at the barrier below
+      out_ok = false;
+    }
+    if (out_ok) {
       tc_fence_after_sync();
       // row sum = both halves' shares (buffer of parity my_nK & 1 is free: its
       // last readers passed this pair's barrier of step my_nK - 1)

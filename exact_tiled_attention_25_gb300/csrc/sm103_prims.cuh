@@ -90,6 +90,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same phase.  Measured on GB300: a try_wait that
+// finds its phase already complete still leaves the issuing thread's
+// tcgen05.mma queue idle for ~100 cycles, a test_wait does not, so waits
+// test first and block only when the phase is really pending.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Block-wide abort flag plus the global status word.  A wait gives up when
 // the phase with the given parity has not completed within kWaitLimitNs, or
 // when another role of the CTA already gave up.
@@ -105,7 +121,7 @@ __device__ __forceinline__ void raise_abort(const Abort& ab, int code) {
 
 __device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, const Abort& ab,
                                                 int code, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -133,6 +149,11 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 // Named barrier over a subset of warps (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Arrive without waiting: a warp that leaves a loop of paired barriers early
+// releases a partner that may already be waiting at the current one.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ----------------------------------------------------------------- TMA ------
