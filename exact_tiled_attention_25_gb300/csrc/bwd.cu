@@ -10,9 +10,9 @@
 //   dQ = scale * dS K,  dK = scale * dS^T Q.
 //
 // Three kernels:
-//  1. prep: D = rowsum(dO * O) and L * log2(e) into 128-row padded arrays
-//     (padding: D = 0, L = +inf, so padded query rows get P = 0), and the
-//     float32 dQ accumulator is zeroed.
+//  1. prep: -D = -rowsum(dO * O) and -L * log2(e) into 128-row padded arrays
+//     (padding: 0 and -inf, so padded query rows get P = 0), and the float32
+//     dQ accumulator is zeroed.
 //  2. main: one CTA per (key/value tile j, head, batch).  K_j and V_j stay in
 //     shared memory; dK_j and dV_j accumulate in tensor memory.  Per query tile
 //     i (causal: i >= j) the MMA thread issues, on tcgen05,
@@ -106,8 +106,8 @@ struct BwdKParams {
   void* dk;
   void* dv;
   float* dq_acc;
-  const float* lse2;    // L * log2(e), [B*H][Npad], +inf padding
-  const float* delta;   // rowsum(dO * O), [B*H][Npad], 0 padding
+  const float* lse2;    // -L * log2(e), [B*H][Npad], -inf padding
+  const float* delta;   // -rowsum(dO * O), [B*H][Npad], 0 padding
   int* status;
   int N;
   int Npad;
@@ -161,8 +161,9 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int off = L / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (li == 0) {
-    delta[prow] = (n < N) ? acc : 0.f;
-    lse2[prow] = (n < N) ? lse[bh * N + n] * kLog2e : INFINITY;
+    // stored negated so the main kernel adds them with packed f32x2 FMAs
+    delta[prow] = (n < N) ? -acc : 0.f;
+    lse2[prow] = (n < N) ? -lse[bh * N + n] * kLog2e : -INFINITY;
   }
 }
 
@@ -406,15 +407,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     for (int n = 0; n < nsteps; ++n) {
       const int st = n % C::NST;
       const int i = i0 + n;
-      const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + st * 1024);
-      const float4* dvec4 = lse4 + 32;
+      const float4* nlse4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + st * 1024);  // -L log2 e
+      const float4* ndvec4 = nlse4 + 32;                                                  // -D
       const bool diag = CAUSAL && i == j;
       // phase A: P^T = exp2(S^T c - L log2 e), written back as 16-bit
       if (!(ok = mbar_wait(&bars.s_full, n & 1, ab, kDevTimeoutSoftmax))) break;
       tc_fence_after_sync();
       uint32_t pb[32];                               // this half's P^T, packed pairs
+      const uint64_t cc = pack2(c2, c2);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 4; ++c) {                  // queries [64 h + 16 c, +16)
         const int qb = 64 * h + 16 * c;
         uint32_t sv[16];
         tmem_ld16(tmem + lane_addr + C::S_COL + qb, sv);
@@ -422,12 +424,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
           const int q0 = qb + e;
-          const float4 l4 = lse4[q0 / 4];
-          float p[4];
-          p[0] = ex2_approx(fmaf(__uint_as_float(sv[e + 0]), c2, -l4.x));
-          p[1] = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), c2, -l4.y));
-          p[2] = ex2_approx(fmaf(__uint_as_float(sv[e + 2]), c2, -l4.z));
-          p[3] = ex2_approx(fmaf(__uint_as_float(sv[e + 3]), c2, -l4.w));
+          const float4 l4 = nlse4[q0 / 4];
+          const uint64_t y0 = ffma2(pack2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cc,
+                                    pack2(l4.x, l4.y));
+          const uint64_t y1 = ffma2(pack2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), cc,
+                                    pack2(l4.z, l4.w));
+          float p[4] = {ex2_approx(lo2(y0)), ex2_approx(hi2(y0)), ex2_approx(lo2(y1)), ex2_approx(hi2(y1))};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             if (diag && k > q0 + u) p[u] = 0.f;
@@ -436,6 +438,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           pb[(16 * c + e) / 2] = FP16 ? cvt_pack_f16(p[0], p[1]) : cvt_pack_bf16(p[0], p[1]);
           pb[(16 * c + e) / 2 + 1] = FP16 ? cvt_pack_f16(p[2], p[3]) : cvt_pack_bf16(p[2], p[3]);
         }
+        // packed P^T of queries [qb, qb + 16) -> columns [64 h + 8 c, +8)
         tmem_st_x8(tmem + lane_addr + C::S_COL + 64 * h + 8 * c,
                    *reinterpret_cast<const uint32_t(*)[8]>(&pb[8 * c]));
       }
@@ -448,7 +451,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (!(ok = mbar_wait(&bars.dp_full, n & 1, ab, kDevTimeoutSoftmax))) break;
       tc_fence_after_sync();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 4; ++c) {                  // queries [64 h + 16 c, +16)
         const int qb = 64 * h + 16 * c;
         uint32_t dpv[16];
         tmem_ld16(tmem + lane_addr + C::DP_COL + qb, dpv);
@@ -457,25 +460,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
           const int q0 = qb + e;
-          const float4 d4 = dvec4[q0 / 4];
+          const float4 d4 = ndvec4[q0 / 4];
           // unpack here, not earlier: keeps packed registers live instead of floats
           const uint32_t pw0 = opaque32(pb[(16 * c + e) / 2]);
           const uint32_t pw1 = opaque32(pb[(16 * c + e) / 2 + 1]);
-          float2 pa, pc;
+          uint64_t pa, pc;
           if (FP16) {
-            pa = __half22float2(*reinterpret_cast<const __half2*>(&pw0));
-            pc = __half22float2(*reinterpret_cast<const __half2*>(&pw1));
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pw0));
+            const float2 fc = __half22float2(*reinterpret_cast<const __half2*>(&pw1));
+            pa = pack2(fa.x, fa.y);
+            pc = pack2(fc.x, fc.y);
           } else {
             // a bf16 value is the upper half of the float32 with the same bits
-            pa = make_float2(__uint_as_float(pw0 << 16), __uint_as_float(pw0 & 0xffff0000u));
-            pc = make_float2(__uint_as_float(pw1 << 16), __uint_as_float(pw1 & 0xffff0000u));
+            pa = pack2(__uint_as_float(pw0 << 16), __uint_as_float(pw0 & 0xffff0000u));
+            pc = pack2(__uint_as_float(pw1 << 16), __uint_as_float(pw1 & 0xffff0000u));
           }
-          const float ds0 = pa.x * (__uint_as_float(dpv[e + 0]) - d4.x);
-          const float ds1 = pa.y * (__uint_as_float(dpv[e + 1]) - d4.y);
-          const float ds2 = pc.x * (__uint_as_float(dpv[e + 2]) - d4.z);
-          const float ds3 = pc.y * (__uint_as_float(dpv[e + 3]) - d4.w);
-          dd[e / 2] = FP16 ? cvt_pack_f16(ds0, ds1) : cvt_pack_bf16(ds0, ds1);
-          dd[e / 2 + 1] = FP16 ? cvt_pack_f16(ds2, ds3) : cvt_pack_bf16(ds2, ds3);
+          const uint64_t dsa = fmul2(pa, fadd2(pack2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
+                                               pack2(d4.x, d4.y)));
+          const uint64_t dsc = fmul2(pc, fadd2(pack2(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
+                                               pack2(d4.z, d4.w)));
+          dd[e / 2] = FP16 ? cvt_pack_f16(lo2(dsa), hi2(dsa)) : cvt_pack_bf16(lo2(dsa), hi2(dsa));
+          dd[e / 2 + 1] = FP16 ? cvt_pack_f16(lo2(dsc), hi2(dsc)) : cvt_pack_bf16(lo2(dsc), hi2(dsc));
         }
         tmem_st_x8(tmem + lane_addr + C::DP_COL + 64 * h + 8 * c, dd);
         // dS^T row k, queries [qb, qb + 16) = 16-byte pieces 2c and 2c + 1 of

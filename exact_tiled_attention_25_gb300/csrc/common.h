@@ -51,8 +51,8 @@ struct BwdParams {
   void* dk;
   void* dv;
   float* dq_acc;   // [B, H, N, d] float32 scratch
-  float* lse2;     // [B, H, Npad] float32 scratch: LSE * log2(e), +inf padding
-  float* delta;    // [B, H, Npad] float32 scratch: rowsum(dO * O), 0 padding
+  float* lse2;     // [B, H, Npad] float32 scratch: -LSE * log2(e), -inf padding
+  float* delta;    // [B, H, Npad] float32 scratch: -rowsum(dO * O), 0 padding
   int B, H, N, d;
   int causal;
   float scale;

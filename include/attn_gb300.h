@@ -81,9 +81,9 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 
 /*
  * attn_bwd_workspace_size -- bytes of device scratch attn_bwd needs:
- * a float32 dQ accumulator [B, H, N, d] and two float32 row vectors (L * log2(e)
- * and D = rowsum(dO * O)) padded to a multiple of 128 rows per head, each part
- * 256-byte aligned.  Returns 0 for invalid sizes.
+ * a float32 dQ accumulator [B, H, N, d] and two float32 row vectors (-L * log2(e)
+ * and -D, D = rowsum(dO * O)) padded to a multiple of 128 rows per head, each
+ * part 256-byte aligned.  Returns 0 for invalid sizes.
  */
 size_t attn_bwd_workspace_size(int B, int H, int N, int d);
 
