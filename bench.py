@@ -39,9 +39,9 @@ WORKLOAD = "attention step (bf16 fwd + bf16 bwd + fp8 pre-pass + fp8 fwd), B=2 H
 # ncu captures summarised in profiles/*_b2h16n8192d128.md (non-causal).  An
 # entry is removed whenever its kernel changes after the capture.
 NCU_TRAFFIC = {
-    "fwd_bf16": 247_967_488,      # fwd_kernel: 201.6 MB read + 46.4 MB write
-    "bwd_bf16": 626_646_528,      # bwd_main_kernel: 404.8 MB read + 221.8 MB write
-    "fwd_fp8": 134_397_952,       # fwd_fp8_kernel: 100.7 MB read + 33.7 MB write
+    "fwd_bf16": 247_067_648,      # fwd_kernel: 201.7 MB read + 45.4 MB write
+    "bwd_bf16": 627_049_728,      # bwd_main_kernel: 405.1 MB read + 221.9 MB write
+    "fwd_fp8": 133_839_872,       # fwd_fp8_kernel: 100.7 MB read + 33.1 MB write
     "fp8_prepass": 484_918_528,   # fp8_quant_kernel: 402.7 MB read + 82.2 MB write
 }
 KERNEL_OF = {"fwd_bf16": "fwd_kernel", "bwd_bf16": "bwd_main_kernel (timed as the whole attn_bwd call)",
