@@ -369,7 +369,47 @@ def run_sweep(torch, attn, dev, stream, causal, steps=20, warmup=3):
             ms = a.elapsed_time(b) / steps
             out[f"{name}_d{d}_h{h}"] = {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1)}
         del q, k, v, do, o, lse
+    out.update(run_varlen_gqa(torch, attn, dev, stream, causal, steps, warmup))
     assert attn.attn_get_device_status() == 0, attn.attn_last_error()
+    return out
+
+
+def run_varlen_gqa(torch, attn, dev, stream, causal, steps=20, warmup=3):
+    """A packed batch of 8 sequences of mixed length (seeded, 256..4096 tokens,
+    ~18K in all) with grouped-query heads: H = 16 query heads sharing H_kv = 4
+    key/value heads, d = 128.  FLOP = sum over sequences of 4*len^2*d*H (halved
+    causal); backward 2.5x."""
+    import workloads
+    cu_np, lens = workloads.varlen_lengths(8, 8, 4096, 256)
+    total, maxlen, h, hkv, d = int(cu_np[-1]), int(lens.max()), 16, 4, 128
+    g = torch.Generator(device=dev).manual_seed(8)
+    q, do = (torch.randn((total, h, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(2))
+    k, v = (torch.randn((total, hkv, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(2))
+    cu = torch.from_numpy(cu_np).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((h, total), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(attn.attn_bwd_varlen_workspace_size(len(lens), maxlen, total, h, d),
+                     dtype=torch.uint8, device=dev)
+    flop = sum(4.0 * float(n) * float(n) * d * h for n in lens) / (2 if causal else 1)
+    fns = [("fwd", lambda: attn.attn_fwd_varlen(q, k, v, cu, maxlen, causal=causal, o=o, lse=lse),
+            flop),
+           ("bwd", lambda: attn.attn_bwd_varlen(q, k, v, o, do, lse, cu, maxlen, causal=causal,
+                                                dq=dq, dk=dk, dv=dv, workspace=ws), 2.5 * flop)]
+    out = {}
+    for name, fn, fl in fns:
+        for _ in range(warmup):
+            fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        out[f"varlen_gqa_{name}_b{len(lens)}_t{total}_h{h}kv{hkv}_d{d}"] = {
+            "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1)}
     return out
 
 

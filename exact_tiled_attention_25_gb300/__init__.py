@@ -7,9 +7,10 @@ streams are PyTorch's job) and passes raw pointers.  Every step of the
 computation runs in the library's CUDA kernels; there is no CPU or PyTorch
 fallback, and a missing library raises.
 
-Tensors are [B, H, N, d], contiguous.  Inputs on the CPU are accepted for the
-forward calls: they are copied to the current CUDA device on the current
-stream, and the outputs are copied back to the CPU.
+Tensors are [B, H, N, d], contiguous; the ``*_varlen`` calls take a packed
+batch [total, H, d] with int32 sequence offsets ``cu_seqlens`` [B + 1].  Inputs
+on the CPU are accepted: they are copied to the current CUDA device on the
+current stream, and the outputs are copied back to the CPU.
 """
 from __future__ import annotations
 
@@ -28,7 +29,9 @@ ATTN_ERR_TIMEOUT = 5
 
 _DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 
-__all__ = ["AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
+__all__ = ["AttnError", "attn_fwd", "attn_fwd_gqa", "attn_fwd_varlen", "attn_bwd",
+           "attn_bwd_gqa", "attn_bwd_varlen", "attn_bwd_varlen_workspace_size",
+           "attn_bwd_workspace_size",
            "attn_fp8_quantize", "attn_fwd_fp8", "attn_get_device_status",
            "attn_status_string", "attn_last_error", "load_library"]
 
@@ -115,6 +118,71 @@ def attn_fwd(q, k, v, causal: bool = False, softmax_scale: float | None = None,
     return o, lse
 
 
+def attn_fwd_gqa(q, k, v, causal: bool = False, softmax_scale: float | None = None,
+                 o=None, lse=None, stream=None):
+    """attn_fwd with H_kv = k.shape[1] key/value heads shared by the H query heads."""
+    lib = _lib.load()
+    (q, k, v), host = _to_device([q, k, v])
+    B, H, N, d = _shape4(q, "q")
+    Hkv = k.shape[1] if k.dim() == 4 else -1
+    if _shape4(k, "k") != (B, Hkv, N, d) or _shape4(v, "v") != (B, Hkv, N, d):
+        raise ValueError("k and v must be [B, H_kv, N, d] with q's B, N, d")
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must all be bfloat16 or all float16")
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    code = lib.attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                            int(bool(causal)), scale, _DTYPES[q.dtype], _stream(stream))
+    _check(code, "attn_fwd_gqa")
+    if host:
+        return o.cpu(), lse.cpu()
+    return o, lse
+
+
+def _shape3(t, name):
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be [total, heads, d]")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return tuple(t.shape)
+
+
+def _cu_seqlens(cu, total):
+    if cu.dtype != torch.int32 or cu.dim() != 1 or cu.numel() < 2 or not cu.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous int32 vector [B + 1]")
+    return cu.numel() - 1
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
+                    softmax_scale: float | None = None, o=None, lse=None, stream=None):
+    """Forward over a packed batch: q [total, H, d], k, v [total, H_kv, d],
+    cu_seqlens int32 [B + 1]; returns O [total, H, d] and LSE float32 [H, total]."""
+    lib = _lib.load()
+    (q, k, v, cu_seqlens), host = _to_device([q, k, v, cu_seqlens])
+    total, H, d = _shape3(q, "q")
+    Hkv = k.shape[1] if k.dim() == 3 else -1
+    if _shape3(k, "k") != (total, Hkv, d) or _shape3(v, "v") != (total, Hkv, d):
+        raise ValueError("k and v must be [total, H_kv, d] with q's total and d")
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must all be bfloat16 or all float16")
+    B = _cu_seqlens(cu_seqlens, total)
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, total), dtype=torch.float32, device=q.device)
+    code = lib.attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
+                               B, int(max_seqlen), total, H, Hkv, d, int(bool(causal)), scale,
+                               _DTYPES[q.dtype], _stream(stream))
+    _check(code, "attn_fwd_varlen")
+    if host:
+        return o.cpu(), lse.cpu()
+    return o, lse
+
+
 def attn_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(_lib.load().attn_bwd_workspace_size(B, H, N, d))
 
@@ -144,6 +212,78 @@ def attn_bwd(q, k, v, o, dout, lse, causal: bool = False, softmax_scale: float |
                         workspace.numel() * workspace.element_size(),
                         B, H, N, d, int(bool(causal)), scale, _DTYPES[q.dtype], _stream(stream))
     _check(code, "attn_bwd")
+    if host:
+        return dq.cpu(), dk.cpu(), dv.cpu()
+    return dq, dk, dv
+
+
+def attn_bwd_gqa(q, k, v, o, dout, lse, causal: bool = False,
+                 softmax_scale: float | None = None, dq=None, dk=None, dv=None,
+                 workspace=None, stream=None):
+    """attn_bwd with k, v (and dk, dv) of H_kv = k.shape[1] heads."""
+    lib = _lib.load()
+    (q, k, v, o, dout, lse), host = _to_device([q, k, v, o, dout, lse])
+    B, H, N, d = _shape4(q, "q")
+    Hkv = k.shape[1] if k.dim() == 4 else -1
+    for t, n, hh in ((k, "k", Hkv), (v, "v", Hkv), (o, "o", H), (dout, "dout", H)):
+        if _shape4(t, n) != (B, hh, N, d) or t.dtype != q.dtype:
+            raise ValueError(f"{n} must be [B, {hh}, N, d] in q's dtype")
+    if q.dtype not in _DTYPES:
+        raise ValueError("tensors must be bfloat16 or float16")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [B, H, N]")
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8,
+                                device=q.device)
+    code = lib.attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(),
+                            B, H, Hkv, N, d, int(bool(causal)), scale, _DTYPES[q.dtype],
+                            _stream(stream))
+    _check(code, "attn_bwd_gqa")
+    if host:
+        return dq.cpu(), dk.cpu(), dv.cpu()
+    return dq, dk, dv
+
+
+def attn_bwd_varlen_workspace_size(B: int, max_seqlen: int, total: int, H: int, d: int) -> int:
+    return int(_lib.load().attn_bwd_varlen_workspace_size(B, max_seqlen, total, H, d))
+
+
+def attn_bwd_varlen(q, k, v, o, dout, lse, cu_seqlens, max_seqlen: int, causal: bool = False,
+                    softmax_scale: float | None = None, dq=None, dk=None, dv=None,
+                    workspace=None, stream=None):
+    """Backward of attn_fwd_varlen: q, o, dout [total, H, d]; k, v [total, H_kv, d];
+    lse float32 [H, total]; returns dQ, dK, dV in the inputs' layouts."""
+    lib = _lib.load()
+    (q, k, v, o, dout, lse, cu_seqlens), host = _to_device([q, k, v, o, dout, lse, cu_seqlens])
+    total, H, d = _shape3(q, "q")
+    Hkv = k.shape[1] if k.dim() == 3 else -1
+    for t, n, hh in ((k, "k", Hkv), (v, "v", Hkv), (o, "o", H), (dout, "dout", H)):
+        if _shape3(t, n) != (total, hh, d) or t.dtype != q.dtype:
+            raise ValueError(f"{n} must be [total, {hh}, d] in q's dtype")
+    if q.dtype not in _DTYPES:
+        raise ValueError("tensors must be bfloat16 or float16")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, total) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [H, total]")
+    B = _cu_seqlens(cu_seqlens, total)
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(attn_bwd_varlen_workspace_size(B, int(max_seqlen), total, H, d),
+                                dtype=torch.uint8, device=q.device)
+    code = lib.attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _ptr(cu_seqlens),
+                               B, int(max_seqlen), total, H, Hkv, d, int(bool(causal)), scale,
+                               _DTYPES[q.dtype], _stream(stream))
+    _check(code, "attn_bwd_varlen")
     if host:
         return dq.cpu(), dk.cpu(), dv.cpu()
     return dq, dk, dv

@@ -20,7 +20,20 @@ c_char_p = ctypes.c_char_p
 SIGNATURES = {
     "attn_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                          c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p]),
+    "attn_fwd_gqa": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                             c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p]),
+    "attn_fwd_varlen": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
+                                c_void_p]),
     "attn_bwd_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
+    "attn_bwd_gqa": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                             c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                             c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p]),
+    "attn_bwd_varlen_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "attn_bwd_varlen": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p,
+                                c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
+                                c_void_p]),
     "attn_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                          c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
                          c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p]),

@@ -54,6 +54,26 @@ attn_status_t check_shape(int B, int H, int N, int d, int causal) {
   return ATTN_OK;
 }
 
+attn_status_t check_heads(int H, int H_kv) {
+  if (H_kv < 1 || H_kv > H || H % H_kv != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "H_kv must divide H (1 <= H_kv <= H)");
+  return ATTN_OK;
+}
+
+// A packed batch: B sequences, the longest max_seqlen tokens, total tokens.
+attn_status_t check_packed(int B, int max_seqlen, int total, int H, int d, int causal) {
+  if (B < 1 || H < 1 || max_seqlen < 1 || total < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H, max_seqlen and total must be >= 1");
+  if (d != 64 && d != 128 && d != 256)
+    return fail(ATTN_ERR_INVALID_ARG, "d must be 64, 128 or 256");
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (static_cast<double>(total) * H * d >= 2147483648.0)
+    return fail(ATTN_ERR_INVALID_ARG, "total*H*d must be < 2^31");
+  if (static_cast<double>(B) * H * (max_seqlen + 127) / 128 * 128 >= 2147483648.0)
+    return fail(ATTN_ERR_INVALID_ARG, "B*H*max_seqlen too large");
+  return ATTN_OK;
+}
+
 attn_status_t check_ptrs(std::initializer_list<const void*> ptrs) {
   for (const void* p : ptrs) {
     if (p == nullptr) return fail(ATTN_ERR_INVALID_ARG, "null tensor pointer");
@@ -135,6 +155,26 @@ attn_status_t make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, u
   return ATTN_OK;
 }
 
+attn_status_t make_tmap_4d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
+                           uint64_t rows, uint64_t heads, uint64_t batches, uint64_t row_bytes,
+                           uint64_t head_bytes, uint64_t batch_bytes, uint32_t box_inner,
+                           uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[4] = {inner, rows, heads, batches};
+  cuuint64_t strides[3] = {row_bytes, head_bytes, batch_bytes};
+  cuuint32_t box[4] = {box_inner, box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUtensorMapDataType dt =
+      elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  CUresult r = enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (4-D) failed with CUresult " + std::to_string(r));
+  return ATTN_OK;
+}
+
 attn_status_t set_smem(const void* kernel, int bytes) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
@@ -180,19 +220,87 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
   return bwd_workspace_layout(B, H, N, d).total;
 }
 
-attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                       int H, int N, int d, int causal, float softmax_scale, attn_dtype_t dtype,
-                       cudaStream_t stream) {
+attn_status_t attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int H_kv, int N, int d, int causal, float softmax_scale,
+                           attn_dtype_t dtype, cudaStream_t stream) {
   g_last_error.clear();
   attn_status_t s;
   if ((s = check_shape(B, H, N, d, causal)) != ATTN_OK) return s;
+  if ((s = check_heads(H, H_kv)) != ATTN_OK) return s;
   if ((s = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return s;
   if ((s = check_scale(softmax_scale)) != ATTN_OK) return s;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16)
     return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_BF16 or ATTN_FP16");
   if ((s = check_device()) != ATTN_OK) return s;
-  FwdParams p{q, k, v, o, lse, B, H, N, d, causal, softmax_scale, dtype == ATTN_FP16 ? 1 : 0};
+  FwdParams p{q, k, v, o, lse, B, H, N, d, H_kv, nullptr, 0, causal, softmax_scale,
+              dtype == ATTN_FP16 ? 1 : 0};
   return launch_fwd(p, stream);
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N, int d, int causal, float softmax_scale, attn_dtype_t dtype,
+                       cudaStream_t stream) {
+  return attn_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, softmax_scale, dtype, stream);
+}
+
+attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int* cu_seqlens, int B, int max_seqlen, int total, int H,
+                              int H_kv, int d, int causal, float softmax_scale,
+                              attn_dtype_t dtype, cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if ((s = check_packed(B, max_seqlen, total, H, d, causal)) != ATTN_OK) return s;
+  if ((s = check_heads(H, H_kv)) != ATTN_OK) return s;
+  if ((s = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return s;
+  if (cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens must be a non-null, 4-byte aligned device array");
+  if ((s = check_scale(softmax_scale)) != ATTN_OK) return s;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_BF16 or ATTN_FP16");
+  if ((s = check_device()) != ATTN_OK) return s;
+  FwdParams p{q, k, v, o, lse, B, H, max_seqlen, d, H_kv, cu_seqlens, total, causal,
+              softmax_scale, dtype == ATTN_FP16 ? 1 : 0};
+  return launch_fwd(p, stream);
+}
+
+// Shared by the backward entry points after their own shape checks.
+static attn_status_t bwd_common(const void* q, const void* k, const void* v, const void* o,
+                                const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                void* workspace, size_t workspace_bytes, size_t workspace_need,
+                                const BwdWorkspace& w, int B, int H, int H_kv, int N, int d,
+                                const int* cu_seqlens, int total, int causal,
+                                float softmax_scale, attn_dtype_t dtype, cudaStream_t stream) {
+  attn_status_t s;
+  if ((s = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace})) != ATTN_OK) return s;
+  if ((s = check_scale(softmax_scale)) != ATTN_OK) return s;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_BF16 or ATTN_FP16");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (workspace_bytes < workspace_need)
+    return fail(ATTN_ERR_INVALID_ARG, "workspace smaller than the workspace-size query returns");
+  if (d == 256) return fail(ATTN_ERR_UNSUPPORTED, "the backward pass supports d = 64 and 128");
+  if ((s = check_device()) != ATTN_OK) return s;
+  char* ws = static_cast<char*>(workspace);
+  BwdParams p{q,  k,  v,  o,  dout, lse, dq, dk, dv, reinterpret_cast<float*>(ws + w.dq_acc),
+              reinterpret_cast<float*>(ws + w.lse2), reinterpret_cast<float*>(ws + w.delta),
+              B,  H,  N,  d,  H_kv, cu_seqlens, total, causal, softmax_scale,
+              dtype == ATTN_FP16 ? 1 : 0};
+  return launch_bwd(p, stream);
+}
+
+attn_status_t attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           void* workspace, size_t workspace_bytes, int B, int H, int H_kv, int N,
+                           int d, int causal, float softmax_scale, attn_dtype_t dtype,
+                           cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if ((s = check_shape(B, H, N, d, causal)) != ATTN_OK) return s;
+  if ((s = check_heads(H, H_kv)) != ATTN_OK) return s;
+  return bwd_common(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
+                    attn_bwd_workspace_size(B, H, N, d), bwd_workspace_layout(B, H, N, d), B, H,
+                    H_kv, N, d, nullptr, 0, causal, softmax_scale, dtype, stream);
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -200,25 +308,31 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                        int causal, float softmax_scale, attn_dtype_t dtype,
                        cudaStream_t stream) {
+  return attn_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, H, N,
+                      d, causal, softmax_scale, dtype, stream);
+}
+
+size_t attn_bwd_varlen_workspace_size(int B, int max_seqlen, int total, int H, int d) {
+  if (B < 1 || max_seqlen < 1 || total < 1 || H < 1 || d < 1) return 0;
+  return bwd_workspace_layout_packed(B, max_seqlen, total, H, d).total;
+}
+
+attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              void* workspace, size_t workspace_bytes, const int* cu_seqlens,
+                              int B, int max_seqlen, int total, int H, int H_kv, int d,
+                              int causal, float softmax_scale, attn_dtype_t dtype,
+                              cudaStream_t stream) {
   g_last_error.clear();
   attn_status_t s;
-  if ((s = check_shape(B, H, N, d, causal)) != ATTN_OK) return s;
-  if ((s = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace})) != ATTN_OK) return s;
-  if ((s = check_scale(softmax_scale)) != ATTN_OK) return s;
-  if (dtype != ATTN_BF16 && dtype != ATTN_FP16)
-    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_BF16 or ATTN_FP16");
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  if (workspace_bytes < attn_bwd_workspace_size(B, H, N, d))
-    return fail(ATTN_ERR_INVALID_ARG, "workspace smaller than attn_bwd_workspace_size()");
-  if (d == 256) return fail(ATTN_ERR_UNSUPPORTED, "the backward pass supports d = 64 and 128");
-  if ((s = check_device()) != ATTN_OK) return s;
-  const BwdWorkspace w = bwd_workspace_layout(B, H, N, d);
-  char* ws = static_cast<char*>(workspace);
-  BwdParams p{q, k, v, o, dout, lse, dq, dk, dv, reinterpret_cast<float*>(ws + w.dq_acc),
-              reinterpret_cast<float*>(ws + w.lse2), reinterpret_cast<float*>(ws + w.delta),
-              B, H, N, d, causal, softmax_scale, dtype == ATTN_FP16 ? 1 : 0};
-  return launch_bwd(p, stream);
+  if ((s = check_packed(B, max_seqlen, total, H, d, causal)) != ATTN_OK) return s;
+  if ((s = check_heads(H, H_kv)) != ATTN_OK) return s;
+  if (cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens must be a non-null, 4-byte aligned device array");
+  return bwd_common(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
+                    attn_bwd_varlen_workspace_size(B, max_seqlen, total, H, d),
+                    bwd_workspace_layout_packed(B, max_seqlen, total, H, d), B, H, H_kv,
+                    max_seqlen, d, cu_seqlens, total, causal, softmax_scale, dtype, stream);
 }
 
 attn_status_t attn_fp8_quantize(const float* q, const float* k, const float* v,
@@ -293,6 +407,10 @@ attn_status_t attn_get_device_status(cudaStream_t stream) {
                                 "softmax",  "epilogue", "reduce",
                                 "shared-memory alignment", "self-test"};
   const int role = (value >> 8) & 0xF;
+  if (value == kDevBadSeqlens)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "cu_seqlens inconsistent (an entry outside [0, total], decreasing, or a sequence "
+                "longer than max_seqlen); those sequences were skipped");
   return fail(ATTN_ERR_TIMEOUT, std::string("kernel wait timed out in role ") +
                                     (role < 8 ? roles[role] : "?") + " (code " +
                                     std::to_string(value) + ")");

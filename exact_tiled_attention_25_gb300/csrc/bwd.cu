@@ -105,25 +105,43 @@ struct Bars {
 struct BwdKParams {
   void* dk;
   void* dv;
-  float* dq_acc;
+  float* dq_acc;        // same layout as dQ
   const float* lse2;    // -L * log2(e), [B*H][Npad], -inf padding
   const float* delta;   // -rowsum(dO * O), [B*H][Npad], 0 padding
   int* status;
-  int N;
+  const int* cu_seqlens;   // packed batch offsets [B + 1], else nullptr
+  int N;                   // sequence length, or the longest sequence of a packed batch
   int Npad;
+  int total;               // tokens of a packed batch
   int H;
+  int H_kv;
+  int group;               // query heads per key/value head
   float scale;
   float scale_log2;
 };
 
+// Sequence b of a packed batch: first token and length, or false when its
+// offsets do not fit (outside [0, total], decreasing, or longer than max_len).
+__device__ __forceinline__ bool packed_seq(const int* cu, int b, int total, int max_len, int& s0,
+                                           int& len) {
+  s0 = cu[b];
+  const int e = cu[b + 1];
+  if (s0 < 0 || e < s0 || e > total || e - s0 > max_len) return false;
+  len = e - s0;
+  return true;
+}
+
 // ------------------------------------------------------------------ prep ----
 // One group of D/8 lanes per row; each lane holds 8 consecutive elements.
-template <int D, bool FP16>
+// Rows of O, dO and dQ are [B, H, N, d] or, for a packed batch (PACKED),
+// [total, H, d] with LSE [H, total].
+template <int D, bool FP16, bool PACKED>
 __global__ void __launch_bounds__(256)
     bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                     const float* __restrict__ lse, float* __restrict__ lse2,
                     float* __restrict__ delta, float* __restrict__ dq_acc, int N, int Npad,
-                    long long total_rows_pad) {
+                    long long total_rows_pad, int H, const int* __restrict__ cu_seqlens,
+                    int total) {
   constexpr int L = D / 8;
   constexpr int ROWS_PER_WARP = 32 / L;
   const int lane = threadIdx.x & 31;
@@ -134,9 +152,20 @@ __global__ void __launch_bounds__(256)
   if (prow >= total_rows_pad) return;
   const long long bh = prow / Npad;
   const int n = static_cast<int>(prow - bh * Npad);
+  int len = N;
+  long long row, lrow;     // row of O / dO / dQ, index into LSE
+  if constexpr (PACKED) {
+    const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+    int s0 = 0;
+    if (!packed_seq(cu_seqlens, b, total, N, s0, len)) len = 0;   // reported by the main kernel
+    row = (static_cast<long long>(s0) + n) * H + h;
+    lrow = static_cast<long long>(h) * total + s0 + n;
+  } else {
+    row = bh * N + n;
+    lrow = row;
+  }
   float acc = 0.f;
-  if (n < N) {
-    const long long row = bh * N + n;
+  if (n < len) {
     const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[li];
     const uint4 b = reinterpret_cast<const uint4*>(dout + row * D)[li];
     const uint32_t av[4] = {a.x, a.y, a.z, a.w};
@@ -162,8 +191,8 @@ __global__ void __launch_bounds__(256)
   for (int off = L / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (li == 0) {
     // stored negated so the main kernel adds them with packed f32x2 FMAs
-    delta[prow] = (n < N) ? -acc : 0.f;
-    lse2[prow] = (n < N) ? -lse[bh * N + n] * kLog2e : -INFINITY;
+    delta[prow] = (n < len) ? -acc : 0.f;
+    lse2[prow] = (n < len) ? -lse[lrow] * kLog2e : -INFINITY;
   }
 }
 
@@ -193,7 +222,7 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------ main ----
-template <int D, bool CAUSAL, bool FP16>
+template <int D, bool CAUSAL, bool FP16, bool PACKED>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -212,16 +241,31 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  // Causal: a 1-D grid ordered by work, key tile 0 (which meets every query
-  // tile) of every head first.  Non-causal: (tile, head, batch).
+  // One CTA per (key tile j, key/value head hk, batch b).  Causal: a 1-D grid
+  // ordered by work, key tile 0 (which meets every query tile) of every head
+  // first.  Non-causal: (tile, head, batch).
   const int ntiles = (kp.N + C::BN - 1) / C::BN;
   const int j = CAUSAL ? static_cast<int>(blockIdx.x / (gridDim.x / ntiles)) : static_cast<int>(blockIdx.x);
-  const int bh = CAUSAL ? static_cast<int>(blockIdx.x % (gridDim.x / ntiles))
-                        : static_cast<int>(blockIdx.z * kp.H + blockIdx.y);
-  const int N = kp.N;
+  const int bhk = CAUSAL ? static_cast<int>(blockIdx.x % (gridDim.x / ntiles))
+                         : static_cast<int>(blockIdx.z * kp.H_kv + blockIdx.y);
+  const int b = bhk / kp.H_kv;
+  const int hk = bhk - b * kp.H_kv;
+  int seq0 = 0, N = kp.N;
+  if constexpr (PACKED) {
+    // this sequence's first token and length; key tiles past its end have no
+    // work (the whole CTA leaves before touching any resource)
+    if (!packed_seq(kp.cu_seqlens, b, kp.total, kp.N, seq0, N)) {
+      if (threadIdx.x == 0 && j == 0) atomicCAS(kp.status, 0, kDevBadSeqlens);
+      return;
+    }
+    if (j * C::BN >= N) return;
+  }
   const int nQ = (N + C::BM - 1) / C::BM;
   const int i0 = CAUSAL ? j : 0;
-  const int nsteps = nQ - i0;
+  // Steps walk query tiles i0 .. nQ-1 of the group's first query head, then of
+  // the next one: dK_j, dV_j accumulate over every query head sharing K_j, V_j.
+  const int nsteps = kp.group * (nQ - i0);
+  const int h0 = hk * kp.group;          // first query head of the group
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.kv_full, 1);
@@ -261,26 +305,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_arrive_expect_tx(&bars.kv_full, 2 * C::TILE);
 #pragma unroll
       for (int c = 0; c < C::CH; ++c) {
-        tma_load_3d(smem + C::OFF_K + c * C::CHUNK, &tmK, &bars.kv_full, c * 64, j * C::BN, bh);
-        tma_load_3d(smem + C::OFF_V + c * C::CHUNK, &tmV, &bars.kv_full, c * 64, j * C::BN, bh);
+        // coordinates {c, token, head, 0} for a packed batch, else {c, row, plane}
+        if constexpr (PACKED) {
+          tma_load_4d(smem + C::OFF_K + c * C::CHUNK, &tmK, &bars.kv_full, c * 64, seq0 + j * C::BN, hk, 0);
+          tma_load_4d(smem + C::OFF_V + c * C::CHUNK, &tmV, &bars.kv_full, c * 64, seq0 + j * C::BN, hk, 0);
+        } else {
+          tma_load_3d(smem + C::OFF_K + c * C::CHUNK, &tmK, &bars.kv_full, c * 64, j * C::BN, bhk);
+          tma_load_3d(smem + C::OFF_V + c * C::CHUNK, &tmV, &bars.kv_full, c * 64, j * C::BN, bhk);
+        }
       }
       int n = 0;
-      for (; n < nsteps; ++n) {
+      int i = i0, h = h0;                  // query tile and query head of step n
+      for (; n < nsteps; ++n, (++i == nQ) ? (i = i0, ++h) : 0) {
         const int st = n % C::NST;
         const int use = n / C::NST;
         if (use >= 1 && !mbar_wait(&bars.stage_empty[st], (use - 1) & 1, ab, kDevTimeoutLoad))
           break;
-        const int i = i0 + n;
         uint8_t* sq = smem + C::OFF_RING + st * 2 * C::TILE;
         uint8_t* sdo = sq + C::TILE;
         float* sld = reinterpret_cast<float*>(smem + C::OFF_LD + st * 1024);
         mbar_arrive_expect_tx(&bars.stage_full[st], 2 * C::TILE + 1024);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
-          tma_load_3d(sq + c * C::CHUNK, &tmQ, &bars.stage_full[st], c * 64, i * C::BM, bh);
-          tma_load_3d(sdo + c * C::CHUNK, &tmDO, &bars.stage_full[st], c * 64, i * C::BM, bh);
+          if constexpr (PACKED) {
+            tma_load_4d(sq + c * C::CHUNK, &tmQ, &bars.stage_full[st], c * 64, seq0 + i * C::BM, h, 0);
+            tma_load_4d(sdo + c * C::CHUNK, &tmDO, &bars.stage_full[st], c * 64, seq0 + i * C::BM, h, 0);
+          } else {
+            tma_load_3d(sq + c * C::CHUNK, &tmQ, &bars.stage_full[st], c * 64, i * C::BM, b * kp.H + h);
+            tma_load_3d(sdo + c * C::CHUNK, &tmDO, &bars.stage_full[st], c * 64, i * C::BM, b * kp.H + h);
+          }
         }
-        const size_t roff = static_cast<size_t>(bh) * kp.Npad + static_cast<size_t>(i) * C::BM;
+        const size_t roff = (static_cast<size_t>(b) * kp.H + h) * kp.Npad + static_cast<size_t>(i) * C::BM;
         bulk_load(sld, kp.lse2 + roff, 512, &bars.stage_full[st]);
         bulk_load(sld + 128, kp.delta + roff, 512, &bars.stage_full[st]);
       }
@@ -404,9 +459,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const float c2 = kp.scale_log2;
     const uint32_t sDSrow = smem_u32(smem + C::OFF_DS) + h * C::CHUNK + k * 128;
     bool ok = true;
-    for (int n = 0; n < nsteps; ++n) {
+    int i = i0;                                      // query tile of step n
+    for (int n = 0; n < nsteps; ++n, i = (i + 1 == nQ) ? i0 : i + 1) {
       const int st = n % C::NST;
-      const int i = i0 + n;
       const float4* nlse4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + st * 1024);  // -L log2 e
       const float4* ndvec4 = nlse4 + 32;                                                  // -D
       const bool diag = CAUSAL && i == j;
@@ -503,8 +558,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_after_sync();
       const uint32_t col = h ? C::DK_COL : C::DV_COL;
       const float mul = h ? kp.scale : 1.f;
-      uint16_t* dst_row = static_cast<uint16_t*>(h ? kp.dk : kp.dv) +
-                          (static_cast<size_t>(bh) * N + key_g) * D;
+      // [B, H_kv, N, d], or [total, H_kv, d] for a packed batch
+      const size_t krow = PACKED ? static_cast<size_t>(seq0 + key_g) * kp.H_kv + hk
+                                 : static_cast<size_t>(bhk) * N + key_g;
+      uint16_t* dst_row = static_cast<uint16_t*>(h ? kp.dk : kp.dv) + krow * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D / 32; ++c0) {
         uint32_t v[32];
@@ -534,7 +591,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const int r = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     constexpr int HC = (C::DQ_T ? C::BM : D) / 2;    // columns per reduce warpgroup
-    for (int n = 0; n < nsteps; ++n) {
+    int i = i0, hq = h0;                             // query tile and head of step n
+    // dQ rows: [B, H, N, d], or [total, H, d] for a packed batch
+    const size_t qstride = PACKED ? static_cast<size_t>(kp.H) * D : D;
+    for (int n = 0; n < nsteps; ++n, (++i == nQ) ? (i = i0, ++hq) : 0) {
       if (!mbar_wait(&bars.dq_full, n & 1, ab, kDevTimeoutReduce)) break;
       tc_fence_after_sync();
       // read this half of the tile, hand the columns back, then reduce
@@ -546,25 +606,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tmem_ld_wait();
       tc_fence_before_sync();
       mbar_arrive(&bars.dq_free);
-      const int q_base = (i0 + n) * C::BM;
+      const int q_base = i * C::BM;
+      float* const qrow0 = kp.dq_acc + (PACKED ? (static_cast<size_t>(seq0) * kp.H + hq) * D
+                                               : (static_cast<size_t>(b) * kp.H + hq) * N * D);
       if (C::DQ_T) {
         // column q = query q_base + g HC + q: the warp's 32 lanes cover 32
         // consecutive floats of one dQ row (one 128-byte line per reduction)
         const int q0 = q_base + g * HC;
-        float* col = kp.dq_acc + (static_cast<size_t>(bh) * N + q0) * D + r;
+        float* col = qrow0 + q0 * qstride + r;
         if (q0 + HC <= N) {
 #pragma unroll
-          for (int q = 0; q < HC; ++q) red_add_f32(col + q * D, __uint_as_float(v[q]));
+          for (int q = 0; q < HC; ++q) red_add_f32(col + q * qstride, __uint_as_float(v[q]));
         } else {
 #pragma unroll
           for (int q = 0; q < HC; ++q)
-            if (q0 + q < N) red_add_f32(col + q * D, __uint_as_float(v[q]));
+            if (q0 + q < N) red_add_f32(col + q * qstride, __uint_as_float(v[q]));
         }
       } else {
         // lane r = query; columns g HC .. g HC + HC of its dQ row
         const int q_g = q_base + r;
         if (q_g < N) {
-          float* dst = kp.dq_acc + (static_cast<size_t>(bh) * N + q_g) * D + g * HC;
+          float* dst = qrow0 + q_g * qstride + g * HC;
 #pragma unroll
           for (int e = 0; e < HC; e += 4)
             red_add_v4(dst + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
@@ -596,7 +658,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool FP16>
+template <int D, bool CAUSAL, bool FP16, bool PACKED>
 attn_status_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
   const int Npad = (p.N + 127) / 128 * 128;
@@ -605,36 +667,53 @@ attn_status_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   {
     constexpr int rows_per_block = 8 * (32 / (D / 8));
     const long long blocks = (rows_pad + rows_per_block - 1) / rows_per_block;
-    bwd_prep_kernel<D, FP16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+    bwd_prep_kernel<D, FP16, PACKED><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.dout), p.lse, p.lse2,
-        p.delta, p.dq_acc, p.N, Npad, rows_pad);
+        p.delta, p.dq_acc, p.N, Npad, rows_pad, p.H, p.cu_seqlens, p.total);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e, "backward prep launch");
   }
   // 2. main
   {
-    auto kern = bwd_main_kernel<D, CAUSAL, FP16>;
+    auto kern = bwd_main_kernel<D, CAUSAL, FP16, PACKED>;
     attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
     if (s != ATTN_OK) return s;
     CUtensorMap tq, tk, tv, tdo;
-    const uint64_t planes = static_cast<uint64_t>(p.B) * p.H;
-    if ((s = make_tmap_3d(&tq, p.q, 2, D, p.N, planes, 64, 128)) != ATTN_OK) return s;
-    if ((s = make_tmap_3d(&tk, p.k, 2, D, p.N, planes, 64, 128)) != ATTN_OK) return s;
-    if ((s = make_tmap_3d(&tv, p.v, 2, D, p.N, planes, 64, 128)) != ATTN_OK) return s;
-    if ((s = make_tmap_3d(&tdo, p.dout, 2, D, p.N, planes, 64, 128)) != ATTN_OK) return s;
+    if constexpr (PACKED) {
+      // {d, total tokens, heads, 1}: token stride heads * d, head stride d
+      const uint64_t T = static_cast<uint64_t>(p.total);
+      const uint64_t qr = 2ull * p.H * D, kvr = 2ull * p.H_kv * D;
+      if ((s = make_tmap_4d(&tq, p.q, 2, D, T, p.H, 1, qr, 2ull * D, T * qr, 64, 128)) != ATTN_OK) return s;
+      if ((s = make_tmap_4d(&tdo, p.dout, 2, D, T, p.H, 1, qr, 2ull * D, T * qr, 64, 128)) != ATTN_OK)
+        return s;
+      if ((s = make_tmap_4d(&tk, p.k, 2, D, T, p.H_kv, 1, kvr, 2ull * D, T * kvr, 64, 128)) != ATTN_OK)
+        return s;
+      if ((s = make_tmap_4d(&tv, p.v, 2, D, T, p.H_kv, 1, kvr, 2ull * D, T * kvr, 64, 128)) != ATTN_OK)
+        return s;
+    } else {
+      // {d, N, B * heads}
+      const uint64_t pq = static_cast<uint64_t>(p.B) * p.H, pkv = static_cast<uint64_t>(p.B) * p.H_kv;
+      if ((s = make_tmap_3d(&tq, p.q, 2, D, p.N, pq, 64, 128)) != ATTN_OK) return s;
+      if ((s = make_tmap_3d(&tdo, p.dout, 2, D, p.N, pq, 64, 128)) != ATTN_OK) return s;
+      if ((s = make_tmap_3d(&tk, p.k, 2, D, p.N, pkv, 64, 128)) != ATTN_OK) return s;
+      if ((s = make_tmap_3d(&tv, p.v, 2, D, p.N, pkv, 64, 128)) != ATTN_OK) return s;
+    }
     int* status = device_status_word();
     if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
-    BwdKParams kp{p.dk, p.dv, p.dq_acc, p.lse2, p.delta, status, p.N, Npad, p.H,
-                  p.scale, p.scale * kLog2e};
+    BwdKParams kp{p.dk,  p.dv,    p.dq_acc, p.lse2, p.delta, status,        p.cu_seqlens,
+                  p.N,   Npad,    p.total,  p.H,    p.H_kv,  p.H / p.H_kv,  p.scale,
+                  p.scale * kLog2e};
     const unsigned ntiles = static_cast<unsigned>((p.N + 127) / 128);
-    const dim3 grid = CAUSAL ? dim3(ntiles * p.H * p.B, 1, 1) : dim3(ntiles, p.H, p.B);
+    const dim3 grid = CAUSAL ? dim3(ntiles * p.H_kv * p.B, 1, 1) : dim3(ntiles, p.H_kv, p.B);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e, "backward main launch");
   }
   // 3. convert
   {
-    const long long n8 = static_cast<long long>(p.B) * p.H * p.N * D / 8;
+    const long long elems = PACKED ? static_cast<long long>(p.total) * p.H * D
+                                   : static_cast<long long>(p.B) * p.H * p.N * D;
+    const long long n8 = elems / 8;
     const long long want = (n8 + 255) / 256;
     const unsigned blocks = static_cast<unsigned>(want < 152 * 16 ? want : 152 * 16);
     bwd_convert_kernel<FP16><<<blocks, 256, 0, stream>>>(p.dq_acc, static_cast<uint16_t*>(p.dq),
@@ -645,17 +724,25 @@ attn_status_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   return ATTN_OK;
 }
 
+template <int D, bool PACKED>
+attn_status_t launch_bwd_dp(const BwdParams& p, cudaStream_t stream) {
+  if (p.causal)
+    return p.fp16 ? launch_bwd_t<D, true, true, PACKED>(p, stream)
+                  : launch_bwd_t<D, true, false, PACKED>(p, stream);
+  return p.fp16 ? launch_bwd_t<D, false, true, PACKED>(p, stream)
+                : launch_bwd_t<D, false, false, PACKED>(p, stream);
+}
+
 template <int D>
 attn_status_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
-  if (p.causal)
-    return p.fp16 ? launch_bwd_t<D, true, true>(p, stream) : launch_bwd_t<D, true, false>(p, stream);
-  return p.fp16 ? launch_bwd_t<D, false, true>(p, stream) : launch_bwd_t<D, false, false>(p, stream);
+  return p.cu_seqlens ? launch_bwd_dp<D, true>(p, stream) : launch_bwd_dp<D, false>(p, stream);
 }
 
 }  // namespace
 
 attn_status_t launch_bwd(const BwdParams& p, cudaStream_t stream) {
-  if (p.N > 65535 * 128 || p.H > 65535 || p.B > 65535)
+  if (p.N > 65535 * 128 || p.H > 65535 || p.B > 65535 ||
+      static_cast<long long>((p.N + 127) / 128) * p.H_kv * p.B > 2147483647LL)
     return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
   switch (p.d) {
     case 64: return launch_bwd_d<64>(p, stream);

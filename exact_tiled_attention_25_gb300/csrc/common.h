@@ -25,6 +25,14 @@ attn_status_t make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, u
                            uint64_t rows, uint64_t planes, uint32_t box_inner,
                            uint32_t box_rows);
 
+// 4-D map over {d, rows, heads, batches} with byte strides for rows, heads and
+// batches (each a multiple of 16); box {box_inner, box_rows, 1, 1}, 128-byte
+// swizzle.  Covers [B, H, N, d] and packed [total, H, d] alike.
+attn_status_t make_tmap_4d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
+                           uint64_t rows, uint64_t heads, uint64_t batches, uint64_t row_bytes,
+                           uint64_t head_bytes, uint64_t batch_bytes, uint32_t box_inner,
+                           uint32_t box_rows);
+
 // Opt a kernel into more than 48 KB of dynamic shared memory (once per kernel).
 attn_status_t set_smem(const void* kernel, int bytes);
 
@@ -34,7 +42,10 @@ struct FwdParams {
   const void* v;
   void* o;
   float* lse;
-  int B, H, N, d;
+  int B, H, N, d;     // N: sequence length, or the longest one of a packed batch
+  int H_kv;           // key/value heads (H % H_kv == 0)
+  const int* cu_seqlens;   // device [B + 1] for a packed batch, else nullptr
+  int total;          // tokens of a packed batch (cu_seqlens[B])
   int causal;
   float scale;
   int fp16;   // 0 = bf16, 1 = fp16
@@ -50,10 +61,13 @@ struct BwdParams {
   void* dq;
   void* dk;
   void* dv;
-  float* dq_acc;   // [B, H, N, d] float32 scratch
+  float* dq_acc;   // float32 scratch in dQ's layout
   float* lse2;     // [B, H, Npad] float32 scratch: -LSE * log2(e), -inf padding
   float* delta;    // [B, H, Npad] float32 scratch: -rowsum(dO * O), 0 padding
-  int B, H, N, d;
+  int B, H, N, d;  // N: sequence length, or the longest one of a packed batch
+  int H_kv;        // key/value heads (H % H_kv == 0)
+  const int* cu_seqlens;   // device [B + 1] for a packed batch, else nullptr
+  int total;       // tokens of a packed batch
   int causal;
   float scale;
   int fp16;
@@ -94,15 +108,29 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct BwdWorkspace {
   size_t dq_acc, lse2, delta, total;
 };
-inline BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
-  const size_t rows = static_cast<size_t>(B) * H * N;
-  const size_t rows_pad = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128 * 128);
+// dq_rows: rows of d floats in the dQ accumulator; rows_pad: entries of each
+// padded row vector.
+inline BwdWorkspace bwd_workspace_layout_rows(size_t dq_rows, size_t rows_pad, int d) {
+  const size_t rows = dq_rows;
   BwdWorkspace w;
   w.dq_acc = 0;
   w.lse2 = align_up(rows * d * sizeof(float), 256);
   w.delta = w.lse2 + align_up(rows_pad * sizeof(float), 256);
   w.total = w.delta + align_up(rows_pad * sizeof(float), 256);
   return w;
+}
+
+inline BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
+  return bwd_workspace_layout_rows(static_cast<size_t>(B) * H * N,
+                                   static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128 * 128), d);
+}
+
+// A packed batch: dQ accumulator [total, H, d]; row vectors padded per (b, h)
+// to the longest sequence.
+inline BwdWorkspace bwd_workspace_layout_packed(int B, int max_seqlen, int total, int H, int d) {
+  return bwd_workspace_layout_rows(static_cast<size_t>(total) * H,
+                                   static_cast<size_t>(B) * H *
+                                       ((static_cast<size_t>(max_seqlen) + 127) / 128 * 128), d);
 }
 
 }  // namespace attn

@@ -71,8 +71,11 @@ struct FwdKParams {
   void* o;
   float* lse;
   int* status;
-  int N;
+  const int* cu_seqlens;   // packed batch: sequence b is tokens [cu[b], cu[b+1]); else nullptr
+  int N;                   // sequence length, or the longest sequence (sizes the grid)
+  int total;               // tokens of a packed batch
   int H;
+  int group;               // query heads per key/value head
   float scale_log2;   // softmax_scale * log2(e)
 };
 
@@ -82,7 +85,9 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
-template <int D, bool CAUSAL, bool FP16>
+// PACKED: a batch of sequences packed back to back ([total, H, d], LSE
+// [H, total], offsets cu_seqlens); otherwise [B, H, N, d] and LSE [B, H, N].
+template <int D, bool CAUSAL, bool FP16, bool PACKED>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdKParams kp) {
@@ -119,7 +124,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                        : static_cast<int>(blockIdx.x);
   const int bh = CAUSAL ? static_cast<int>(blockIdx.x % (gridDim.x / npairs))
                         : static_cast<int>(blockIdx.z * kp.H + blockIdx.y);
-  const int N = kp.N;
+  // A packed batch: this sequence's first token and length; tiles past its end
+  // have nothing to do (the whole CTA leaves before touching any resource).
+  int seq0 = 0, N = kp.N;
+  if constexpr (PACKED) {
+    const int b = bh / kp.H;
+    seq0 = kp.cu_seqlens[b];
+    const int end = kp.cu_seqlens[b + 1];
+    if (seq0 < 0 || end < seq0 || end > kp.total || end - seq0 > kp.N) {
+      if (threadIdx.x == 0) atomicCAS(kp.status, 0, kDevBadSeqlens);
+      return;
+    }
+    N = end - seq0;
+    if (g * NQ * BM >= N) return;
+  }
   const int nKtot = (N + BN - 1) / BN;
 
   int nK[NQ];
@@ -168,14 +186,24 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
+      // Tensor-map coordinates: {c, row, plane} with plane = b * heads + head
+      // for [B, heads, N, d]; {c, token, head, 0} for a packed batch.
+      const int b = bh / kp.H;
+      const int hq = bh - b * kp.H;            // query head
+      const int hkv = hq / kp.group;           // its key/value head
+      const int kv_plane = b * (kp.H / kp.group) + hkv;
 #pragma unroll
       for (int t = 0; t < NQ; ++t) {
         if (nK[t] == 0) continue;
         mbar_arrive_expect_tx(&q_full[t], C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c)
-          tma_load_3d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, &q_full[t], c * 64,
-                      (g * NQ + t) * BM, bh);
+          if constexpr (PACKED)
+            tma_load_4d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, &q_full[t], c * 64,
+                        seq0 + (g * NQ + t) * BM, hq, 0);
+          else
+            tma_load_3d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, &q_full[t], c * 64,
+                        (g * NQ + t) * BM, bh);
       }
       int it = 0;
       bool ok = true;
@@ -191,8 +219,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           uint8_t* dst = sKV + slot * C::TILE_BYTES;
 #pragma unroll
           for (int c = 0; c < C::CH; ++c)
-            tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tmV : &tmK, &kv_full[slot], c * 64,
-                        j * BN, bh);
+            if constexpr (PACKED)
+              tma_load_4d(dst + c * C::CHUNK_BYTES, kv ? &tmV : &tmK, &kv_full[slot], c * 64,
+                          seq0 + j * BN, hkv, 0);
+            else
+              tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tmV : &tmK, &kv_full[slot], c * 64,
+                          j * BN, kv_plane);
           ++it;
         }
       }
@@ -380,8 +412,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       named_bar_sync(pair_bar, 64);
       const float l_row = l + xch[my_nK & 1][t][h ^ 1][r];
       const float inv_l = 1.f / l_row;
-      uint16_t* orow = static_cast<uint16_t*>(kp.o) + (static_cast<size_t>(bh) * N + row_g) * D +
-                       (D / 2) * h;
+      // O row: [B, H, N, d], or [total, H, d] for a packed batch
+      const size_t orow_off = PACKED ? (static_cast<size_t>(seq0 + row_g) * kp.H + bh % kp.H) * D
+                                     : (static_cast<size_t>(bh) * N + row_g) * D;
+      uint16_t* orow = static_cast<uint16_t*>(kp.o) + orow_off + (D / 2) * h;
 #pragma unroll 1
       for (int c0 = 0; c0 < D / 64; ++c0) {
         uint32_t o[32];
@@ -390,9 +424,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a = __uint_as_float(o[2 * i]) * inv_l;
-          const float b = __uint_as_float(o[2 * i + 1]) * inv_l;
-          pk[i] = FP16 ? cvt_pack_f16(a, b) : cvt_pack_bf16(a, b);
+          const float o0 = __uint_as_float(o[2 * i]) * inv_l;
+          const float o1 = __uint_as_float(o[2 * i + 1]) * inv_l;
+          pk[i] = FP16 ? cvt_pack_f16(o0, o1) : cvt_pack_bf16(o0, o1);
         }
         if (row_g < N) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 32);
@@ -402,7 +436,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
       }
       if (h == 0 && row_g < N)
-        kp.lse[static_cast<size_t>(bh) * N + row_g] =
+        kp.lse[PACKED ? static_cast<size_t>(bh % kp.H) * kp.total + seq0 + row_g
+                      : static_cast<size_t>(bh) * N + row_g] =
             (m_ref * c2 + lg2_approx(l_row)) * 0.69314718055994530942f;
     }
   }
@@ -432,20 +467,38 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool FP16>
+template <int D, bool CAUSAL, bool FP16, bool PACKED>
 attn_status_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fwd_kernel<D, CAUSAL, FP16>;
+  auto kern = fwd_kernel<D, CAUSAL, FP16, PACKED>;
   attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (s != ATTN_OK) return s;
   CUtensorMap tq, tk, tv;
-  const uint64_t planes = static_cast<uint64_t>(p.B) * p.H;
-  if ((s = make_tmap_3d(&tq, p.q, 2, D, p.N, planes, 64, BM)) != ATTN_OK) return s;
-  if ((s = make_tmap_3d(&tk, p.k, 2, D, p.N, planes, 64, BN)) != ATTN_OK) return s;
-  if ((s = make_tmap_3d(&tv, p.v, 2, D, p.N, planes, 64, BN)) != ATTN_OK) return s;
+  if constexpr (PACKED) {
+    // {d, total tokens, heads, 1}: token stride heads * d, head stride d
+    const uint64_t T = static_cast<uint64_t>(p.total);
+    if ((s = make_tmap_4d(&tq, p.q, 2, D, T, p.H, 1, 2ull * p.H * D, 2ull * D, 2ull * T * p.H * D,
+                          64, BM)) != ATTN_OK)
+      return s;
+    if ((s = make_tmap_4d(&tk, p.k, 2, D, T, p.H_kv, 1, 2ull * p.H_kv * D, 2ull * D,
+                          2ull * T * p.H_kv * D, 64, BN)) != ATTN_OK)
+      return s;
+    if ((s = make_tmap_4d(&tv, p.v, 2, D, T, p.H_kv, 1, 2ull * p.H_kv * D, 2ull * D,
+                          2ull * T * p.H_kv * D, 64, BN)) != ATTN_OK)
+      return s;
+  } else {
+    // {d, N, B * heads}
+    if ((s = make_tmap_3d(&tq, p.q, 2, D, p.N, static_cast<uint64_t>(p.B) * p.H, 64, BM)) != ATTN_OK)
+      return s;
+    if ((s = make_tmap_3d(&tk, p.k, 2, D, p.N, static_cast<uint64_t>(p.B) * p.H_kv, 64, BN)) != ATTN_OK)
+      return s;
+    if ((s = make_tmap_3d(&tv, p.v, 2, D, p.N, static_cast<uint64_t>(p.B) * p.H_kv, 64, BN)) != ATTN_OK)
+      return s;
+  }
   int* status = device_status_word();
   if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
-  FwdKParams kp{p.o, p.lse, status, p.N, p.H, p.scale * 1.4426950408889634f};
+  FwdKParams kp{p.o,   p.lse, status, p.cu_seqlens,           p.N,
+                p.total, p.H,  p.H / p.H_kv, p.scale * 1.4426950408889634f};
   const int rows_per_cta = BM * C::NQ;
   const unsigned npairs = static_cast<unsigned>((p.N + rows_per_cta - 1) / rows_per_cta);
   const dim3 grid = CAUSAL ? dim3(npairs * p.H * p.B, 1, 1) : dim3(npairs, p.H, p.B);
@@ -455,17 +508,25 @@ attn_status_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
   return ATTN_OK;
 }
 
+template <int D, bool PACKED>
+attn_status_t launch_fwd_dp(const FwdParams& p, cudaStream_t stream) {
+  if (p.causal)
+    return p.fp16 ? launch_fwd_t<D, true, true, PACKED>(p, stream)
+                  : launch_fwd_t<D, true, false, PACKED>(p, stream);
+  return p.fp16 ? launch_fwd_t<D, false, true, PACKED>(p, stream)
+                : launch_fwd_t<D, false, false, PACKED>(p, stream);
+}
+
 template <int D>
 attn_status_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
-  if (p.causal)
-    return p.fp16 ? launch_fwd_t<D, true, true>(p, stream) : launch_fwd_t<D, true, false>(p, stream);
-  return p.fp16 ? launch_fwd_t<D, false, true>(p, stream) : launch_fwd_t<D, false, false>(p, stream);
+  return p.cu_seqlens ? launch_fwd_dp<D, true>(p, stream) : launch_fwd_dp<D, false>(p, stream);
 }
 
 }  // namespace
 
 attn_status_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
-  if (p.N > 65535 * 256 || p.H > 65535 || p.B > 65535)
+  if (p.N > 65535 * 256 || p.H > 65535 || p.B > 65535 ||
+      static_cast<long long>((p.N + 255) / 128) * p.H * p.B > 2147483647LL)
     return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
   switch (p.d) {
     case 64: return launch_fwd_d<64>(p, stream);

@@ -25,6 +25,8 @@ enum : int {
   kDevTimeoutReduce = 0x500,
   kDevSmemMisaligned = 0x600,  // dynamic shared memory not 1024-byte aligned
   kDevTimeoutSelftest = 0x700, // the wait of attn_selftest_wait_timeout
+  kDevBadSeqlens = 0x800,      // cu_seqlens entry outside [0, total], decreasing, or a
+                               // sequence longer than max_seqlen: that sequence is skipped
 };
 
 // Wall-clock budget for any single barrier wait (nanoseconds).  Every
@@ -168,6 +170,16 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// 4-D tiled load: {inner, row, head, batch} coordinates.
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map,
+                                            uint64_t* bar, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
 

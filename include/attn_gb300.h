@@ -80,6 +80,46 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        attn_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * attn_fwd_gqa -- attn_fwd with grouped-query attention: the H query heads
+ * share H_kv key/value heads (1 <= H_kv <= H, H % H_kv == 0); query head h
+ * reads key/value head h / (H / H_kv).  H_kv = H is attn_fwd, H_kv = 1 is
+ * multi-query attention.
+ *   q, o : [B, H, N, d];   k, v : [B, H_kv, N, d];   lse : [B, H, N] float32.
+ * Other arguments, errors and semantics as attn_fwd.
+ * Source: "FlashAttention 3 Hardware Acceleration: Hopper GPU Strategies for
+ * Long-Context Enterprise Inference Optimization", section "Runtime Kernel
+ * Selection" (grouped query attention patterns).
+ */
+attn_status_t attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int H_kv, int N, int d, int causal, float softmax_scale,
+                           attn_dtype_t dtype, cudaStream_t stream);
+
+/*
+ * attn_fwd_varlen -- forward over a batch of B sequences of different lengths
+ * packed back to back without padding, with grouped-query attention.
+ *   q, o       : [total, H, d] in `dtype` (token-major, d fastest)
+ *   k, v       : [total, H_kv, d]
+ *   lse        : [H, total] float32
+ *   cu_seqlens : DEVICE int32 [B + 1]; sequence b is tokens [cu_seqlens[b],
+ *                cu_seqlens[b+1]); cu_seqlens[0] = 0, non-decreasing,
+ *                cu_seqlens[B] = total.  Empty sequences are allowed.
+ *   max_seqlen : >= the longest sequence (it sizes the grid).
+ * Attention and the causal mask act within each sequence (query i of a sequence
+ * sees that sequence's keys 0..i).  The host checks shapes and pointers; the
+ * device checks each sequence against total and max_seqlen, skips any that
+ * does not fit, and reports it through attn_get_device_status()
+ * (ATTN_ERR_INVALID_ARG).
+ * Source: "FlashAttention 3 Hardware Acceleration: Hopper GPU Strategies for
+ * Long-Context Enterprise Inference Optimization", sections "GPU Compatibility
+ * and Enablement Matrix" (variable-length sequence handling) and "Runtime
+ * Kernel Selection" (grouped query attention).
+ */
+attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int* cu_seqlens, int B, int max_seqlen, int total, int H,
+                              int H_kv, int d, int causal, float softmax_scale,
+                              attn_dtype_t dtype, cudaStream_t stream);
+
+/*
  * attn_bwd_workspace_size -- bytes of device scratch attn_bwd needs:
  * a float32 dQ accumulator [B, H, N, d] and two float32 row vectors (-L * log2(e)
  * and -D, D = rowsum(dO * O)) padded to a multiple of 128 rows per head, each
@@ -107,6 +147,45 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                        int causal, float softmax_scale, attn_dtype_t dtype,
                        cudaStream_t stream);
+
+/*
+ * attn_bwd_gqa -- attn_bwd with grouped-query attention (see attn_fwd_gqa):
+ *   q, o, dout, dq : [B, H, N, d];   k, v, dk, dv : [B, H_kv, N, d];
+ *   lse : [B, H, N].  dK and dV of a shared key/value head are the sums over
+ *   the H / H_kv query heads that read it; one CTA per key tile and key/value
+ *   head accumulates them over the whole group on chip, so they need no
+ *   atomics.  The workspace is attn_bwd_workspace_size(B, H, N, d).
+ * Source: as attn_bwd, and "FlashAttention 3 Hardware Acceleration: Hopper GPU
+ * Strategies for Long-Context Enterprise Inference Optimization", section
+ * "Runtime Kernel Selection" (grouped query attention).
+ */
+attn_status_t attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           void* workspace, size_t workspace_bytes, int B, int H, int H_kv, int N,
+                           int d, int causal, float softmax_scale, attn_dtype_t dtype,
+                           cudaStream_t stream);
+
+/*
+ * attn_bwd_varlen_workspace_size -- bytes of device scratch attn_bwd_varlen
+ * needs: a float32 dQ accumulator [total, H, d] and two float32 row vectors
+ * (-L * log2(e) and -D) of B * H * (max_seqlen rounded up to 128) entries,
+ * each part 256-byte aligned.  Returns 0 for invalid sizes.
+ */
+size_t attn_bwd_varlen_workspace_size(int B, int max_seqlen, int total, int H, int d);
+
+/*
+ * attn_bwd_varlen -- backward of attn_fwd_varlen over the same packed batch:
+ *   q, o, dout, dq : [total, H, d];   k, v, dk, dv : [total, H_kv, d];
+ *   lse : [H, total] from attn_fwd_varlen;   cu_seqlens, max_seqlen, total as
+ *   there (device-checked the same way).  d = 64 or 128.
+ * Source: as attn_bwd and attn_fwd_varlen.
+ */
+attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              void* workspace, size_t workspace_bytes, const int* cu_seqlens,
+                              int B, int max_seqlen, int total, int H, int H_kv, int d,
+                              int causal, float softmax_scale, attn_dtype_t dtype,
+                              cudaStream_t stream);
 
 /*
  * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device memory.

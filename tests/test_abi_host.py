@@ -113,3 +113,52 @@ def test_device_check_fails_loudly_without_a_gpu(lib):
 def test_selftest_rejects_bad_limits(lib):
     assert lib.attn_selftest_wait_timeout(0, None) == 1
     assert lib.attn_selftest_wait_timeout(2000000, None) == 1
+
+
+def test_gqa_and_varlen_entry_points_are_declared():
+    names = declared_functions()
+    for expected in ("attn_fwd_gqa", "attn_fwd_varlen", "attn_bwd_gqa", "attn_bwd_varlen",
+                     "attn_bwd_varlen_workspace_size"):
+        assert expected in names
+
+
+@pytest.mark.parametrize("H,H_kv", [(4, 3), (4, 0), (2, 4)])
+def test_gqa_rejects_heads_that_do_not_group(lib, H, H_kv):
+    assert lib.attn_fwd_gqa(16, 16, 16, 16, 16, 1, H, H_kv, 128, 128, 0, 0.1, 0, None) == 1
+    assert b"H_kv" in lib.attn_last_error()
+    ws = lib.attn_bwd_workspace_size(1, H, 128, 128)
+    assert lib.attn_bwd_gqa(16, 16, 16, 16, 16, 16, 16, 16, 16, 256, ws,
+                            1, H, H_kv, 128, 128, 0, 0.1, 0, None) == 1
+
+
+def _fwd_varlen(lib, cu=16, B=2, max_len=128, total=200, H=2, H_kv=1, d=128, causal=0):
+    return lib.attn_fwd_varlen(16, 16, 16, 16, 16, cu, B, max_len, total, H, H_kv, d, causal, 0.1,
+                               0, None)
+
+
+@pytest.mark.parametrize("kwargs,why", [
+    (dict(cu=0), "cu_seqlens"),
+    (dict(cu=18), "cu_seqlens"),
+    (dict(total=0), "total"),
+    (dict(max_len=0), "max_seqlen"),
+    (dict(B=0), "B"),
+    (dict(d=80), "d"),
+    (dict(H_kv=3), "H_kv"),
+    (dict(total=1 << 30, H=16), "2^31"),
+])
+def test_varlen_rejects_bad_arguments_without_a_gpu(lib, kwargs, why):
+    assert _fwd_varlen(lib, **kwargs) == 1
+    assert why.lower() in lib.attn_last_error().decode().lower()
+
+
+def test_varlen_workspace_size(lib):
+    up = lambda x: -(-x // 256) * 256
+    B, max_len, total, H, d = 3, 300, 700, 4, 64
+    rows_pad = B * H * (-(-max_len // 128) * 128)
+    expect = up(total * H * d * 4) + 2 * up(rows_pad * 4)
+    assert lib.attn_bwd_varlen_workspace_size(B, max_len, total, H, d) == expect
+    assert lib.attn_bwd_varlen_workspace_size(0, max_len, total, H, d) == 0
+    ws = lib.attn_bwd_varlen_workspace_size(2, 128, 200, 2, 64)
+    code = lib.attn_bwd_varlen(16, 16, 16, 16, 16, 16, 16, 16, 16, 256, ws - 1, 16,
+                               2, 128, 200, 2, 1, 64, 0, 0.1, 0, None)
+    assert code == 1 and b"workspace" in lib.attn_last_error()

@@ -102,3 +102,12 @@ def round_to(x: np.ndarray, dtype: str):
 def as_f64(t) -> np.ndarray:
     """Exact float64 copy of a CPU torch tensor (any float dtype)."""
     return t.double().numpy()
+
+
+def varlen_lengths(seed: int, B: int, max_len: int, min_len: int = 0):
+    """B sequence lengths drawn uniformly from [min_len, max_len] (int32 offsets
+    cu_seqlens [B + 1] and the lengths)."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(min_len, max_len + 1, size=B).astype(np.int64)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    return cu, lens
