@@ -287,55 +287,136 @@ def run_ours(args, rank, world):
 def run_e2e(args, torch, attn, dev, stream, step_parts, causal, scale, q32, k32, v32, do32,
             signs):
     """The same step through the public API with inputs in pinned host memory:
-    host-to-device copies of the inputs and device-to-host copies of every
-    output are inside the timed region."""
+    host-to-device copies of every step's inputs and device-to-host copies of
+    every output are inside the timed region.
+
+    Two measurements.  `serial`: one stream, each step uploads, computes and
+    downloads in turn.  `value` (pipelined, as a caller streaming batches would
+    run it): uploads on a copy stream, compute on the launching stream and
+    downloads on a third stream, with two device buffer sets, so step k+1's
+    upload and step k-1's download overlap step k's kernels.  Every step still
+    moves the same bytes; the timed region runs from the first upload to the
+    end of the last download."""
     names = [n for n, *_ in step_parts]
     pin = lambda t: t.cpu().pin_memory()
     h_in = {"q": pin(q32.to(torch.bfloat16)), "k": pin(k32.to(torch.bfloat16)),
             "v": pin(v32.to(torch.bfloat16)), "do": pin(do32.to(torch.bfloat16))}
     if "fp8_prepass" in names:
         h_in.update(q32=pin(q32), k32=pin(k32), v32=pin(v32), signs=pin(signs))
-    d_in = {k_: torch.empty_like(t, device=dev) for k_, t in h_in.items()}
-    outs = {}
+    bf = torch.bfloat16
+    shp = tuple(h_in["q"].shape)
+    B_, H_, N_, _ = shp
 
-    def step():
+    def new_slot():
+        d_in = {k_: torch.empty_like(t, device=dev) for k_, t in h_in.items()}
+        outs = {"o": torch.empty(shp, dtype=bf, device=dev),
+                "lse": torch.empty((B_, H_, N_), dtype=torch.float32, device=dev)}
+        if "bwd_bf16" in names:
+            outs.update(dq=torch.empty(shp, dtype=bf, device=dev),
+                        dk=torch.empty(shp, dtype=bf, device=dev),
+                        dv=torch.empty(shp, dtype=bf, device=dev),
+                        ws=torch.empty(attn.attn_bwd_workspace_size(B_, H_, N_, shp[3]),
+                                       dtype=torch.uint8, device=dev))
+        if "fwd_fp8" in names:
+            outs.update(o8=torch.empty(shp, dtype=bf, device=dev),
+                        lse8=torch.empty((B_, H_, N_), dtype=torch.float32, device=dev))
+        return d_in, outs
+
+    slots = [new_slot(), new_slot()]
+    result_keys = [k_ for k_ in ("o", "lse", "dq", "dk", "dv", "o8", "lse8") if k_ in slots[0][1]]
+    h_out = [{k_: torch.empty(slots[0][1][k_].shape, dtype=slots[0][1][k_].dtype, pin_memory=True)
+              for k_ in result_keys} for _ in range(2)]
+
+    def compute(d_in, outs, s):
+        attn.attn_fwd(d_in["q"], d_in["k"], d_in["v"], causal=causal, softmax_scale=scale,
+                      o=outs["o"], lse=outs["lse"], stream=s)
+        if "bwd_bf16" in names:
+            attn.attn_bwd(d_in["q"], d_in["k"], d_in["v"], outs["o"], d_in["do"], outs["lse"],
+                          causal=causal, softmax_scale=scale, dq=outs["dq"], dk=outs["dk"],
+                          dv=outs["dv"], workspace=outs["ws"], stream=s)
+        if "fp8_prepass" in names:
+            (q8, k8, v8), (qs, ks, vs) = attn.attn_fp8_quantize(
+                d_in["q32"], d_in["k32"], d_in["v32"], d_in["signs"], stream=s)
+            if "fwd_fp8" in names:
+                attn.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=causal, softmax_scale=scale,
+                                  o=outs["o8"], lse=outs["lse8"], stream=s)
+
+    def upload(d_in):
         for k_, t in h_in.items():
             d_in[k_].copy_(t, non_blocking=True)
-        res = []
-        o, lse = attn.attn_fwd(d_in["q"], d_in["k"], d_in["v"], causal=causal,
-                               softmax_scale=scale)
-        res += [o, lse]
-        if "bwd_bf16" in names:
-            res += list(attn.attn_bwd(d_in["q"], d_in["k"], d_in["v"], o, d_in["do"], lse,
-                                      causal=causal, softmax_scale=scale))
-        if "fp8_prepass" in names:
-            (q8, k8, v8), (qs, ks, vs) = attn.attn_fp8_quantize(d_in["q32"], d_in["k32"],
-                                                                d_in["v32"], d_in["signs"])
-            if "fwd_fp8" in names:
-                res += list(attn.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=causal,
-                                              softmax_scale=scale))
-        for i, t in enumerate(res):
-            if i not in outs:
-                outs[i] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            outs[i].copy_(t, non_blocking=True)
-        return res
+
+    def download(outs, hb):
+        for k_ in result_keys:
+            hb[k_].copy_(outs[k_], non_blocking=True)
+
+    # serial: one stream
+    def serial_step():
+        d_in, outs = slots[0]
+        upload(d_in)
+        compute(d_in, outs, stream)
+        download(outs, h_out[0])
+
+    def timed(run, steps, s_first, s_last):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(s_first)
+        run(steps)
+        b.record(s_last)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    def serial(steps):
+        with torch.cuda.stream(stream):
+            for _ in range(steps):
+                serial_step()
+
+    # (two upload streams measured no faster: the host link is the limit)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def pipelined(steps):
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        comp_done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
+        used = [False, False]
+
+        def start_upload(slot):
+            with torch.cuda.stream(s_in):
+                if used[slot]:
+                    s_in.wait_event(comp_done[slot])       # the step before is done reading them
+                upload(slots[slot][0])
+                in_ready[slot].record(s_in)
+
+        start_upload(0)
+        for k in range(steps):
+            cur, nxt = k % 2, (k + 1) % 2
+            if k + 1 < steps:
+                start_upload(nxt)
+            stream.wait_event(in_ready[cur])
+            if used[cur]:
+                stream.wait_event(out_done[cur])           # step k-2's results are downloaded
+            with torch.cuda.stream(stream):
+                compute(slots[cur][0], slots[cur][1], stream)
+                comp_done[cur].record(stream)
+            used[cur] = True
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[cur])
+                download(slots[cur][1], h_out[cur])
+                out_done[cur].record(s_out)
 
     for _ in range(max(1, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / args.steps
+        serial(1)
+    pipelined(max(2, args.warmup))
+    ms_serial = timed(serial, args.steps, stream, stream)
+    ms = timed(pipelined, args.steps, s_in, s_out)
     flop = sum(f for _, _, f, _ in step_parts)
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
     return {"value": round(flop / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipelined": True,
+            "serial_value": round(flop / (ms_serial * 1e-3) / 1e12, 2),
+            "serial_ms_per_step": round(ms_serial, 4)}
 
 
 def run_sweep(torch, attn, dev, stream, causal, steps=20, warmup=3):
