@@ -451,8 +451,36 @@ def run_sweep(torch, attn, dev, stream, causal, steps=20, warmup=3):
             out[f"{name}_d{d}_h{h}"] = {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1)}
         del q, k, v, do, o, lse
     out.update(run_varlen_gqa(torch, attn, dev, stream, causal, steps, warmup))
+    out.update(run_prepass_rope(torch, attn, dev, stream, steps, warmup))
     assert attn.attn_get_device_status() == 0, attn.attn_last_error()
     return out
+
+
+def run_prepass_rope(torch, attn, dev, stream, steps=20, warmup=3):
+    """The FP8 pre-pass with the rotary embedding fused in (block mode,
+    Hadamard on Q and K) at the timed shape: GB/s of algorithmic bytes (read 3
+    float32 tensors and the two [N, d/2] tables, write 3 e4m3 tensors and the
+    descales)."""
+    import workloads
+    g = torch.Generator(device=dev).manual_seed(9)
+    q, k, v = (torch.randn((B, H, N, D), generator=g, device=dev) for _ in range(3))
+    cos, sin = (torch.from_numpy(t).to(dev) for t in workloads.rope_tables(N, D))
+    signs = torch.where(torch.rand(D, generator=g, device=dev) < 0.5, -1.0, 1.0).float()
+    fn = lambda: attn.attn_fp8_quantize_rope(q, k, v, cos, sin, hadamard_signs=signs, stream=stream)
+    for _ in range(warmup):
+        fn()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    nblk = (N + 127) // 128
+    nbytes = 3 * B * H * N * D * (4 + 1) + 3 * B * H * nblk * 4 + 2 * N * (D // 2) * 4
+    return {f"fp8_prepass_rope_b{B}h{H}n{N}d{D}": {"ms": round(ms, 4),
+                                                    "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}}
 
 
 def run_varlen_gqa(torch, attn, dev, stream, causal, steps=20, warmup=3):

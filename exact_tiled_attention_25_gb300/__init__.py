@@ -32,7 +32,7 @@ _DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 __all__ = ["AttnError", "attn_fwd", "attn_fwd_gqa", "attn_fwd_varlen", "attn_bwd",
            "attn_bwd_gqa", "attn_bwd_varlen", "attn_bwd_varlen_workspace_size",
            "attn_bwd_workspace_size",
-           "attn_fp8_quantize", "attn_fwd_fp8", "attn_get_device_status",
+           "attn_fp8_quantize", "attn_fp8_quantize_rope", "attn_fwd_fp8", "attn_get_device_status",
            "attn_status_string", "attn_last_error", "load_library"]
 
 
@@ -311,6 +311,37 @@ def attn_fp8_quantize(q, k, v, hadamard_signs=None, per_tensor: bool = False, st
                                  *[_ptr(t) for t in outs], *[_ptr(t) for t in desc],
                                  B, H, N, d, int(bool(per_tensor)), _stream(stream))
     _check(code, "attn_fp8_quantize")
+    if host:
+        return tuple(t.cpu() for t in outs), tuple(t.cpu() for t in desc)
+    return tuple(outs), tuple(desc)
+
+
+def attn_fp8_quantize_rope(q, k, v, rope_cos, rope_sin, hadamard_signs=None, stream=None):
+    """attn_fp8_quantize (block mode) with Q and K rotated by the tables
+    rope_cos, rope_sin (float32 [N, d/2]) before the Hadamard transform."""
+    lib = _lib.load()
+    ins = [q, k, v, rope_cos, rope_sin] + ([hadamard_signs] if hadamard_signs is not None else [])
+    ins, host = _to_device(ins)
+    q, k, v, rc, rs = ins[:5]
+    signs = ins[5] if hadamard_signs is not None else None
+    B, H, N, d = _shape4(q, "q")
+    for t, n in ((k, "k"), (v, "v")):
+        if _shape4(t, n) != (B, H, N, d) or t.dtype != torch.float32:
+            raise ValueError(f"{n} must match q")
+    if q.dtype != torch.float32:
+        raise ValueError("FP8 pre-pass inputs are float32")
+    for t, n in ((rc, "rope_cos"), (rs, "rope_sin")):
+        if t.dtype != torch.float32 or tuple(t.shape) != (N, d // 2) or not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous float32 [N, d/2]")
+    if signs is not None and (signs.dtype != torch.float32 or signs.numel() != d):
+        raise ValueError("hadamard_signs must be d float32 values")
+    nblk = (N + 127) // 128
+    outs = [torch.empty((B, H, N, d), dtype=torch.uint8, device=q.device) for _ in range(3)]
+    desc = [torch.empty((B, H, nblk), dtype=torch.float32, device=q.device) for _ in range(3)]
+    code = lib.attn_fp8_quantize_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(rc), _ptr(rs), _ptr(signs),
+                                      *[_ptr(t) for t in outs], *[_ptr(t) for t in desc],
+                                      B, H, N, d, _stream(stream))
+    _check(code, "attn_fp8_quantize_rope")
     if host:
         return tuple(t.cpu() for t in outs), tuple(t.cpu() for t in desc)
     return tuple(outs), tuple(desc)

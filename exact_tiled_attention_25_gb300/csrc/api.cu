@@ -358,6 +358,27 @@ attn_status_t attn_fp8_quantize(const float* q, const float* k, const float* v,
   return launch_fp8_quantize(p, stream);
 }
 
+attn_status_t attn_fp8_quantize_rope(const float* q, const float* k, const float* v,
+                                     const float* rope_cos, const float* rope_sin,
+                                     const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                     uint8_t* v8, float* q_descale, float* k_descale,
+                                     float* v_descale, int B, int H, int N, int d,
+                                     cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if ((s = check_shape(B, H, N, d, 0)) != ATTN_OK) return s;
+  if ((s = check_ptrs({q, k, v, rope_cos, rope_sin, q8, k8, v8, q_descale, k_descale,
+                       v_descale})) != ATTN_OK)
+    return s;
+  if (hadamard_signs && !aligned16(hadamard_signs))
+    return fail(ATTN_ERR_INVALID_ARG, "hadamard_signs not 16-byte aligned");
+  if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
+  if ((s = check_device()) != ATTN_OK) return s;
+  Fp8QuantParams p{{q, k, v}, {q8, k8, v8}, {q_descale, k_descale, v_descale}, hadamard_signs,
+                   B, H, N, d, 0, rope_cos, rope_sin};
+  return launch_fp8_quantize(p, stream);
+}
+
 attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
                            const float* q_descale, const float* k_descale,
                            const float* v_descale, void* o, float* lse, int B, int H, int N,

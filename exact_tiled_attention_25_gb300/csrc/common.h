@@ -80,6 +80,8 @@ struct Fp8QuantParams {
   const float* signs;
   int B, H, N, d;
   int per_tensor;
+  const float* rope_cos = nullptr;   // [N, d/2] rotary tables (block mode), or nullptr
+  const float* rope_sin = nullptr;
 };
 
 struct Fp8FwdParams {

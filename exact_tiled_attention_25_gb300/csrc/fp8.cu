@@ -35,14 +35,21 @@ constexpr float kE4m3Max = 448.f;
 // ============================================================== pre-pass ====
 // Mode: 0 = fused block mode (amax + quantise), 1 = block amax only (into
 // descale), 2 = quantise with the descale already in place.
-template <int MODE>
+// ROPE (block mode): rotary embedding of Q and K rows first, from caller tables
+// rope_cos, rope_sin [N, d/2]: the pair (x_i, x_{i+d/2}) of the row at position
+// n becomes (x_i c - x_{i+d/2} s, x_{i+d/2} c + x_i s), c, s = table[n][i].
+// ("FlashAttention-3: Hopper Asynchrony and FP8 Attention", section "FP8
+// accuracy controls": the Hadamard transform can be fused with the rotary
+// embedding.)
+template <int MODE, bool ROPE = false>
 __global__ void __launch_bounds__(256)
     fp8_quant_kernel(const float* __restrict__ src0, const float* __restrict__ src1,
                      const float* __restrict__ src2, uint8_t* __restrict__ dst0,
                      uint8_t* __restrict__ dst1, uint8_t* __restrict__ dst2,
                      float* __restrict__ desc0, float* __restrict__ desc1,
                      float* __restrict__ desc2, const float* __restrict__ signs, int N,
-                     int nblk) {
+                     int nblk, const float* __restrict__ rope_cos = nullptr,
+                     const float* __restrict__ rope_sin = nullptr) {
   constexpr int D = 128;
   const int which = blockIdx.z;
   const float* src = which == 0 ? src0 : (which == 1 ? src1 : src2);
@@ -65,6 +72,21 @@ __global__ void __launch_bounds__(256)
     const int row = blk * 128 + warp * 16 + r;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (row < N) v = reinterpret_cast<const float4*>(src + (static_cast<size_t>(bh) * N + row) * D)[lane];
+    if (ROPE && which < 2) {
+      // lanes 0..15 hold columns 0..63, lanes 16..31 their partners 64..127
+      const float ox = __shfl_xor_sync(0xffffffffu, v.x, 16);
+      const float oy = __shfl_xor_sync(0xffffffffu, v.y, 16);
+      const float oz = __shfl_xor_sync(0xffffffffu, v.z, 16);
+      const float ow = __shfl_xor_sync(0xffffffffu, v.w, 16);
+      if (row < N) {
+        const size_t t = static_cast<size_t>(row) * (D / 2) + 4 * (lane & 15);
+        const float4 c = *reinterpret_cast<const float4*>(rope_cos + t);
+        const float4 sn = *reinterpret_cast<const float4*>(rope_sin + t);
+        const float sg = (lane < 16) ? -1.f : 1.f;   // first half: x c - partner s
+        v = make_float4(fmaf(sg * ox, sn.x, v.x * c.x), fmaf(sg * oy, sn.y, v.y * c.y),
+                        fmaf(sg * oz, sn.z, v.z * c.z), fmaf(sg * ow, sn.w, v.w * c.w));
+      }
+    }
     if (hadamard) {
       v.x *= s4.x; v.y *= s4.y; v.z *= s4.z; v.w *= s4.w;
       // stages of span 1 and 2 inside the lane (columns 4*lane .. 4*lane+3)
@@ -521,7 +543,12 @@ attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) 
   if (p.B * p.H > 65535 || nblk > 2147483647 / 128)
     return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
   dim3 grid(nblk, p.B * p.H, 3);
-  if (!p.per_tensor) {
+  if (p.rope_cos) {
+    fp8_quant_kernel<0, true><<<grid, 256, 0, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0],
+                                                        p.dst[1], p.dst[2], p.descale[0],
+                                                        p.descale[1], p.descale[2], p.signs, p.N,
+                                                        nblk, p.rope_cos, p.rope_sin);
+  } else if (!p.per_tensor) {
     fp8_quant_kernel<0><<<grid, 256, 0, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1],
                                                   p.dst[2], p.descale[0], p.descale[1],
                                                   p.descale[2], p.signs, p.N, nblk);

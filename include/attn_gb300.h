@@ -234,6 +234,27 @@ attn_status_t attn_fp8_quantize(const float* q, const float* k, const float* v,
                                 cudaStream_t stream);
 
 /*
+ * attn_fp8_quantize_rope -- attn_fp8_quantize (block mode) with the rotary
+ * position embedding of Q and K fused in front of the Hadamard transform
+ * ("FlashAttention-3: Hopper Asynchrony and FP8 Attention", section "FP8
+ * accuracy controls": the transform can be fused with rotary embedding; the
+ * pages do not define the embedding, so the tables come from the caller).
+ *   rope_cos, rope_sin : device float32 [N, d/2]: for the row at position n
+ *                        (0 <= n < N, the same for every b, h) each pair
+ *                        (x_i, x_{i+d/2}), i < d/2, becomes
+ *                        (x_i c - x_{i+d/2} s,  x_{i+d/2} c + x_i s),
+ *                        c = rope_cos[n][i], s = rope_sin[n][i].
+ *   V is not rotated.  hadamard_signs may be NULL (rotation only).  Other
+ *   arguments, outputs and errors as attn_fp8_quantize; d = 128.
+ */
+attn_status_t attn_fp8_quantize_rope(const float* q, const float* k, const float* v,
+                                     const float* rope_cos, const float* rope_sin,
+                                     const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                     uint8_t* v8, float* q_descale, float* k_descale,
+                                     float* v_descale, int B, int H, int N, int d,
+                                     cudaStream_t stream);
+
+/*
  * attn_fwd_fp8 -- FP8 e4m3 forward on the output of attn_fp8_quantize.
  *   q8, k8, v8 : [B, H, N, d] e4m3; d must be 128.
  *   *_descale  : [B, H, ceil(N/128)] float32 block descales.

@@ -18,7 +18,8 @@ from .attention import (attention_forward, attention_backward, attention_probs,
                         attention_forward_rows,
                         attention_forward_head, attention_backward_head)
 from .fp8 import (E4M3_MAX, e4m3_encode, e4m3_decode, sylvester_hadamard,
-                  incoherent_transform, quantize_e4m3_blocks, dequantize_e4m3_blocks)
+                  incoherent_transform, quantize_e4m3_blocks, dequantize_e4m3_blocks,
+                  rotary_embed)
 from .varlen import (attention_forward_gqa, attention_backward_gqa,
                      attention_forward_varlen, attention_backward_varlen)
 
@@ -26,7 +27,7 @@ __all__ = [
     "attention_forward", "attention_backward", "attention_probs", "attention_forward_rows",
     "attention_forward_head", "attention_backward_head",
     "E4M3_MAX", "e4m3_encode", "e4m3_decode", "sylvester_hadamard",
-    "incoherent_transform", "quantize_e4m3_blocks", "dequantize_e4m3_blocks",
+    "incoherent_transform", "quantize_e4m3_blocks", "dequantize_e4m3_blocks", "rotary_embed",
     "attention_forward_gqa", "attention_backward_gqa",
     "attention_forward_varlen", "attention_backward_varlen",
 ]

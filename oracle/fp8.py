@@ -27,6 +27,10 @@ Readings where the pages are silent (each one is listed in the design notes):
   transformed.
 * Per-tensor mode (the comparator in the outlier test) uses one scale for the
   whole tensor and no transform.
+* Rotary embedding (the pages say only that the Hadamard transform can be
+  fused with it): applied to Q and K before the transform, from caller tables
+  cos, sin [N, d/2]; the pair (x_i, x_{i+d/2}) at position n is rotated by the
+  angle whose cosine and sine are cos[n, i], sin[n, i].  V is not rotated.
 """
 from __future__ import annotations
 
@@ -93,12 +97,24 @@ def incoherent_transform(x, signs) -> np.ndarray:
     return x @ m
 
 
+def rotary_embed(x, cos, sin) -> np.ndarray:
+    """Rotate pairs (x_i, x_{i+d/2}) of every row of a [..., N, d] array by the
+    per-position tables cos, sin [N, d/2] (float64)."""
+    x = np.asarray(x, dtype=np.float64)
+    c = np.asarray(cos, dtype=np.float64)
+    s = np.asarray(sin, dtype=np.float64)
+    h = x.shape[-1] // 2
+    a, b = x[..., :h], x[..., h:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
 def quantize_e4m3_blocks(x, block_rows: int = 128, per_tensor: bool = False,
-                         signs=None):
+                         signs=None, rope=None):
     """Quantise a [B, H, N, d] tensor to e4m3 codes with float32 descales.
 
-    Steps, in order: optional incoherent transform (float64, then rounded to
-    float32, the precision the GPU pre-pass holds its values in); amax per
+    Steps, in order: optional rotary embedding (rope = (cos, sin) tables) and
+    incoherent transform (float64, then rounded to float32, the precision the
+    GPU pre-pass holds its values in); amax per
     block (or per tensor); descale = amax / 448 in float32 (1 when amax is 0);
     code = e4m3(x / descale) with a float32 division.
 
@@ -106,6 +122,8 @@ def quantize_e4m3_blocks(x, block_rows: int = 128, per_tensor: bool = False,
     In per-tensor mode every descale entry holds the same value.
     """
     x = np.asarray(x)
+    if rope is not None:
+        x = rotary_embed(x, *rope)
     if signs is not None:
         x = incoherent_transform(x, signs)
     x = x.astype(np.float32)

@@ -107,3 +107,52 @@ def test_fp8_outlier_config_rmse(attn):
     print("fp8 rmse", rmse)
     assert rmse["block"] <= FP8_RMSE and rmse["block_hadamard"] <= FP8_RMSE
     assert rmse["block_hadamard"] < rmse["per_tensor"]
+
+
+@pytest.mark.parametrize("with_hadamard", [False, True])
+@pytest.mark.parametrize("N", [1, 300, 1024])
+def test_quantiser_with_rope(attn, N, with_hadamard):
+    """Rotary embedding fused in front of the Hadamard: the GPU rotates and
+    transforms in float32, the oracle in float64, so descales agree to float32
+    rounding and codes differ by at most one e4m3 step, rarely."""
+    shape = (2, 2, N, 128)
+    xs = workloads.normal_with_outliers(13 + N, shape, 3)
+    signs = workloads.random_signs(5, 128) if with_hadamard else None
+    cos, sin = workloads.rope_tables(N, 128)
+    g = [torch.from_numpy(x).to(dev()) for x in xs]
+    s = None if signs is None else torch.from_numpy(signs).to(dev())
+    codes, desc = attn.attn_fp8_quantize_rope(*g, torch.from_numpy(cos).to(dev()),
+                                              torch.from_numpy(sin).to(dev()), hadamard_signs=s)
+    check_status(attn)
+    for which, (x, c, d) in enumerate(zip(xs, codes, desc)):
+        c, d = c.cpu().numpy(), d.cpu().numpy()
+        rc, rd = oracle.quantize_e4m3_blocks(x, signs=signs if which < 2 else None,
+                                             rope=(cos, sin) if which < 2 else None)
+        if which == 2:                                 # V is neither rotated nor transformed
+            np.testing.assert_array_equal(d, rd)
+            np.testing.assert_array_equal(c, rc)
+            continue
+        np.testing.assert_allclose(d, rd, rtol=4e-6)
+        got, ref = oracle.e4m3_decode(c), oracle.e4m3_decode(rc)
+        step = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -6))) - 3)
+        assert np.all(np.abs(got - ref) <= step * 1.0001)
+        assert np.mean(c != rc) < 2e-3
+
+
+def test_fp8_forward_with_rope_matches_rotated_attention(attn):
+    """Scores of the rotated Q, K: the FP8 forward on the fused pre-pass output
+    against exact float64 attention on the rotated float32 inputs."""
+    B, H, N, d = 1, 2, 640, 128
+    q, k, v = workloads.normal_with_outliers(44, (B, H, N, d), 3)
+    signs = workloads.random_signs(5, d)
+    cos, sin = workloads.rope_tables(N, d)
+    g = [torch.from_numpy(x).to(dev()) for x in (q, k, v)]
+    (q8, k8, v8), (qd, kd, vd) = attn.attn_fp8_quantize_rope(
+        *g, torch.from_numpy(cos).to(dev()), torch.from_numpy(sin).to(dev()),
+        hadamard_signs=torch.from_numpy(signs).to(dev()))
+    o, lse = attn.attn_fwd_fp8(q8, k8, v8, qd, kd, vd, causal=True, softmax_scale=1 / np.sqrt(d))
+    check_status(attn)
+    rq, rk = oracle.rotary_embed(q, cos, sin), oracle.rotary_embed(k, cos, sin)
+    ref_o, _ = oracle.attention_forward(rq, rk, v, 1 / np.sqrt(d), True)
+    err = o.float().cpu().numpy() - ref_o
+    assert np.sqrt(np.mean(err ** 2)) <= FP8_RMSE

@@ -111,3 +111,12 @@ def varlen_lengths(seed: int, B: int, max_len: int, min_len: int = 0):
     lens = rng.integers(min_len, max_len + 1, size=B).astype(np.int64)
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     return cu, lens
+
+
+def rope_tables(N: int, d: int, base: float = 10000.0):
+    """float32 rotary tables cos, sin [N, d/2] of the common frequency ladder
+    theta_i = base^(-2i/d) at positions 0..N-1 (an input, like the Hadamard
+    signs: the kernels and the oracle both take the tables as given)."""
+    i = np.arange(d // 2, dtype=np.float64)
+    ang = np.arange(N, dtype=np.float64)[:, None] * base ** (-2.0 * i / d)[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
