@@ -452,7 +452,45 @@ def run_sweep(torch, attn, dev, stream, causal, steps=20, warmup=3):
         del q, k, v, do, o, lse
     out.update(run_varlen_gqa(torch, attn, dev, stream, causal, steps, warmup))
     out.update(run_prepass_rope(torch, attn, dev, stream, steps, warmup))
+    out.update(run_decode(torch, attn, dev, stream, steps, warmup))
     assert attn.attn_get_device_status() == 0, attn.attn_last_error()
+    return out
+
+
+def run_decode(torch, attn, dev, stream, steps=20, warmup=3):
+    """Paged decode: 16 sequences of 8192 cached tokens, H = 32 query heads
+    sharing H_kv = 8 key/value heads, d = 128, pages of 64 tokens in a shuffled
+    order, n_q = 1 and 4 new tokens (causal).  GB/s of algorithmic bytes: the
+    cached keys and values read once, plus Q and O."""
+    Bq, L, h, hkv, d, ps = 16, 8192, 32, 8, 128, 64
+    npg = Bq * L // ps
+    g = torch.Generator(device=dev).manual_seed(10)
+    kc, vc = (torch.randn((npg, ps, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+              for _ in range(2))
+    table = torch.randperm(npg, generator=g, device=dev).to(torch.int32).view(Bq, L // ps)
+    lens = torch.full((Bq,), L, dtype=torch.int32, device=dev)
+    out = {}
+    for n_q in (1, 4):
+        q = torch.randn((Bq, h, n_q, d), generator=g, device=dev).to(torch.bfloat16)
+        o = torch.empty_like(q)
+        lse = torch.empty((Bq, h, n_q), dtype=torch.float32, device=dev)
+        ws = torch.empty(attn.attn_decode_workspace_size(Bq, h, hkv, n_q, d, L), dtype=torch.uint8,
+                         device=dev)
+        fn = lambda: attn.attn_decode_paged(q, kc, vc, table, lens, L, causal=True, o=o, lse=lse,
+                                            workspace=ws, stream=stream)
+        for _ in range(warmup):
+            fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        nbytes = 2 * Bq * L * hkv * d * 2 + 2 * Bq * h * n_q * d * 2
+        out[f"decode_b{Bq}_len{L}_h{h}kv{hkv}_d{d}_nq{n_q}_page{ps}"] = {
+            "ms": round(ms, 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
     return out
 
 

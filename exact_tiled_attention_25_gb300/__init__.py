@@ -32,7 +32,8 @@ _DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 __all__ = ["AttnError", "attn_fwd", "attn_fwd_gqa", "attn_fwd_varlen", "attn_bwd",
            "attn_bwd_gqa", "attn_bwd_varlen", "attn_bwd_varlen_workspace_size",
            "attn_bwd_workspace_size",
-           "attn_fp8_quantize", "attn_fp8_quantize_rope", "attn_fwd_fp8", "attn_get_device_status",
+           "attn_fp8_quantize", "attn_fp8_quantize_rope", "attn_fwd_fp8",
+           "attn_decode_paged", "attn_decode_workspace_size", "attn_get_device_status",
            "attn_status_string", "attn_last_error", "load_library"]
 
 
@@ -345,6 +346,49 @@ def attn_fp8_quantize_rope(q, k, v, rope_cos, rope_sin, hadamard_signs=None, str
     if host:
         return tuple(t.cpu() for t in outs), tuple(t.cpu() for t in desc)
     return tuple(outs), tuple(desc)
+
+
+def attn_decode_workspace_size(B: int, H: int, H_kv: int, n_q: int, d: int, max_seqlen: int) -> int:
+    return int(_lib.load().attn_decode_workspace_size(B, H, H_kv, n_q, d, max_seqlen))
+
+
+def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, max_seqlen: int,
+                      causal: bool = True, softmax_scale: float | None = None, o=None, lse=None,
+                      workspace=None, stream=None):
+    """Decode step: q [B, H, n_q, d] against a paged cache [num_pages, page_size, H_kv, d]
+    with an int32 block table [B, max_pages] and int32 seq_lens [B];
+    returns O [B, H, n_q, d] and LSE float32 [B, H, n_q]."""
+    lib = _lib.load()
+    (q, k_cache, v_cache, block_table, seq_lens), host = _to_device(
+        [q, k_cache, v_cache, block_table, seq_lens])
+    B, H, n_q, d = _shape4(q, "q")
+    num_pages, page_size, Hkv, dk = _shape4(k_cache, "k_cache")
+    if tuple(v_cache.shape) != (num_pages, page_size, Hkv, dk) or not v_cache.is_contiguous():
+        raise ValueError("v_cache must match k_cache")
+    if dk != d or q.dtype not in _DTYPES or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise ValueError("q and the caches must share d and dtype (bfloat16 or float16)")
+    for t, n, shp in ((block_table, "block_table", 2), (seq_lens, "seq_lens", 1)):
+        if t.dtype != torch.int32 or t.dim() != shp or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 tensor of rank {shp}")
+    if block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_table and seq_lens need one entry per sequence")
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, n_q), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(attn_decode_workspace_size(B, H, Hkv, n_q, d, int(max_seqlen)),
+                                dtype=torch.uint8, device=q.device)
+    code = lib.attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                 _ptr(seq_lens), _ptr(o), _ptr(lse), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), B, H, Hkv, n_q, d,
+                                 num_pages, page_size, block_table.shape[1], int(max_seqlen),
+                                 int(bool(causal)), scale, _DTYPES[q.dtype], _stream(stream))
+    _check(code, "attn_decode_paged")
+    if host:
+        return o.cpu(), lse.cpu()
+    return o, lse
 
 
 def attn_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, causal: bool = False,

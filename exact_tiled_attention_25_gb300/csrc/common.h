@@ -135,4 +135,55 @@ inline BwdWorkspace bwd_workspace_layout_packed(int B, int max_seqlen, int total
                                        ((static_cast<size_t>(max_seqlen) + 127) / 128 * 128), d);
 }
 
+// Paged decode (few new query tokens per sequence against a paged cache).
+struct DecodeParams {
+  const void* q;            // [B, H, n_q, d]
+  const void* k_cache;      // [num_pages, page_size, H_kv, d]
+  const void* v_cache;
+  const int* block_table;   // [B, max_pages]
+  const int* seq_lens;      // [B]
+  void* o;                  // [B, H, n_q, d]
+  float* lse;               // [B, H, n_q]
+  float* o_part;            // workspace: [B, H, n_q, splits, d] float32
+  float* lse_part;          // workspace: [B, H, n_q, splits] float32
+  int B, H, H_kv, n_q, d;
+  int num_pages, page_size, max_pages, max_seqlen;
+  int causal;
+  float scale;
+  int fp16;
+};
+
+// Key-range splits of a decode call, each a whole number of 128-key tiles.
+// One CTA runs per SM at a time, so the split size minimises the modelled time
+// ceil(CTAs / 152) waves x (tiles per CTA + about 1.5 tiles of per-CTA start-up
+// and drain), trading the last wave's idle SMs against start-up costs.
+struct DecodeSplits {
+  int splits, tiles_per_split;
+};
+inline DecodeSplits decode_splits(int B, int H_kv, int max_seqlen) {
+  const int ntiles = (max_seqlen + 127) / 128;
+  const long long base = static_cast<long long>(B) * H_kv;
+  int best_tps = ntiles;
+  double best = 1e300;
+  for (int tps = 1; tps <= ntiles; ++tps) {
+    const long long splits = (ntiles + tps - 1) / tps;
+    if (tps > 1 && (ntiles + tps - 2) / (tps - 1) == splits) continue;   // same split count
+    const long long waves = (base * splits + 151) / 152;
+    const double cost = static_cast<double>(waves) * (tps + 1.5);
+    if (cost < best) {
+      best = cost;
+      best_tps = tps;
+    }
+  }
+  return {(ntiles + best_tps - 1) / best_tps, best_tps};
+}
+
+inline size_t decode_workspace_bytes(int B, int H, int H_kv, int n_q, int d, int max_seqlen) {
+  const DecodeSplits sp = decode_splits(B, H_kv, max_seqlen);
+  const size_t rows = static_cast<size_t>(B) * H * n_q * sp.splits;
+  return align_up(rows * d * sizeof(float), 256) + align_up(rows * sizeof(float), 256);
+}
+
+attn_status_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
 }  // namespace attn

@@ -1,0 +1,480 @@
+// BF16/FP16 decode attention over a paged key/value cache on sm_103a.
+//
+// Method: "FlashAttention-3: Hopper Asynchrony and FP8 Attention", section
+// "Where It Breaks", leaves a decode-focused inference kernel as open work;
+// "FlashAttention 3 Hardware Acceleration: Hopper GPU Strategies for
+// Long-Context Enterprise Inference Optimization" describes the key/value
+// cache held in fixed-size blocks ("Memory Fragmentation") and separate
+// prefill and decode functions ("Production Inference Engines").  The
+// arithmetic is the forward pass of exact attention for a few new query
+// tokens per sequence.
+//
+// GB300 design:
+//  * One query tile holds the G = H / H_kv query heads that share a key/value
+//    head times the n_q new tokens (G * n_q <= 128 rows); in [B, H, n_q, d]
+//    these rows are contiguous, so one TMA box per 64 columns loads them.  The
+//    key/value head is then read once for all of them: a decode step is bound
+//    by HBM bandwidth over the cache, and the tensor cores (S = Q K^T, O += P V
+//    through tensor memory, as in the forward) have ample headroom.
+//  * Keys and values come from a cache [num_pages, page_size, H_kv, d] through
+//    a 4-D tensor map; a 128-key tile is fetched page by page through the
+//    block table (one box of min(page_size, 128) rows per page).  Tokens past
+//    the sequence end and pages outside the cache are fetched as zeros.
+//  * The key range of a sequence is split across CTAs (flash-decoding): each
+//    split writes its partial O / l and log-sum-exp per row, and a combine
+//    kernel merges the splits by their log-sum-exps.
+//  * The score tile is double-buffered in tensor memory, so S(j + 1) is
+//    computed while the softmax of tile j runs.
+//  * Causal masking is bottom-right aligned: query token t of n_q sits at
+//    position len - n_q + t and sees keys 0 .. len - n_q + t.
+#include <cmath>
+
+#include "common.h"
+#include "sm103_prims.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kSmemLimit = 232448;
+constexpr int DBM = 128;   // query-tile rows
+constexpr int DBN = 128;   // keys per tile
+
+template <int D>
+struct DecCfg {
+  static constexpr int CH = D / 64;                   // 128-byte column chunks per row
+  static constexpr int CHUNK = DBM * 128;             // one 128-row x 128-byte chunk
+  static constexpr int TILE = DBM * D * 2;            // a Q, K or V tile
+  static constexpr int NSLOT_FIT = (kSmemLimit - 2048 - TILE) / TILE;
+  static constexpr int NSLOT = NSLOT_FIT > 8 ? 8 : NSLOT_FIT;
+  static constexpr int SMEM = 1024 + TILE + NSLOT * TILE;
+  static constexpr int THREADS = 6 * 32;              // 4 softmax warps, producer, MMA
+  static constexpr int LOAD_WARP = 4;
+  static constexpr int MMA_WARP = 5;
+  __host__ __device__ static constexpr uint32_t S_COL(int buf) { return 128u * buf; }
+  static constexpr uint32_t O_COL = 256;
+  static_assert(NSLOT >= 4, "ring too short");
+  static_assert(O_COL + D <= 512, "TMEM overflow");
+};
+
+struct DecKParams {
+  const int* block_table;   // [B, max_pages]
+  const int* seq_lens;      // [B]
+  float* o_part;            // [B, H, n_q, splits, D]: O / l of each split
+  float* lse_part;          // [B, H, n_q, splits]
+  int* status;
+  int H, group, n_q, rows_real;
+  int max_pages, page_size, box_rows, num_pages;
+  int splits, tiles_per_split;
+  int causal;
+  float scale_log2;
+};
+
+__device__ __forceinline__ float lg2_dec(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int D, bool FP16>
+__global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const DecKParams kp) {
+  using C = DecCfg<D>;
+  constexpr int NSLOT = C::NSLOT;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + C::TILE;
+
+  __shared__ __align__(8) uint64_t q_full;
+  __shared__ __align__(8) uint64_t kv_full[NSLOT];
+  __shared__ __align__(8) uint64_t kv_empty[NSLOT];
+  __shared__ __align__(8) uint64_t s_full[2];    // per score buffer
+  __shared__ __align__(8) uint64_t p_full[2];    // per score buffer
+  __shared__ __align__(8) uint64_t pv_done;      // one phase per tile
+  __shared__ __align__(8) uint64_t o_full;
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ int load_items_sh;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int split = blockIdx.x;
+  const int hk = blockIdx.y;
+  const int b = blockIdx.z;
+  const int len = kp.seq_lens[b];
+  if (len < 0 || len > kp.max_pages * kp.page_size) {
+    if (threadIdx.x == 0) atomicCAS(kp.status, 0, kDevBadSeqlens);
+    return;
+  }
+  const int ntiles = (len + DBN - 1) / DBN;
+  const int j0 = split * kp.tiles_per_split;
+  const int nK = max(0, min(ntiles, j0 + kp.tiles_per_split) - j0);
+  const int r = warp * 32 + lane;             // query-tile row of a softmax thread
+  const int gq = r / kp.n_q, tq = r - gq * kp.n_q;
+  const size_t prow = (static_cast<size_t>(b) * kp.H + hk * kp.group + gq) * kp.n_q + tq;
+  if (nK == 0) {
+    // no keys in this split: it contributes nothing to the merge
+    if (warp < 4 && r < kp.rows_real) kp.lse_part[prow * kp.splits + split] = -INFINITY;
+    return;
+  }
+  const int total_items = 2 * nK;              // K_0, V_0, K_1, V_1, ... of this split
+
+  if (threadIdx.x == 0) {
+    mbar_init(&q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+    }
+    mbar_init(&pv_done, 1);
+    mbar_init(&o_full, 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    load_items_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+  const Abort ab{&abort_sh, kp.status};
+
+  if (warp == C::LOAD_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(&q_full, C::TILE);
+#pragma unroll
+      for (int c = 0; c < C::CH; ++c)
+        tma_load_3d(sQ + c * C::CHUNK, &tmQ, &q_full, c * 64, hk * kp.group * kp.n_q, b);
+      const int* table = kp.block_table + static_cast<size_t>(b) * kp.max_pages;
+      const int nbox = DBN / kp.box_rows;
+      int it = 0;
+      bool ok = true;
+      for (int j = 0; j < nK && ok; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int slot = it % NSLOT;
+          const int use = it / NSLOT;
+          if (use >= 1 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, ab, kDevTimeoutLoad)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&kv_full[slot], C::TILE);
+          uint8_t* dst = sKV + slot * C::TILE;
+          for (int x = 0; x < nbox; ++x) {
+            const int tok = (j0 + j) * DBN + x * kp.box_rows;
+            const int page = tok / kp.page_size;
+            int phys = kp.num_pages;               // out of range: zero-filled box
+            if (tok < len && page < kp.max_pages) {
+              const int pg = table[page];
+              if (pg >= 0 && pg < kp.num_pages) phys = pg;
+              else atomicCAS(kp.status, 0, kDevBadSeqlens);
+            }
+#pragma unroll
+            for (int c = 0; c < C::CH; ++c)
+              tma_load_4d(dst + c * C::CHUNK + x * kp.box_rows * 128, kv ? &tmV : &tmK,
+                          &kv_full[slot], c * 64, tok % kp.page_size, hk, phys);
+          }
+          ++it;
+        }
+      }
+      load_items_sh = it;
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr Elt E = FP16 ? Elt::F16 : Elt::BF16;
+      constexpr uint32_t idS = idesc_f16(E, 128, DBN, false, false);
+      constexpr uint32_t idPV = idesc_f16(E, 128, D, false, true);
+      const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);              // K-major Q
+      const uint64_t kdesc0 = sdesc_sw128(smem_u32(sKV), 16, 1024);            // K-major K
+      const uint64_t vdesc0 = sdesc_sw128(smem_u32(sKV), C::CHUNK, 1024);      // MN-major V
+      bool ok = mbar_wait(&q_full, 0, ab, kDevTimeoutMma);
+      // S(jj) = Q K_jj^T into buffer jj % 2
+      auto issue_s = [&](int jj) -> bool {
+        const int item = 2 * jj;
+        const int slot = item % NSLOT;
+        if (!mbar_wait(&kv_full[slot], (item / NSLOT) & 1, ab, kDevTimeoutMma)) return false;
+        const uint64_t kdesc = opaque(sdesc_add(kdesc0, slot * C::TILE));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::CHUNK + (kk % 4) * 32;
+          mma_f16_ss(tmem + C::S_COL(jj & 1), sdesc_add(qdesc, off), sdesc_add(kdesc, off), idS,
+                     kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[jj & 1]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && nK > 1) ok = issue_s(1);
+      for (int j = 0; j < nK && ok; ++j) {
+        // O += P(j) V_j, P(j) packed 16-bit in columns [0, 64) of buffer j % 2
+        const int item = 2 * j + 1;
+        const int slot = item % NSLOT;
+        if (!(ok = mbar_wait(&kv_full[slot], (item / NSLOT) & 1, ab, kDevTimeoutMma))) break;
+        const uint64_t vdesc = opaque(sdesc_add(vdesc0, slot * C::TILE));
+        if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1, ab, kDevTimeoutMma))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < DBN / 16; ++kk)
+          mma_f16_ts(tmem + C::O_COL, tmem + C::S_COL(j & 1) + 8 * kk,
+                     sdesc_add(vdesc, kk * 16 * 128), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&pv_done);
+        if (j == nK - 1) mma_commit(&o_full);
+        if (j + 2 < nK) ok = issue_s(j + 2);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    // Thread r owns row r (TMEM lane r) of S and O.
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const float c2 = kp.scale_log2;
+    // keys this row may see: all of the sequence, or (causal) up to its position
+    const int vis_end = kp.causal ? min(len, len - kp.n_q + tq + 1) : len;
+    float m_ref = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nK; ++j) {
+      if (__any_sync(0xffffffffu, !mbar_wait(&s_full[j & 1], (j >> 1) & 1, ab, kDevTimeoutSoftmax))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      if (r == 0) {
+        // S(j) complete: every MMA reading K_j, and (issued before S(j)) the
+        // P V product that read V_{j-2}, has completed.  Release only slots
+        // the producer refills.
+        if (2 * j + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j) % NSLOT]);
+        if (j >= 2 && 2 * j - 3 + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j - 3) % NSLOT]);
+      }
+      const uint32_t tS = tmem + lane_addr + C::S_COL(j & 1);
+      uint32_t sr[DBN];
+#pragma unroll
+      for (int c0 = 0; c0 < DBN / 32; ++c0)
+        tmem_ld32(tS + c0 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0 * 32]));
+      tmem_ld_wait();
+      const int kbase = (j0 + j) * DBN;
+      if (kbase + DBN > vis_end) {
+        const int lim = vis_end - kbase;
+#pragma unroll
+        for (int c = 0; c < DBN; ++c)
+          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+      }
+      float mx[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        mx[u] = fmax3(__uint_as_float(sr[8 * u]), __uint_as_float(sr[8 * u + 1]),
+                      fmax3(__uint_as_float(sr[8 * u + 2]), __uint_as_float(sr[8 * u + 3]),
+                            fmax3(__uint_as_float(sr[8 * u + 4]), __uint_as_float(sr[8 * u + 5]),
+                                  fmaxf(__uint_as_float(sr[8 * u + 6]), __uint_as_float(sr[8 * u + 7])))));
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], mx[u + 8]);
+      const float m_new = fmaxf(m_ref, fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                             fmaxf(mx[6], mx[7])));
+      // lazy rescale: move the exponent reference only when the max grew by
+      // more than 2^8
+      const bool need = (m_new - m_ref) * c2 > 8.f;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2_approx((m_ref - m_new) * c2);
+        l *= alpha;
+        m_ref = m_new;
+      }
+      const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref * c2;
+      const uint64_t cc = pack2(c2, c2);
+      const uint64_t nn = pack2(neg, neg);
+      uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+      for (int c0 = 0; c0 < DBN / 32; ++c0) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = c0 * 32 + 2 * i;
+          const uint64_t y = ffma2(pack2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), cc, nn);
+          const float p0 = ex2_approx(lo2(y));
+          const float p1 = ex2_approx(hi2(y));
+          if (i & 1) acc1 = fadd2(acc1, pack2(p0, p1));
+          else acc0 = fadd2(acc0, pack2(p0, p1));
+          pk[i] = FP16 ? cvt_pack_f16(p0, p1) : cvt_pack_bf16(p0, p1);
+        }
+        // packed P of keys [32 c0, +32) -> columns [16 c0, +16)
+        tmem_st16(tS + c0 * 16, pk);
+      }
+      const uint64_t acc = fadd2(acc0, acc1);
+      l += lo2(acc) + hi2(acc);
+      // Rescale O.  P(j-1) V_{j-1} may still be in flight (it is issued after
+      // step j-1 ends), so wait for it; this step's product is issued only
+      // after the arrive below.
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        if (__any_sync(0xffffffffu, !mbar_wait(&pv_done, (j - 1) & 1, ab, kDevTimeoutSoftmax))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll 1
+        for (int c0 = 0; c0 < D / 32; ++c0) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_addr + C::O_COL + c0 * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tmem + lane_addr + C::O_COL + c0 * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&p_full[j & 1]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && !__any_sync(0xffffffffu, !mbar_wait(&o_full, 0, ab, kDevTimeoutEpilogue))) {
+      tc_fence_after_sync();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      float* dst = kp.o_part + (prow * kp.splits + split) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 32; ++c0) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_addr + C::O_COL + c0 * 32, o);
+        tmem_ld_wait();
+        if (r < kp.rows_real) {
+          float4* d4 = reinterpret_cast<float4*>(dst + c0 * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            d4[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+        }
+      }
+      if (r < kp.rows_real)
+        kp.lse_part[prow * kp.splits + split] =
+            l > 0.f ? (m_ref * c2 + lg2_dec(l)) * 0.69314718055994530942f : -INFINITY;
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (abort_sh) {
+    if (warp == C::LOAD_WARP && lane == 0) {
+      mbar_wait_drain(&q_full, 0);
+      const int issued = load_items_sh;
+      for (int s = 0; s < NSLOT && s < issued; ++s)
+        mbar_wait_drain(&kv_full[s], ((issued - 1 - s) / NSLOT) & 1);
+    }
+    if (warp == C::MMA_WARP && lane == 0) {
+      mma_commit(&drain_bar);
+      mbar_wait_drain(&drain_bar, 0);
+    }
+    __syncthreads();
+  }
+  if (warp == C::MMA_WARP) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge the splits of every (b, h, t) row: LSE = log sum_s exp(lse_s) and
+// O = sum_s exp(lse_s - LSE) O_s.  One warp per row, D / 32 columns per lane.
+template <int D, bool FP16>
+__global__ void __launch_bounds__(256)
+    decode_combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                          uint16_t* __restrict__ o, float* __restrict__ lse, long long rows,
+                          int splits) {
+  constexpr int PER = D / 32;
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float* lp = lse_part + row * splits;
+  float mx = -INFINITY;
+  for (int s = lane; s < splits; s += 32) mx = fmaxf(mx, lp[s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  float sum = 0.f;
+  if (mx != -INFINITY)
+    for (int s = lane; s < splits; s += 32) sum += expf(lp[s] - mx);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  const float total = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = 0; s < splits; ++s) {
+      const float ls = lp[s];
+      if (ls == -INFINITY) continue;
+      const float w = expf(ls - total);
+      const float* op = o_part + (row * splits + s) * D + lane * PER;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, op[i], acc[i]);
+    }
+  }
+  uint16_t* orow = o + row * D + lane * PER;
+#pragma unroll
+  for (int i = 0; i < PER; i += 2) {
+    const uint32_t pk = FP16 ? cvt_pack_f16(acc[i], acc[i + 1]) : cvt_pack_bf16(acc[i], acc[i + 1]);
+    *reinterpret_cast<uint32_t*>(orow + i) = pk;
+  }
+  if (lane == 0) lse[row] = total;
+}
+
+template <int D, bool FP16>
+attn_status_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
+  using C = DecCfg<D>;
+  auto kern = decode_split_kernel<D, FP16>;
+  attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), C::SMEM);
+  if (s != ATTN_OK) return s;
+  CUtensorMap tq, tk, tv;
+  // Q: {d, H * n_q rows, B}: the query tile of key/value head hk starts at row
+  // hk * G * n_q
+  if ((s = make_tmap_3d(&tq, p.q, 2, D, static_cast<uint64_t>(p.H) * p.n_q, p.B, 64, DBM)) != ATTN_OK)
+    return s;
+  // cache: {d, page_size, H_kv, num_pages}, one box per page (or per 128 rows)
+  const int box_rows = p.page_size < DBN ? p.page_size : DBN;
+  const uint64_t tok_b = 2ull * p.H_kv * D, head_b = 2ull * D, page_b = tok_b * p.page_size;
+  if ((s = make_tmap_4d(&tk, p.k_cache, 2, D, p.page_size, p.H_kv, p.num_pages, tok_b, head_b, page_b, 64,
+                        box_rows)) != ATTN_OK)
+    return s;
+  if ((s = make_tmap_4d(&tv, p.v_cache, 2, D, p.page_size, p.H_kv, p.num_pages, tok_b, head_b, page_b, 64,
+                        box_rows)) != ATTN_OK)
+    return s;
+  int* status = device_status_word();
+  if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
+  const DecodeSplits sp = decode_splits(p.B, p.H_kv, p.max_seqlen);
+  DecKParams kp{p.block_table, p.seq_lens, p.o_part,  p.lse_part,  status,
+                p.H,           p.H / p.H_kv, p.n_q,   (p.H / p.H_kv) * p.n_q,
+                p.max_pages,   p.page_size, box_rows, p.num_pages,
+                sp.splits,     sp.tiles_per_split, p.causal, p.scale * 1.4426950408889634f};
+  kern<<<dim3(sp.splits, p.H_kv, p.B), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, kp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "decode split kernel launch");
+  const long long rows = static_cast<long long>(p.B) * p.H * p.n_q;
+  decode_combine_kernel<D, FP16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
+      p.o_part, p.lse_part, static_cast<uint16_t*>(p.o), p.lse, rows, sp.splits);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "decode combine kernel launch");
+  return ATTN_OK;
+}
+
+}  // namespace
+
+attn_status_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
+  if (p.B > 65535 || p.H_kv > 65535) return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
+  switch (p.d) {
+    case 64: return p.fp16 ? launch_decode_t<64, true>(p, stream) : launch_decode_t<64, false>(p, stream);
+    case 128: return p.fp16 ? launch_decode_t<128, true>(p, stream) : launch_decode_t<128, false>(p, stream);
+  }
+  return fail(ATTN_ERR_UNSUPPORTED, "decode supports d = 64 and 128");
+}
+
+}  // namespace attn

@@ -210,6 +210,51 @@ attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, cons
                                float softmax_scale, attn_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * attn_decode_workspace_size -- bytes of device scratch attn_decode_paged needs
+ * for the partial results of its key-range splits (float32 O and log-sum-exp
+ * per split and query row).  Returns 0 for invalid sizes.
+ */
+size_t attn_decode_workspace_size(int B, int H, int H_kv, int n_q, int d, int max_seqlen);
+
+/*
+ * attn_decode_paged -- decode step: n_q new query tokens per sequence against a
+ * paged key/value cache, with grouped-query heads.
+ *   q           : [B, H, n_q, d] in `dtype`; token t of sequence b is at position
+ *                 seq_lens[b] - n_q + t (its keys and values are already in the
+ *                 cache).
+ *   k_cache,
+ *   v_cache     : [num_pages, page_size, H_kv, d] in `dtype`.
+ *   block_table : DEVICE int32 [B, max_pages]: logical page p of sequence b is
+ *                 physical page block_table[b][p].
+ *   seq_lens    : DEVICE int32 [B]: tokens of each sequence in the cache
+ *                 (0 <= seq_lens[b] <= max_pages * page_size).
+ *   o           : [B, H, n_q, d] in `dtype`;  lse : [B, H, n_q] float32 (natural
+ *                 log of the scaled, masked scores; -inf and O = 0 for a row
+ *                 that sees no key).
+ *   workspace   : at least attn_decode_workspace_size(B, H, H_kv, n_q, d,
+ *                 max_seqlen) bytes, 256-byte aligned.
+ *   max_seqlen  : >= every seq_lens[b] (sizes the key-range split).
+ *   causal      : 1 = query t sees keys 0 .. seq_lens[b] - n_q + t (bottom-right
+ *                 aligned); 0 = every key of the sequence.
+ * Limits: d = 64 or 128; (H / H_kv) * n_q <= 128; page_size a power of two in
+ * [8, 65536].  Out-of-range seq_lens or block_table entries are skipped on the
+ * device and reported by attn_get_device_status() as ATTN_ERR_INVALID_ARG.
+ * Source: exact attention ("FlashAttention-3: Hopper Asynchrony and FP8
+ * Attention", "Symbol Map"; its section "Where It Breaks" leaves a
+ * decode-focused kernel as open work) over the paged cache of "FlashAttention 3
+ * Hardware Acceleration: Hopper GPU Strategies for Long-Context Enterprise
+ * Inference Optimization", sections "Memory Fragmentation" (the cache in
+ * fixed-size blocks) and "Production Inference Engines" (separate decode
+ * functions).
+ */
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                                const int* block_table, const int* seq_lens, void* o, float* lse,
+                                void* workspace, size_t workspace_bytes, int B, int H, int H_kv,
+                                int n_q, int d, int num_pages, int page_size, int max_pages,
+                                int max_seqlen, int causal, float softmax_scale,
+                                attn_dtype_t dtype, cudaStream_t stream);
+
+/*
  * attn_fp8_quantize -- FP8 e4m3 pre-pass with block scaling and incoherent
  * processing ("FlashAttention-3: Hopper Asynchrony and FP8 Attention", section
  * "FP8 accuracy controls").

@@ -162,3 +162,24 @@ def test_varlen_workspace_size(lib):
     code = lib.attn_bwd_varlen(16, 16, 16, 16, 16, 16, 16, 16, 16, 256, ws - 1, 16,
                                2, 128, 200, 2, 1, 64, 0, 0.1, 0, None)
     assert code == 1 and b"workspace" in lib.attn_last_error()
+
+
+def test_decode_is_declared_and_validates(lib):
+    names = declared_functions()
+    assert "attn_decode_paged" in names and "attn_decode_workspace_size" in names
+    ws = lib.attn_decode_workspace_size(2, 8, 2, 1, 128, 1000)
+    assert ws > 0 and lib.attn_decode_workspace_size(0, 8, 2, 1, 128, 1000) == 0
+
+    def call(**kw):
+        a = dict(B=2, H=8, H_kv=2, n_q=1, d=128, num_pages=10, page_size=64, max_pages=5,
+                 max_seqlen=300, causal=1, scale=0.1, ws=ws)
+        a.update(kw)
+        return lib.attn_decode_paged(16, 16, 16, 16, 16, 16, 16, 256, a["ws"], a["B"], a["H"],
+                                     a["H_kv"], a["n_q"], a["d"], a["num_pages"], a["page_size"],
+                                     a["max_pages"], a["max_seqlen"], a["causal"], a["scale"], 0, None)
+    for kw, code, why in ((dict(page_size=48), 1, "page_size"), (dict(page_size=4), 1, "page_size"),
+                          (dict(d=256), 1, "d ="), (dict(H_kv=3), 1, "H_kv"),
+                          (dict(H=64, H_kv=1, n_q=4), 2, "128"), (dict(ws=ws - 1), 1, "workspace"),
+                          (dict(causal=2), 1, "causal")):
+        assert call(**kw) == code, kw
+        assert why.lower() in lib.attn_last_error().decode().lower(), (kw, lib.attn_last_error())

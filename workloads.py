@@ -120,3 +120,23 @@ def rope_tables(N: int, d: int, base: float = 10000.0):
     i = np.arange(d // 2, dtype=np.float64)
     ang = np.arange(N, dtype=np.float64)[:, None] * base ** (-2.0 * i / d)[None, :]
     return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def paged_cache(seed: int, seq_lens, page_size: int, H_kv: int, d: int, spare_pages: int = 3):
+    """A paged key/value cache holding sequences of the given lengths: float32
+    caches [num_pages, page_size, H_kv, d] of N(0,1) values and an int32 block
+    table [B, max_pages] whose pages are a seeded random permutation (plus
+    unused spare pages); unused table entries are -1."""
+    rng = np.random.default_rng(seed)
+    need = [-(-int(n) // page_size) for n in seq_lens]
+    max_pages = max(max(need), 1)
+    num_pages = sum(need) + spare_pages
+    perm = rng.permutation(num_pages).astype(np.int32)
+    table = np.full((len(seq_lens), max_pages), -1, dtype=np.int32)
+    at = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[at:at + n]
+        at += n
+    kc = rng.standard_normal((num_pages, page_size, H_kv, d), dtype=np.float32)
+    vc = rng.standard_normal((num_pages, page_size, H_kv, d), dtype=np.float32)
+    return kc, vc, table
