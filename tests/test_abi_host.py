@@ -172,7 +172,7 @@ def test_decode_is_declared_and_validates(lib):
 
     def call(**kw):
         a = dict(B=2, H=8, H_kv=2, n_q=1, d=128, num_pages=10, page_size=64, max_pages=5,
-                 max_seqlen=300, causal=1, scale=0.1, ws=ws)
+                 max_seqlen=1000, causal=1, scale=0.1, ws=ws)
         a.update(kw)
         return lib.attn_decode_paged(16, 16, 16, 16, 16, 16, 16, 256, a["ws"], a["B"], a["H"],
                                      a["H_kv"], a["n_q"], a["d"], a["num_pages"], a["page_size"],
