@@ -22,7 +22,8 @@ from .fp8 import (E4M3_MAX, e4m3_encode, e4m3_decode, sylvester_hadamard,
                   rotary_embed)
 from .varlen import (attention_forward_gqa, attention_backward_gqa,
                      attention_forward_varlen, attention_backward_varlen)
-from .decode import attention_decode_paged
+from .decode import (attention_decode_paged, attention_decode_paged_fp8,
+                     dequantize_paged_cache, quantize_paged_cache)
 
 __all__ = [
     "attention_forward", "attention_backward", "attention_probs", "attention_forward_rows",
@@ -31,4 +32,5 @@ __all__ = [
     "incoherent_transform", "quantize_e4m3_blocks", "dequantize_e4m3_blocks", "rotary_embed",
     "attention_forward_gqa", "attention_backward_gqa",
     "attention_forward_varlen", "attention_backward_varlen", "attention_decode_paged",
+    "attention_decode_paged_fp8", "quantize_paged_cache", "dequantize_paged_cache",
 ]
