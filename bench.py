@@ -453,6 +453,7 @@ def run_sweep(torch, attn, dev, stream, causal, steps=20, warmup=3):
     out.update(run_varlen_gqa(torch, attn, dev, stream, causal, steps, warmup))
     out.update(run_prepass_rope(torch, attn, dev, stream, steps, warmup))
     out.update(run_decode(torch, attn, dev, stream, steps, warmup))
+    out.update(run_decode_fp8(torch, attn, dev, stream, steps, warmup))
     assert attn.attn_get_device_status() == 0, attn.attn_last_error()
     return out
 
@@ -490,6 +491,47 @@ def run_decode(torch, attn, dev, stream, steps=20, warmup=3):
         ms = a.elapsed_time(b) / steps
         nbytes = 2 * Bq * L * hkv * d * 2 + 2 * Bq * h * n_q * d * 2
         out[f"decode_b{Bq}_len{L}_h{h}kv{hkv}_d{d}_nq{n_q}_page{ps}"] = {
+            "ms": round(ms, 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    return out
+
+
+def run_decode_fp8(torch, attn, dev, stream, steps=20, warmup=3):
+    """Paged decode over an e4m3 cache at the shape of run_decode: random codes
+    with a random descale per (page, head); n_q = 1 and 4, and n_q = 1 with the
+    key transform.  GB/s of algorithmic bytes: the cached codes read once, the
+    descales, Q and O."""
+    Bq, L, h, hkv, d, ps = 16, 8192, 32, 8, 128, 64
+    npg = Bq * L // ps
+    g = torch.Generator(device=dev).manual_seed(11)
+    kc, vc = (torch.randn((npg, ps, hkv, d), generator=g, device=dev).to(torch.float8_e4m3fn)
+              .view(torch.uint8) for _ in range(2))
+    kd, vd = (torch.rand((npg, hkv), generator=g, device=dev) * 0.02 + 0.01 for _ in range(2))
+    table = torch.randperm(npg, generator=g, device=dev).to(torch.int32).view(Bq, L // ps)
+    lens = torch.full((Bq,), L, dtype=torch.int32, device=dev)
+    signs = torch.where(torch.rand(d, generator=g, device=dev) < 0.5, -1.0, 1.0).float()
+    out = {}
+    for n_q, sg in ((1, None), (4, None), (1, signs)):
+        q = torch.randn((Bq, h, n_q, d), generator=g, device=dev).to(torch.bfloat16)
+        o = torch.empty_like(q)
+        lse = torch.empty((Bq, h, n_q), dtype=torch.float32, device=dev)
+        ws = torch.empty(attn.attn_decode_workspace_size(Bq, h, hkv, n_q, d, L), dtype=torch.uint8,
+                         device=dev)
+        fn = lambda: attn.attn_decode_paged_fp8(q, kc, vc, kd, vd, table, lens, L, causal=True,
+                                                hadamard_signs=sg, o=o, lse=lse, workspace=ws,
+                                                stream=stream)
+        for _ in range(warmup):
+            fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        nbytes = 2 * Bq * L * hkv * d + 2 * npg * hkv * 4 + 2 * Bq * h * n_q * d * 2
+        tag = "_hadamard" if sg is not None else ""
+        out[f"decode_fp8_b{Bq}_len{L}_h{h}kv{hkv}_d{d}_nq{n_q}_page{ps}{tag}"] = {
             "ms": round(ms, 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
     return out
 

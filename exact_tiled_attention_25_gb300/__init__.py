@@ -33,7 +33,8 @@ __all__ = ["AttnError", "attn_fwd", "attn_fwd_gqa", "attn_fwd_varlen", "attn_bwd
            "attn_bwd_gqa", "attn_bwd_varlen", "attn_bwd_varlen_workspace_size",
            "attn_bwd_workspace_size",
            "attn_fp8_quantize", "attn_fp8_quantize_rope", "attn_fwd_fp8",
-           "attn_decode_paged", "attn_decode_workspace_size", "attn_get_device_status",
+           "attn_decode_paged", "attn_decode_paged_fp8", "attn_decode_workspace_size",
+           "attn_get_device_status",
            "attn_status_string", "attn_last_error", "load_library"]
 
 
@@ -386,6 +387,59 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, max_seqlen: in
                                  num_pages, page_size, block_table.shape[1], int(max_seqlen),
                                  int(bool(causal)), scale, _DTYPES[q.dtype], _stream(stream))
     _check(code, "attn_decode_paged")
+    if host:
+        return o.cpu(), lse.cpu()
+    return o, lse
+
+
+def attn_decode_paged_fp8(q, k_cache, v_cache, k_descale, v_descale, block_table, seq_lens,
+                          max_seqlen: int, causal: bool = True, softmax_scale: float | None = None,
+                          hadamard_signs=None, o=None, lse=None, workspace=None, stream=None):
+    """Decode step against an e4m3 paged cache: q [B, H, n_q, 128] bf16/fp16,
+    caches uint8 [num_pages, page_size, H_kv, 128] with float32 descales
+    [num_pages, H_kv]; hadamard_signs (float32 [128]) when the keys were stored
+    transformed.  Returns O (q's dtype) and LSE float32 [B, H, n_q]."""
+    lib = _lib.load()
+    ins = [q, k_cache, v_cache, k_descale, v_descale, block_table, seq_lens]
+    if hadamard_signs is not None:
+        ins.append(hadamard_signs)
+    ins, host = _to_device(ins)
+    q, k_cache, v_cache, k_descale, v_descale, block_table, seq_lens = ins[:7]
+    signs = ins[7] if hadamard_signs is not None else None
+    B, H, n_q, d = _shape4(q, "q")
+    num_pages, page_size, Hkv, dk = _shape4(k_cache, "k_cache")
+    if tuple(v_cache.shape) != (num_pages, page_size, Hkv, dk) or not v_cache.is_contiguous():
+        raise ValueError("v_cache must match k_cache")
+    if dk != d or q.dtype not in _DTYPES:
+        raise ValueError("q must be bfloat16 or float16 with the caches' d")
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise ValueError("the caches hold uint8 e4m3 codes")
+    for t, n in ((k_descale, "k_descale"), (v_descale, "v_descale")):
+        if t.dtype != torch.float32 or tuple(t.shape) != (num_pages, Hkv) or not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous float32 [num_pages, H_kv]")
+    if signs is not None and (signs.dtype != torch.float32 or signs.numel() != d):
+        raise ValueError("hadamard_signs must be d float32 values")
+    for t, n, shp in ((block_table, "block_table", 2), (seq_lens, "seq_lens", 1)):
+        if t.dtype != torch.int32 or t.dim() != shp or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 tensor of rank {shp}")
+    if block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_table and seq_lens need one entry per sequence")
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, n_q), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(attn_decode_workspace_size(B, H, Hkv, n_q, d, int(max_seqlen)),
+                                dtype=torch.uint8, device=q.device)
+    code = lib.attn_decode_paged_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_descale),
+                                     _ptr(v_descale), _ptr(signs), _ptr(block_table),
+                                     _ptr(seq_lens), _ptr(o), _ptr(lse), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), B, H, Hkv, n_q,
+                                     d, num_pages, page_size, block_table.shape[1],
+                                     int(max_seqlen), int(bool(causal)), scale, _DTYPES[q.dtype],
+                                     _stream(stream))
+    _check(code, "attn_decode_paged_fp8")
     if host:
         return o.cpu(), lse.cpu()
     return o, lse

@@ -51,6 +51,10 @@ SIGNATURES = {
     "attn_decode_paged": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_void_p, c_size_t, c_int, c_int, c_int, c_int, c_int,
                                   c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p]),
+    "attn_decode_paged_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                      c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                      c_int, c_int, c_float, c_int, c_void_p]),
     "attn_fwd_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,
                              c_void_p]),

@@ -429,6 +429,57 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   return launch_decode(p, stream);
 }
 
+attn_status_t attn_decode_paged_fp8(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                    const float* k_descale, const float* v_descale,
+                                    const float* hadamard_signs, const int* block_table,
+                                    const int* seq_lens, void* o, float* lse, void* workspace,
+                                    size_t workspace_bytes, int B, int H, int H_kv, int n_q, int d,
+                                    int num_pages, int page_size, int max_pages, int max_seqlen,
+                                    int causal, float softmax_scale, attn_dtype_t dtype,
+                                    cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if (B < 1 || H < 1 || n_q < 1 || num_pages < 1 || max_pages < 1 || max_seqlen < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H, n_q, num_pages, max_pages and max_seqlen must be >= 1");
+  if ((s = check_heads(H, H_kv)) != ATTN_OK) return s;
+  if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 decode supports d = 128");
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if ((H / H_kv) * n_q > 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "(H / H_kv) * n_q must be <= 128 (one query tile)");
+  if (page_size < 16 || page_size > 65536 || (page_size & (page_size - 1)) != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "page_size must be a power of two in [16, 65536] for an FP8 cache");
+  if (static_cast<long long>(max_pages) * page_size > 2147483647LL ||
+      static_cast<double>(num_pages) * page_size * H_kv * d >= 9.0e15)
+    return fail(ATTN_ERR_INVALID_ARG, "cache too large");
+  if (static_cast<double>(B) * H * n_q * d >= 2147483648.0)
+    return fail(ATTN_ERR_INVALID_ARG, "B*H*n_q*d must be < 2^31");
+  if ((s = check_ptrs({q, k_cache, v_cache, o, lse, workspace, k_descale, v_descale})) != ATTN_OK)
+    return s;
+  if (hadamard_signs && (reinterpret_cast<uintptr_t>(hadamard_signs) & 15u))
+    return fail(ATTN_ERR_INVALID_ARG, "hadamard_signs must be 16-byte aligned");
+  if (!block_table || !seq_lens || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "block_table and seq_lens must be non-null, 4-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (workspace_bytes < attn_decode_workspace_size(B, H, H_kv, n_q, d, max_seqlen))
+    return fail(ATTN_ERR_INVALID_ARG, "workspace smaller than attn_decode_workspace_size()");
+  if ((s = check_scale(softmax_scale)) != ATTN_OK) return s;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_BF16 or ATTN_FP16");
+  if ((s = check_device()) != ATTN_OK) return s;
+  const DecodeSplits sp = decode_splits(B, H_kv, max_seqlen);
+  const size_t rows = static_cast<size_t>(B) * H * n_q * sp.splits;
+  char* ws = static_cast<char*>(workspace);
+  DecodeParams p{q, k_cache, v_cache, block_table, seq_lens, o, lse,
+                 reinterpret_cast<float*>(ws),
+                 reinterpret_cast<float*>(ws + align_up(rows * d * sizeof(float), 256)),
+                 B, H, H_kv, n_q, d, num_pages, page_size, max_pages, max_seqlen, causal,
+                 softmax_scale, dtype == ATTN_FP16 ? 1 : 0,
+                 1, k_descale, v_descale, hadamard_signs};
+  return launch_decode(p, stream);
+}
+
 attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
                            const float* q_descale, const float* k_descale,
                            const float* v_descale, void* o, float* lse, int B, int H, int N,

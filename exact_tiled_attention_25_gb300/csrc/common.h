@@ -151,6 +151,12 @@ struct DecodeParams {
   int causal;
   float scale;
   int fp16;
+  // e4m3 cache (d = 128): codes in k_cache / v_cache, one float32 descale per
+  // (physical page, key/value head), optional key-transform signs
+  int fp8 = 0;
+  const float* k_descale = nullptr;   // [num_pages, H_kv]
+  const float* v_descale = nullptr;
+  const float* signs = nullptr;       // [d] of +-1, or nullptr
 };
 
 // Key-range splits of a decode call, each a whole number of 128-key tiles.

@@ -1,4 +1,5 @@
-// BF16/FP16 decode attention over a paged key/value cache on sm_103a.
+// Decode attention over a paged key/value cache on sm_103a: BF16/FP16 caches,
+// and e4m3 caches with per-page block scaling.
 //
 // Method: "FlashAttention-3: Hopper Asynchrony and FP8 Attention", section
 // "Where It Breaks", leaves a decode-focused inference kernel as open work;
@@ -27,6 +28,9 @@
 //    computed while the softmax of tile j runs.
 //  * Causal masking is bottom-right aligned: query token t of n_q sits at
 //    position len - n_q + t and sees keys 0 .. len - n_q + t.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include <cmath>
 
 #include "common.h"
@@ -67,6 +71,11 @@ struct DecKParams {
   int splits, tiles_per_split;
   int causal;
   float scale_log2;
+  // e4m3 cache only
+  const float* k_descale;   // [num_pages, H_kv]
+  const float* v_descale;
+  const float* signs;       // d values +-1 of the key transform, or nullptr
+  int H_kv, page_shift;
 };
 
 __device__ __forceinline__ float lg2_dec(float x) {
@@ -428,6 +437,481 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) lse[row] = total;
 }
 
+// ================================================================ e4m3 cache ====
+// The same schedule over a cache of e4m3 codes with one float32 descale per
+// (physical page, key/value head), d = 128.  Both products run as kind::f8f6f4:
+//  * the query tile arrives in 16-bit; each softmax thread quantises its row
+//    to e4m3 in shared memory (optionally after the transform x -> x M, M =
+//    diag(signs) H_d / sqrt(d), which the keys were stored with), with one
+//    descale dq = amax / 448 per row, by the block quantiser's rule;
+//  * a 128-key tile may span several pages (page_size >= 16), so descales are
+//    kept per 16-key group: the score coefficient of group g is
+//    scale * log2(e) * dq * dk_g, and the value descale enters the exponent:
+//    the running maximum is taken over y = s + log2(dv_g), so P' = 2^(y - m)
+//    <= 1 multiplies the raw value codes and the row sum adds P' / dv_g.
+//    No value-descale pre-scan or extra O rescale is needed.
+//  * lanes 0..15 of every softmax warp fetch the descales of a tile two tiles
+//    ahead (block table one tile earlier still) and share them by shuffles.
+struct Dec8Cfg {
+  static constexpr int D = 128;
+  static constexpr int CHUNK16 = DBM * 128;          // 64 columns of the 16-bit query tile
+  static constexpr int Q16 = 2 * CHUNK16;            // 16-bit query tile
+  static constexpr int TILE8 = DBM * D;              // e4m3 query, key or value tile
+  static constexpr int NSLOT_FIT = (kSmemLimit - 2048 - Q16 - TILE8) / TILE8;
+  static constexpr int NSLOT = NSLOT_FIT > 12 ? 12 : NSLOT_FIT;
+  static constexpr int SMEM = 1024 + Q16 + TILE8 + NSLOT * TILE8;
+  static constexpr int THREADS = 6 * 32;
+  static constexpr int LOAD_WARP = 4;
+  static constexpr int MMA_WARP = 5;
+  __host__ __device__ static constexpr uint32_t S_COL(int buf) { return 128u * buf; }
+  static constexpr uint32_t O_COL = 256;
+  static_assert(NSLOT >= 6, "ring too short");
+};
+
+template <bool FP16>
+__global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
+    decode_fp8_split_kernel(const __grid_constant__ CUtensorMap tmQ,
+                            const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmV, const DecKParams kp) {
+  using C = Dec8Cfg;
+  constexpr int D = C::D;
+  constexpr int NSLOT = C::NSLOT;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;                  // 16-bit query tile, two 64-column chunks
+  uint8_t* sQ8 = smem + C::Q16;        // e4m3 query tile
+  uint8_t* sKV = sQ8 + C::TILE8;
+
+  __shared__ __align__(8) uint64_t q_full;
+  __shared__ __align__(8) uint64_t q8_full;
+  __shared__ __align__(8) uint64_t kv_full[NSLOT];
+  __shared__ __align__(8) uint64_t kv_empty[NSLOT];
+  __shared__ __align__(8) uint64_t s_full[2];
+  __shared__ __align__(8) uint64_t p_full[2];
+  __shared__ __align__(8) uint64_t pv_done;
+  __shared__ __align__(8) uint64_t o_full;
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ int load_items_sh;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int split = blockIdx.x;
+  const int hk = blockIdx.y;
+  const int b = blockIdx.z;
+  const int len = kp.seq_lens[b];
+  if (len < 0 || len > kp.max_pages * kp.page_size) {
+    if (threadIdx.x == 0) atomicCAS(kp.status, 0, kDevBadSeqlens);
+    return;
+  }
+  const int ntiles = (len + DBN - 1) / DBN;
+  const int j0 = split * kp.tiles_per_split;
+  const int nK = max(0, min(ntiles, j0 + kp.tiles_per_split) - j0);
+  const int r = warp * 32 + lane;
+  const int gq = r / kp.n_q, tq = r - gq * kp.n_q;
+  const size_t prow = (static_cast<size_t>(b) * kp.H + hk * kp.group + gq) * kp.n_q + tq;
+  if (nK == 0) {
+    if (warp < 4 && r < kp.rows_real) kp.lse_part[prow * kp.splits + split] = -INFINITY;
+    return;
+  }
+  const int total_items = 2 * nK;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&q_full, 1);
+    mbar_init(&q8_full, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+    }
+    mbar_init(&pv_done, 1);
+    mbar_init(&o_full, 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    load_items_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+  const Abort ab{&abort_sh, kp.status};
+  const int* table = kp.block_table + static_cast<size_t>(b) * kp.max_pages;
+
+  if (warp == C::LOAD_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(&q_full, C::Q16);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        tma_load_3d(sQ + c * C::CHUNK16, &tmQ, &q_full, c * 64, hk * kp.group * kp.n_q, b);
+      const int nbox = DBN / kp.box_rows;
+      int it = 0;
+      bool ok = true;
+      for (int j = 0; j < nK && ok; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int slot = it % NSLOT;
+          const int use = it / NSLOT;
+          if (use >= 1 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, ab, kDevTimeoutLoad)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&kv_full[slot], C::TILE8);
+          uint8_t* dst = sKV + slot * C::TILE8;
+          for (int x = 0; x < nbox; ++x) {
+            const int tok = (j0 + j) * DBN + x * kp.box_rows;
+            const int page = tok >> kp.page_shift;
+            int phys = kp.num_pages;               // out of range: zero-filled box
+            if (tok < len && page < kp.max_pages) {
+              const int pg = table[page];
+              if (pg >= 0 && pg < kp.num_pages) phys = pg;
+              else atomicCAS(kp.status, 0, kDevBadSeqlens);
+            }
+            tma_load_4d(dst + x * kp.box_rows * 128, kv ? &tmV : &tmK, &kv_full[slot], 0,
+                        tok & (kp.page_size - 1), hk, phys);
+          }
+          ++it;
+        }
+      }
+      load_items_sh = it;
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_e4m3(128, DBN, false, false);
+      constexpr uint32_t idPV = idesc_e4m3(128, D, false, true);
+      const uint64_t qdesc = sdesc_sw128(smem_u32(sQ8), 16, 1024);            // K-major Q
+      const uint64_t kdesc0 = sdesc_sw128(smem_u32(sKV), 16, 1024);           // K-major K
+      const uint64_t vdesc0 = sdesc_sw128(smem_u32(sKV), C::TILE8, 1024);     // MN-major V
+      bool ok = mbar_wait(&q8_full, 0, ab, kDevTimeoutMma);
+      auto issue_s = [&](int jj) -> bool {
+        const int item = 2 * jj;
+        const int slot = item % NSLOT;
+        if (!mbar_wait(&kv_full[slot], (item / NSLOT) & 1, ab, kDevTimeoutMma)) return false;
+        const uint64_t kdesc = opaque(sdesc_add(kdesc0, slot * C::TILE8));
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk)
+          mma_f8_ss(tmem + C::S_COL(jj & 1), sdesc_add(qdesc, kk * 32), sdesc_add(kdesc, kk * 32),
+                    idS, kk > 0 ? 1u : 0u);
+        mma_commit(&s_full[jj & 1]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && nK > 1) ok = issue_s(1);
+      for (int j = 0; j < nK && ok; ++j) {
+        // O += P'(j) V_j, P' packed e4m3 in columns [0, 32) of buffer j % 2
+        const int item = 2 * j + 1;
+        const int slot = item % NSLOT;
+        if (!(ok = mbar_wait(&kv_full[slot], (item / NSLOT) & 1, ab, kDevTimeoutMma))) break;
+        const uint64_t vdesc = opaque(sdesc_add(vdesc0, slot * C::TILE8));
+        if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1, ab, kDevTimeoutMma))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < DBN / 32; ++kk)
+          mma_f8_ts(tmem + C::O_COL, tmem + C::S_COL(j & 1) + 8 * kk,
+                    sdesc_add(vdesc, kk * 32 * 128), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&pv_done);
+        if (j == nK - 1) mma_commit(&o_full);
+        if (j + 2 < nK) ok = issue_s(j + 2);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    bool ok = true;
+    float c_q = 0.f;   // scale * log2(e) * dq of this row
+    // ---- quantise this thread's query row
+    if (__any_sync(0xffffffffu, !mbar_wait(&q_full, 0, ab, kDevTimeoutSoftmax))) {
+      ok = false;
+    } else {
+      float x[D];
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 w = *reinterpret_cast<const uint4*>(sQ + c * C::CHUNK16 + r * 128 +
+                                                          ((u ^ (r & 7)) << 4));
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float2 f;
+            if (FP16) f = __half22float2(*reinterpret_cast<const __half2*>(&ws[e]));
+            else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
+            x[c * 64 + u * 8 + 2 * e] = f.x;
+            x[c * 64 + u * 8 + 2 * e + 1] = f.y;
+          }
+        }
+      if (kp.signs) {
+        // x -> (x o signs) H_d / sqrt(d), fast Walsh-Hadamard butterflies
+#pragma unroll
+        for (int i = 0; i < D; i += 4) {
+          const float4 sg = __ldg(reinterpret_cast<const float4*>(kp.signs + i));
+          x[i] *= sg.x;
+          x[i + 1] *= sg.y;
+          x[i + 2] *= sg.z;
+          x[i + 3] *= sg.w;
+        }
+#pragma unroll
+        for (int h = 1; h < D; h <<= 1)
+#pragma unroll
+          for (int i = 0; i < D; ++i)
+            if ((i & h) == 0) {
+              const float a = x[i], bb = x[i + h];
+              x[i] = a + bb;
+              x[i + h] = a - bb;
+            }
+#pragma unroll
+        for (int i = 0; i < D; ++i) x[i] *= 0.08838834764831845f;   // 1 / sqrt(128)
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < D; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      // descale = amax / 448 and code = e4m3(x / descale), both IEEE float32
+      // divisions: the rule of the block quantiser (once per CTA)
+      const float dq = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+      c_q = kp.scale_log2 * dq;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        uint32_t wq[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = u * 16 + e * 4;
+          wq[e] = cvt_pack_e4m3x4(__fdiv_rn(x[i], dq), __fdiv_rn(x[i + 1], dq), __fdiv_rn(x[i + 2], dq),
+                                  __fdiv_rn(x[i + 3], dq));
+        }
+        st_shared_v4(smem_u32(sQ8 + r * 128 + ((u ^ (r & 7)) << 4)), wq[0], wq[1], wq[2], wq[3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&q8_full);
+    }
+    // ---- descales of the 16-key groups, fetched ahead by lanes 0..15
+    const float* dsrc = (lane & 8) ? kp.v_descale : kp.k_descale;
+    auto page_of = [&](int jj) -> int {
+      const int tok = (j0 + jj) * DBN + 16 * (lane & 7);
+      if (lane >= 16 || jj >= nK || tok >= len) return -1;
+      const int ph = __ldg(table + (tok >> kp.page_shift));
+      return (ph >= 0 && ph < kp.num_pages) ? ph : -1;
+    };
+    auto desc_of = [&](int ph) -> float {
+      return ph < 0 ? 1.f : __ldg(dsrc + static_cast<size_t>(ph) * kp.H_kv + hk);
+    };
+    float dcur = desc_of(page_of(0));
+    float dnext = desc_of(page_of(1));
+    int ph2 = page_of(2);
+
+    const int vis_end = kp.causal ? min(len, len - kp.n_q + tq + 1) : len;
+    float m_ref = -INFINITY;   // log2 units of y = s + log2(dv)
+    float l = 0.f;             // sum of 2^(s - m_ref)
+    for (int j = 0; j < nK && ok; ++j) {
+      // group coefficients: lanes g < 8 hold dk_g, lanes 8 + g hold dv_g
+      const float lgd = lg2_dec(dcur);
+      const float invd = 1.f / dcur;
+      float coef[8], lgv[8], ivv[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        coef[g] = c_q * __shfl_sync(0xffffffffu, dcur, g);
+        lgv[g] = __shfl_sync(0xffffffffu, lgd, 8 + g);
+        ivv[g] = __shfl_sync(0xffffffffu, invd, 8 + g);
+      }
+      if (__any_sync(0xffffffffu, !mbar_wait(&s_full[j & 1], (j >> 1) & 1, ab, kDevTimeoutSoftmax))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      if (r == 0) {
+        if (2 * j + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j) % NSLOT]);
+        if (j >= 2 && 2 * j - 3 + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j - 3) % NSLOT]);
+      }
+      const uint32_t tS = tmem + lane_addr + C::S_COL(j & 1);
+      uint32_t sr[DBN];
+#pragma unroll
+      for (int c0 = 0; c0 < DBN / 32; ++c0)
+        tmem_ld32(tS + c0 * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0 * 32]));
+      tmem_ld_wait();
+      const int kbase = (j0 + j) * DBN;
+      if (kbase + DBN > vis_end) {
+        const int lim = vis_end - kbase;
+#pragma unroll
+        for (int c = 0; c < DBN; ++c)
+          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+      }
+      // max over y: per 16-key group, raw max x coefficient + log2(dv)
+      float mt = -INFINITY;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const int c = 16 * g;
+        const float m16 = fmaxf(
+            fmax3(fmax3(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), __uint_as_float(sr[c + 2])),
+                  fmax3(__uint_as_float(sr[c + 3]), __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5])),
+                  fmax3(__uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]), __uint_as_float(sr[c + 8]))),
+            fmax3(fmax3(__uint_as_float(sr[c + 9]), __uint_as_float(sr[c + 10]), __uint_as_float(sr[c + 11])),
+                  fmax3(__uint_as_float(sr[c + 12]), __uint_as_float(sr[c + 13]), __uint_as_float(sr[c + 14])),
+                  __uint_as_float(sr[c + 15])));
+        mt = fmaxf(mt, fmaf(m16, coef[g], lgv[g]));
+      }
+      // The reference follows the running maximum exactly (no lazy slack):
+      // the largest weight is then exactly 1, which e4m3 holds exactly, and in
+      // a peaked row that weight carries most of the sum.  A lagging reference
+      // (weights up to 2^8) rounds it too and about doubles the P rounding
+      // error; the running maximum of a decode row rises on few tiles, so the
+      // extra O rescales cost little.
+      const float m_new = fmaxf(m_ref, mt);
+      const bool need = m_new > m_ref;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2_approx(m_ref - m_new);
+        l *= alpha;
+        m_ref = m_new;
+      }
+      const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+#pragma unroll
+      for (int c0 = 0; c0 < DBN / 32; ++c0) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int hg = 0; hg < 2; ++hg) {
+          const int g = 2 * c0 + hg;
+          const uint64_t cc = pack2(coef[g], coef[g]);
+          const float off = neg + lgv[g];
+          const uint64_t nn = pack2(off, off);
+          uint64_t acc = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = 16 * g + 4 * i;
+            const uint64_t y0 = ffma2(pack2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), cc, nn);
+            const uint64_t y1 = ffma2(pack2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), cc, nn);
+            const float p0 = ex2_approx(lo2(y0));
+            const float p1 = ex2_approx(hi2(y0));
+            const float p2 = ex2_approx(lo2(y1));
+            const float p3 = ex2_approx(hi2(y1));
+            acc = fadd2(acc, fadd2(pack2(p0, p1), pack2(p2, p3)));
+            pk[4 * hg + i] = cvt_pack_e4m3x4(p0, p1, p2, p3);
+          }
+          l = fmaf(lo2(acc) + hi2(acc), ivv[g], l);
+        }
+        // P' of keys [32 c0, +32) -> columns [8 c0, +8)
+        tmem_st_x8(tS + c0 * 8, pk);
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        if (__any_sync(0xffffffffu, !mbar_wait(&pv_done, (j - 1) & 1, ab, kDevTimeoutSoftmax))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll 1
+        for (int c0 = 0; c0 < D / 32; ++c0) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_addr + C::O_COL + c0 * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tmem + lane_addr + C::O_COL + c0 * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&p_full[j & 1]);
+      // advance the descale pipeline
+      dcur = dnext;
+      dnext = desc_of(ph2);
+      ph2 = page_of(j + 3);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && !__any_sync(0xffffffffu, !mbar_wait(&o_full, 0, ab, kDevTimeoutEpilogue))) {
+      tc_fence_after_sync();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      float* dst = kp.o_part + (prow * kp.splits + split) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 32; ++c0) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_addr + C::O_COL + c0 * 32, o);
+        tmem_ld_wait();
+        if (r < kp.rows_real) {
+          float4* d4 = reinterpret_cast<float4*>(dst + c0 * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            d4[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+        }
+      }
+      if (r < kp.rows_real)
+        kp.lse_part[prow * kp.splits + split] =
+            l > 0.f ? (m_ref + lg2_dec(l)) * 0.69314718055994530942f : -INFINITY;
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (abort_sh) {
+    if (warp == C::LOAD_WARP && lane == 0) {
+      mbar_wait_drain(&q_full, 0);
+      const int issued = load_items_sh;
+      for (int s = 0; s < NSLOT && s < issued; ++s)
+        mbar_wait_drain(&kv_full[s], ((issued - 1 - s) / NSLOT) & 1);
+    }
+    if (warp == C::MMA_WARP && lane == 0) {
+      mma_commit(&drain_bar);
+      mbar_wait_drain(&drain_bar, 0);
+    }
+    __syncthreads();
+  }
+  if (warp == C::MMA_WARP) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <bool FP16>
+attn_status_t launch_decode_fp8_t(const DecodeParams& p, cudaStream_t stream) {
+  using C = Dec8Cfg;
+  auto kern = decode_fp8_split_kernel<FP16>;
+  attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), C::SMEM);
+  if (s != ATTN_OK) return s;
+  CUtensorMap tq, tk, tv;
+  if ((s = make_tmap_3d(&tq, p.q, 2, C::D, static_cast<uint64_t>(p.H) * p.n_q, p.B, 64, DBM)) != ATTN_OK)
+    return s;
+  // e4m3 cache: {d, page_size, H_kv, num_pages}, one 128-byte row per token
+  const int box_rows = p.page_size < DBN ? p.page_size : DBN;
+  const uint64_t tok_b = static_cast<uint64_t>(p.H_kv) * C::D, head_b = C::D, page_b = tok_b * p.page_size;
+  if ((s = make_tmap_4d(&tk, p.k_cache, 1, C::D, p.page_size, p.H_kv, p.num_pages, tok_b, head_b, page_b,
+                        C::D, box_rows)) != ATTN_OK)
+    return s;
+  if ((s = make_tmap_4d(&tv, p.v_cache, 1, C::D, p.page_size, p.H_kv, p.num_pages, tok_b, head_b, page_b,
+                        C::D, box_rows)) != ATTN_OK)
+    return s;
+  int* status = device_status_word();
+  if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
+  const DecodeSplits sp = decode_splits(p.B, p.H_kv, p.max_seqlen);
+  int shift = 0;
+  while ((1 << shift) < p.page_size) ++shift;
+  DecKParams kp{p.block_table, p.seq_lens, p.o_part,  p.lse_part,  status,
+                p.H,           p.H / p.H_kv, p.n_q,   (p.H / p.H_kv) * p.n_q,
+                p.max_pages,   p.page_size, box_rows, p.num_pages,
+                sp.splits,     sp.tiles_per_split, p.causal, p.scale * 1.4426950408889634f,
+                p.k_descale,   p.v_descale, p.signs, p.H_kv, shift};
+  kern<<<dim3(sp.splits, p.H_kv, p.B), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, kp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "FP8 decode split kernel launch");
+  const long long rows = static_cast<long long>(p.B) * p.H * p.n_q;
+  decode_combine_kernel<128, FP16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
+      p.o_part, p.lse_part, static_cast<uint16_t*>(p.o), p.lse, rows, sp.splits);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "decode combine kernel launch");
+  return ATTN_OK;
+}
+
 template <int D, bool FP16>
 attn_status_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   using C = DecCfg<D>;
@@ -470,6 +954,10 @@ attn_status_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
 
 attn_status_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   if (p.B > 65535 || p.H_kv > 65535) return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
+  if (p.fp8) {
+    if (p.d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 decode supports d = 128");
+    return p.fp16 ? launch_decode_fp8_t<true>(p, stream) : launch_decode_fp8_t<false>(p, stream);
+  }
   switch (p.d) {
     case 64: return p.fp16 ? launch_decode_t<64, true>(p, stream) : launch_decode_t<64, false>(p, stream);
     case 128: return p.fp16 ? launch_decode_t<128, true>(p, stream) : launch_decode_t<128, false>(p, stream);

@@ -255,6 +255,43 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
                                 attn_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * attn_decode_paged_fp8 -- attn_decode_paged over a cache of e4m3 codes with
+ * block scaling: one descale per (physical page, key/value head).
+ *   q              : [B, H, n_q, d] in `dtype` (bf16 or fp16); the kernel
+ *                    quantises each query row to e4m3 with its own descale
+ *                    (row amax / 448), after multiplying it by M when
+ *                    hadamard_signs is given.
+ *   k_cache,
+ *   v_cache        : uint8 e4m3 (OCP E4M3, "fn") codes [num_pages, page_size,
+ *                    H_kv, d].  Value = code x descale of the block.
+ *   k_descale,
+ *   v_descale      : DEVICE float32 [num_pages, H_kv], positive and finite.
+ *   hadamard_signs : DEVICE float32 [d] of +1 / -1, or NULL.  Give it when the
+ *                    keys were stored transformed, K M with M = diag(signs)
+ *                    H_d / sqrt(d) (H_d the Sylvester Hadamard matrix): the query
+ *                    is transformed by the same M, and (q M)(K M)^T = q K^T.
+ *                    Values are never transformed.
+ *   Other arguments, outputs, workspace (attn_decode_workspace_size), masking
+ *   and device-side error reporting as attn_decode_paged.  O is in `dtype`.
+ * Limits: d = 128; (H / H_kv) * n_q <= 128; page_size a power of two in
+ * [16, 65536].  Both products run on e4m3 operands (P rounded to e4m3, as in
+ * attn_fwd_fp8); accuracy is that of the FP8 forward.
+ * Source: the FP8 path of "FlashAttention-3: Hopper Asynchrony and FP8
+ * Attention" ("FP8 accuracy controls": block quantisation, incoherent
+ * processing) applied to the decode step that its section "Where It Breaks"
+ * leaves open (persistent FP8 inference), over the paged cache of "FlashAttention
+ * 3 Hardware Acceleration: ...", section "Memory Fragmentation".
+ */
+attn_status_t attn_decode_paged_fp8(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                    const float* k_descale, const float* v_descale,
+                                    const float* hadamard_signs, const int* block_table,
+                                    const int* seq_lens, void* o, float* lse, void* workspace,
+                                    size_t workspace_bytes, int B, int H, int H_kv, int n_q, int d,
+                                    int num_pages, int page_size, int max_pages, int max_seqlen,
+                                    int causal, float softmax_scale, attn_dtype_t dtype,
+                                    cudaStream_t stream);
+
+/*
  * attn_fp8_quantize -- FP8 e4m3 pre-pass with block scaling and incoherent
  * processing ("FlashAttention-3: Hopper Asynchrony and FP8 Attention", section
  * "FP8 accuracy controls").

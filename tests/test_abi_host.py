@@ -183,3 +183,24 @@ def test_decode_is_declared_and_validates(lib):
                           (dict(causal=2), 1, "causal")):
         assert call(**kw) == code, kw
         assert why.lower() in lib.attn_last_error().decode().lower(), (kw, lib.attn_last_error())
+
+
+def test_fp8_decode_is_declared_and_validates(lib):
+    assert "attn_decode_paged_fp8" in declared_functions()
+    ws = lib.attn_decode_workspace_size(2, 8, 2, 1, 128, 1000)
+
+    def call(signs=None, **kw):
+        a = dict(B=2, H=8, H_kv=2, n_q=1, d=128, num_pages=10, page_size=64, max_pages=5,
+                 max_seqlen=1000, causal=1, scale=0.1, ws=ws, kd=16, vd=16)
+        a.update(kw)
+        return lib.attn_decode_paged_fp8(16, 16, 16, a["kd"], a["vd"], signs, 16, 16, 16, 16, 256,
+                                         a["ws"], a["B"], a["H"], a["H_kv"], a["n_q"], a["d"],
+                                         a["num_pages"], a["page_size"], a["max_pages"],
+                                         a["max_seqlen"], a["causal"], a["scale"], 0, None)
+    for kw, code, why in ((dict(page_size=8), 1, "page_size"), (dict(page_size=96), 1, "page_size"),
+                          (dict(d=64), 2, "d = 128"), (dict(H_kv=3), 1, "H_kv"),
+                          (dict(H=64, H_kv=1, n_q=4), 2, "128"), (dict(ws=ws - 1), 1, "workspace"),
+                          (dict(kd=0), 1, "null"), (dict(vd=8), 1, "aligned"),
+                          (dict(signs=8), 1, "hadamard_signs"), (dict(scale=0.0), 1, "softmax_scale")):
+        assert call(**kw) == code, kw
+        assert why.lower() in lib.attn_last_error().decode().lower(), (kw, lib.attn_last_error())
