@@ -460,10 +460,11 @@ def run_sweep(torch, attn, dev, stream, causal, steps=20, warmup=3):
 
 def run_decode(torch, attn, dev, stream, steps=20, warmup=3):
     """Paged decode: 16 sequences of 8192 cached tokens, H = 32 query heads
-    sharing H_kv = 8 key/value heads, d = 128, pages of 64 tokens in a shuffled
-    order, n_q = 1 and 4 new tokens (causal).  GB/s of algorithmic bytes: the
-    cached keys and values read once, plus Q and O."""
-    Bq, L, h, hkv, d, ps = 16, 8192, 32, 8, 128, 64
+    sharing H_kv = 8 key/value heads, d = 128, pages of 256 tokens (the block
+    size of the paged cache the sources describe) in a shuffled order, n_q = 1
+    and 4 new tokens (causal).  GB/s of algorithmic bytes: the cached keys and
+    values read once, plus Q and O."""
+    Bq, L, h, hkv, d, ps = 16, 8192, 32, 8, 128, 256
     npg = Bq * L // ps
     g = torch.Generator(device=dev).manual_seed(10)
     kc, vc = (torch.randn((npg, ps, hkv, d), generator=g, device=dev).to(torch.bfloat16)
@@ -500,7 +501,7 @@ def run_decode_fp8(torch, attn, dev, stream, steps=20, warmup=3):
     with a random descale per (page, head); n_q = 1 and 4, and n_q = 1 with the
     key transform.  GB/s of algorithmic bytes: the cached codes read once, the
     descales, Q and O."""
-    Bq, L, h, hkv, d, ps = 16, 8192, 32, 8, 128, 64
+    Bq, L, h, hkv, d, ps = 16, 8192, 32, 8, 128, 256
     npg = Bq * L // ps
     g = torch.Generator(device=dev).manual_seed(11)
     kc, vc = (torch.randn((npg, ps, hkv, d), generator=g, device=dev).to(torch.float8_e4m3fn)

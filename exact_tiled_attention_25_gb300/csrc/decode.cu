@@ -84,6 +84,88 @@ __device__ __forceinline__ float lg2_dec(float x) {
   return y;
 }
 
+// Producer of one split.  The whole warp runs the loop.  The physical pages
+// of the split's boxes (one box = min(page_size, 128) rows of one page) are
+// read from the block table in windows of 32 boxes, one box per lane, and the
+// next window is read while the current one is in use: no table read waits in
+// front of a copy.  When a window comes into use its entries are checked and,
+// for an e4m3 cache, the descales of its pages are prefetched into L2 for the
+// softmax warps.  Lane 0 waits for free ring slots and issues the copies; the
+// keys and values of a tile use the same pages.  Item i (K_j = 2j, V_j = 2j + 1)
+// goes to ring slot (i + SHIFT) % NSLOT: the first SHIFT slots may start out
+// holding other data, released through their empty barrier like a used slot.
+template <int NSLOT, int CH, int CHUNK, int TILE, int SHIFT>
+__device__ __forceinline__ void decode_produce(const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                               uint8_t* sKV, uint64_t* kv_full, uint64_t* kv_empty,
+                                               const DecKParams& kp, const int* table, int j0,
+                                               int nK, int len, int hk, int lane, const Abort& ab,
+                                               int* load_items_sh) {
+  const int nbox = DBN / kp.box_rows;       // divides 32, so windows start at tile starts
+  const int nboxes = nK * nbox;
+  // box 32 w + lane lies in the split and the sequence
+  auto in_seq = [&](int w) -> bool {
+    const int bx = w * 32 + lane;
+    return bx < nboxes && (j0 * nbox + bx) * kp.box_rows < len;
+  };
+  // raw table entry of box 32 w + lane (checked when its window comes into use)
+  auto load_window = [&](int w) -> int {
+    if (!in_seq(w)) return kp.num_pages;
+    return __ldg(table + (((j0 * nbox + w * 32 + lane) * kp.box_rows) >> kp.page_shift));
+  };
+  // physical page of box 32 w + lane: num_pages (a zero-filled box) past the
+  // sequence, or for an entry outside the cache (reported)
+  auto take = [&](int pg, int w) -> int {
+    if (!in_seq(w)) return kp.num_pages;
+    if (pg < 0 || pg >= kp.num_pages) {
+      atomicCAS(kp.status, 0, kDevBadSeqlens);
+      return kp.num_pages;
+    }
+    if (kp.k_descale) {
+      const size_t at = static_cast<size_t>(pg) * kp.H_kv + hk;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(kp.k_descale + at));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(kp.v_descale + at));
+    }
+    return pg;
+  };
+  int win = take(load_window(0), 0);
+  int win_next = load_window(1);
+  int it = 0;
+  bool ok = true;
+  for (int j = 0; j < nK && ok; ++j) {
+    const int wcur = (j * nbox) / 32;
+    if (j > 0 && ((j * nbox) & 31) == 0) {
+      win = take(win_next, wcur);
+      win_next = load_window(wcur + 1);
+    }
+    for (int kv = 0; kv < 2; ++kv) {
+      const int slot = (it + SHIFT) % NSLOT;
+      const int use = (it + SHIFT) / NSLOT;
+      int go = 1;
+      if (lane == 0) {
+        if (use >= 1 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, ab, kDevTimeoutLoad)) go = 0;
+        else mbar_arrive_expect_tx(&kv_full[slot], TILE);
+      }
+      if (!__shfl_sync(0xffffffffu, go, 0)) {
+        ok = false;
+        break;
+      }
+      uint8_t* dst = sKV + slot * TILE;
+      for (int x = 0; x < nbox; ++x) {
+        const int phys = __shfl_sync(0xffffffffu, win, (j * nbox + x) & 31);
+        if (lane == 0) {
+          const int tok = (j0 + j) * DBN + x * kp.box_rows;
+#pragma unroll
+          for (int c = 0; c < CH; ++c)
+            tma_load_4d(dst + c * CHUNK + x * kp.box_rows * 128, kv ? tmV : tmK, &kv_full[slot],
+                        c * 64, tok & (kp.page_size - 1), hk, phys);
+        }
+      }
+      ++it;
+    }
+  }
+  if (lane == 0) *load_items_sh = it;
+}
+
 template <int D, bool FP16>
 __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -169,39 +251,10 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < C::CH; ++c)
         tma_load_3d(sQ + c * C::CHUNK, &tmQ, &q_full, c * 64, hk * kp.group * kp.n_q, b);
-      const int* table = kp.block_table + static_cast<size_t>(b) * kp.max_pages;
-      const int nbox = DBN / kp.box_rows;
-      int it = 0;
-      bool ok = true;
-      for (int j = 0; j < nK && ok; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int slot = it % NSLOT;
-          const int use = it / NSLOT;
-          if (use >= 1 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, ab, kDevTimeoutLoad)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&kv_full[slot], C::TILE);
-          uint8_t* dst = sKV + slot * C::TILE;
-          for (int x = 0; x < nbox; ++x) {
-            const int tok = (j0 + j) * DBN + x * kp.box_rows;
-            const int page = tok / kp.page_size;
-            int phys = kp.num_pages;               // out of range: zero-filled box
-            if (tok < len && page < kp.max_pages) {
-              const int pg = table[page];
-              if (pg >= 0 && pg < kp.num_pages) phys = pg;
-              else atomicCAS(kp.status, 0, kDevBadSeqlens);
-            }
-#pragma unroll
-            for (int c = 0; c < C::CH; ++c)
-              tma_load_4d(dst + c * C::CHUNK + x * kp.box_rows * 128, kv ? &tmV : &tmK,
-                          &kv_full[slot], c * 64, tok % kp.page_size, hk, phys);
-          }
-          ++it;
-        }
-      }
-      load_items_sh = it;
     }
+    decode_produce<NSLOT, C::CH, C::CHUNK, C::TILE, 0>(
+        &tmK, &tmV, sKV, kv_full, kv_empty, kp, kp.block_table + static_cast<size_t>(b) * kp.max_pages,
+        j0, nK, len, hk, lane, ab, &load_items_sh);
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
@@ -225,6 +278,8 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
                      kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[jj & 1]);
+        // the slot of K_jj is free once these products complete
+        if (item + NSLOT < total_items) mma_commit(&kv_empty[slot]);
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -242,6 +297,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
           mma_f16_ts(tmem + C::O_COL, tmem + C::S_COL(j & 1) + 8 * kk,
                      sdesc_add(vdesc, kk * 16 * 128), idPV, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&pv_done);
+        if (item + NSLOT < total_items) mma_commit(&kv_empty[slot]);   // V_j's slot
         if (j == nK - 1) mma_commit(&o_full);
         if (j + 2 < nK) ok = issue_s(j + 2);
       }
@@ -262,13 +318,6 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         break;
       }
       tc_fence_after_sync();
-      if (r == 0) {
-        // S(j) complete: every MMA reading K_j, and (issued before S(j)) the
-        // P V product that read V_{j-2}, has completed.  Release only slots
-        // the producer refills.
-        if (2 * j + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j) % NSLOT]);
-        if (j >= 2 && 2 * j - 3 + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j - 3) % NSLOT]);
-      }
       const uint32_t tS = tmem + lane_addr + C::S_COL(j & 1);
       uint32_t sr[DBN];
 #pragma unroll
@@ -451,15 +500,18 @@ __global__ void __launch_bounds__(256)
 //    <= 1 multiplies the raw value codes and the row sum adds P' / dv_g.
 //    No value-descale pre-scan or extra O rescale is needed.
 //  * lanes 0..15 of every softmax warp fetch the descales of a tile two tiles
-//    ahead (block table one tile earlier still) and share them by shuffles.
+//    ahead (its block-table entries two tiles before that) and share them by
+//    shuffles.
 struct Dec8Cfg {
   static constexpr int D = 128;
   static constexpr int CHUNK16 = DBM * 128;          // 64 columns of the 16-bit query tile
-  static constexpr int Q16 = 2 * CHUNK16;            // 16-bit query tile
+  static constexpr int Q16 = 2 * CHUNK16;            // 16-bit query tile, in ring slots 0 and 1
   static constexpr int TILE8 = DBM * D;              // e4m3 query, key or value tile
-  static constexpr int NSLOT_FIT = (kSmemLimit - 2048 - Q16 - TILE8) / TILE8;
-  static constexpr int NSLOT = NSLOT_FIT > 12 ? 12 : NSLOT_FIT;
-  static constexpr int SMEM = 1024 + Q16 + TILE8 + NSLOT * TILE8;
+  static constexpr int NSLOT_FIT = (kSmemLimit - 2048 - TILE8) / TILE8;
+  static constexpr int NSLOT = NSLOT_FIT > 14 ? 14 : NSLOT_FIT;
+  static constexpr int SHIFT = 2;                    // ring slots the query tile occupies first
+  static constexpr int SMEM = 1024 + TILE8 + NSLOT * TILE8;
+  static_assert(Q16 == SHIFT * TILE8, "query staging must fill whole ring slots");
   static constexpr int THREADS = 6 * 32;
   static constexpr int LOAD_WARP = 4;
   static constexpr int MMA_WARP = 5;
@@ -479,9 +531,9 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;                  // 16-bit query tile, two 64-column chunks
-  uint8_t* sQ8 = smem + C::Q16;        // e4m3 query tile
-  uint8_t* sKV = sQ8 + C::TILE8;
+  uint8_t* sQ8 = smem;                 // e4m3 query tile
+  uint8_t* sKV = smem + C::TILE8;      // ring of NSLOT key / value tiles
+  uint8_t* sQ = sKV;                   // 16-bit query tile (two 64-column chunks) in slots 0, 1
 
   __shared__ __align__(8) uint64_t q_full;
   __shared__ __align__(8) uint64_t q8_full;
@@ -546,6 +598,13 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
   const uint32_t tmem = tmem_base_sh;
   const Abort ab{&abort_sh, kp.status};
   const int* table = kp.block_table + static_cast<size_t>(b) * kp.max_pages;
+  // Phase parity of the full barrier of item i's slot: the uses of that slot
+  // before it, not counting the query tile that first occupies slots
+  // 0 .. SHIFT-1 (it arrives through q_full, not through the slot's barrier).
+  auto full_parity = [](int i) -> uint32_t {
+    const int slot = (i + C::SHIFT) % NSLOT;
+    return static_cast<uint32_t>((i + C::SHIFT) / NSLOT - (slot < C::SHIFT ? 1 : 0)) & 1u;
+  };
 
   if (warp == C::LOAD_WARP) {
     // ------------------------------------------------------------ producer
@@ -557,36 +616,9 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c)
         tma_load_3d(sQ + c * C::CHUNK16, &tmQ, &q_full, c * 64, hk * kp.group * kp.n_q, b);
-      const int nbox = DBN / kp.box_rows;
-      int it = 0;
-      bool ok = true;
-      for (int j = 0; j < nK && ok; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int slot = it % NSLOT;
-          const int use = it / NSLOT;
-          if (use >= 1 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, ab, kDevTimeoutLoad)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&kv_full[slot], C::TILE8);
-          uint8_t* dst = sKV + slot * C::TILE8;
-          for (int x = 0; x < nbox; ++x) {
-            const int tok = (j0 + j) * DBN + x * kp.box_rows;
-            const int page = tok >> kp.page_shift;
-            int phys = kp.num_pages;               // out of range: zero-filled box
-            if (tok < len && page < kp.max_pages) {
-              const int pg = table[page];
-              if (pg >= 0 && pg < kp.num_pages) phys = pg;
-              else atomicCAS(kp.status, 0, kDevBadSeqlens);
-            }
-            tma_load_4d(dst + x * kp.box_rows * 128, kv ? &tmV : &tmK, &kv_full[slot], 0,
-                        tok & (kp.page_size - 1), hk, phys);
-          }
-          ++it;
-        }
-      }
-      load_items_sh = it;
     }
+    decode_produce<NSLOT, 1, 0, C::TILE8, 2>(&tmK, &tmV, sKV, kv_full, kv_empty, kp, table, j0, nK,
+                                             len, hk, lane, ab, &load_items_sh);
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
@@ -596,16 +628,23 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
       const uint64_t kdesc0 = sdesc_sw128(smem_u32(sKV), 16, 1024);           // K-major K
       const uint64_t vdesc0 = sdesc_sw128(smem_u32(sKV), C::TILE8, 1024);     // MN-major V
       bool ok = mbar_wait(&q8_full, 0, ab, kDevTimeoutMma);
+      if (ok) {
+        // every softmax thread has read its 16-bit query row: slots 0 and 1
+        // are free for keys and values
+        for (int sl = 0; sl < C::SHIFT; ++sl) mbar_arrive(&kv_empty[sl]);
+      }
       auto issue_s = [&](int jj) -> bool {
         const int item = 2 * jj;
-        const int slot = item % NSLOT;
-        if (!mbar_wait(&kv_full[slot], (item / NSLOT) & 1, ab, kDevTimeoutMma)) return false;
+        const int slot = (item + C::SHIFT) % NSLOT;
+        if (!mbar_wait(&kv_full[slot], full_parity(item), ab, kDevTimeoutMma)) return false;
         const uint64_t kdesc = opaque(sdesc_add(kdesc0, slot * C::TILE8));
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk)
           mma_f8_ss(tmem + C::S_COL(jj & 1), sdesc_add(qdesc, kk * 32), sdesc_add(kdesc, kk * 32),
                     idS, kk > 0 ? 1u : 0u);
         mma_commit(&s_full[jj & 1]);
+        // the slot of K_jj is free once these products complete
+        if (item + NSLOT < total_items) mma_commit(&kv_empty[slot]);
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -613,8 +652,8 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
       for (int j = 0; j < nK && ok; ++j) {
         // O += P'(j) V_j, P' packed e4m3 in columns [0, 32) of buffer j % 2
         const int item = 2 * j + 1;
-        const int slot = item % NSLOT;
-        if (!(ok = mbar_wait(&kv_full[slot], (item / NSLOT) & 1, ab, kDevTimeoutMma))) break;
+        const int slot = (item + C::SHIFT) % NSLOT;
+        if (!(ok = mbar_wait(&kv_full[slot], full_parity(item), ab, kDevTimeoutMma))) break;
         const uint64_t vdesc = opaque(sdesc_add(vdesc0, slot * C::TILE8));
         if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1, ab, kDevTimeoutMma))) break;
         tc_fence_after_sync();
@@ -623,6 +662,7 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
           mma_f8_ts(tmem + C::O_COL, tmem + C::S_COL(j & 1) + 8 * kk,
                     sdesc_add(vdesc, kk * 32 * 128), idPV, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&pv_done);
+        if (item + NSLOT < total_items) mma_commit(&kv_empty[slot]);   // V_j's slot
         if (j == nK - 1) mma_commit(&o_full);
         if (j + 2 < nK) ok = issue_s(j + 2);
       }
@@ -635,6 +675,12 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
     // ---- quantise this thread's query row
     if (__any_sync(0xffffffffu, !mbar_wait(&q_full, 0, ab, kDevTimeoutSoftmax))) {
       ok = false;
+    } else if (r >= kp.rows_real) {
+      // padding row: its scores are never used; zero codes
+#pragma unroll
+      for (int u = 0; u < 8; ++u) st_shared_v4(smem_u32(sQ8 + r * 128 + (u << 4)), 0u, 0u, 0u, 0u);
+      fence_proxy_async_smem();
+      mbar_arrive(&q8_full);
     } else {
       float x[D];
 #pragma unroll
@@ -675,12 +721,21 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < D; ++i) x[i] *= 0.08838834764831845f;   // 1 / sqrt(128)
       }
-      float amax = 0.f;
+      float am[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < D; ++i) amax = fmaxf(amax, fabsf(x[i]));
-      // descale = amax / 448 and code = e4m3(x / descale), both IEEE float32
-      // divisions: the rule of the block quantiser (once per CTA)
+      for (int i = 0; i < D; ++i) am[i & 3] = fmaxf(am[i & 3], fabsf(x[i]));
+      const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
+      // descale = amax / 448 and code = e4m3(x / descale) with x / descale
+      // rounded as an IEEE float32 division (the block quantiser's rule).
+      // One division gives y = RN(1 / dq); each quotient is then
+      // q0 = RN(x y) corrected by one step of Markstein's method (P. Markstein,
+      // IBM J. Res. Dev. 34(1), 1990): r = x - dq q0 exactly by FMA, q = RN(q0 + r y).
       const float dq = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+      const float y = __fdiv_rn(1.f, dq);
+      auto quot = [&](float v) -> float {
+        const float q0 = v * y;
+        return fmaf(fmaf(-dq, q0, v), y, q0);
+      };
       c_q = kp.scale_log2 * dq;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -688,8 +743,7 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = u * 16 + e * 4;
-          wq[e] = cvt_pack_e4m3x4(__fdiv_rn(x[i], dq), __fdiv_rn(x[i + 1], dq), __fdiv_rn(x[i + 2], dq),
-                                  __fdiv_rn(x[i + 3], dq));
+          wq[e] = cvt_pack_e4m3x4(quot(x[i]), quot(x[i + 1]), quot(x[i + 2]), quot(x[i + 3]));
         }
         st_shared_v4(smem_u32(sQ8 + r * 128 + ((u ^ (r & 7)) << 4)), wq[0], wq[1], wq[2], wq[3]);
       }
@@ -701,15 +755,17 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
     auto page_of = [&](int jj) -> int {
       const int tok = (j0 + jj) * DBN + 16 * (lane & 7);
       if (lane >= 16 || jj >= nK || tok >= len) return -1;
-      const int ph = __ldg(table + (tok >> kp.page_shift));
-      return (ph >= 0 && ph < kp.num_pages) ? ph : -1;
+      return __ldg(table + (tok >> kp.page_shift));   // checked when used, a tile later
     };
     auto desc_of = [&](int ph) -> float {
-      return ph < 0 ? 1.f : __ldg(dsrc + static_cast<size_t>(ph) * kp.H_kv + hk);
+      return (ph < 0 || ph >= kp.num_pages) ? 1.f
+                                             : __ldg(dsrc + static_cast<size_t>(ph) * kp.H_kv + hk);
     };
+    // descales two tiles ahead of use, block-table entries two tiles before that
+    int ph3 = page_of(3), ph4 = page_of(4);
     float dcur = desc_of(page_of(0));
-    float dnext = desc_of(page_of(1));
-    int ph2 = page_of(2);
+    float dn1 = desc_of(page_of(1));
+    float dn2 = desc_of(page_of(2));
 
     const int vis_end = kp.causal ? min(len, len - kp.n_q + tq + 1) : len;
     float m_ref = -INFINITY;   // log2 units of y = s + log2(dv)
@@ -717,7 +773,8 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
     for (int j = 0; j < nK && ok; ++j) {
       // group coefficients: lanes g < 8 hold dk_g, lanes 8 + g hold dv_g
       const float lgd = lg2_dec(dcur);
-      const float invd = 1.f / dcur;
+      float invd;
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(invd) : "f"(dcur));
       float coef[8], lgv[8], ivv[8];
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
@@ -730,10 +787,6 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
         break;
       }
       tc_fence_after_sync();
-      if (r == 0) {
-        if (2 * j + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j) % NSLOT]);
-        if (j >= 2 && 2 * j - 3 + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j - 3) % NSLOT]);
-      }
       const uint32_t tS = tmem + lane_addr + C::S_COL(j & 1);
       uint32_t sr[DBN];
 #pragma unroll
@@ -768,7 +821,7 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
       // error; the running maximum of a decode row rises on few tiles, so the
       // extra O rescales cost little.
       const float m_new = fmaxf(m_ref, mt);
-      const bool need = m_new > m_ref;
+      const bool need = (m_new - m_ref) > 8.f;   // EXPERIMENT lazy
       float alpha = 1.f;
       if (need) {
         alpha = ex2_approx(m_ref - m_new);
@@ -823,9 +876,11 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(&p_full[j & 1]);
       // advance the descale pipeline
-      dcur = dnext;
-      dnext = desc_of(ph2);
-      ph2 = page_of(j + 3);
+      dcur = dn1;
+      dn1 = dn2;
+      dn2 = desc_of(ph3);
+      ph3 = ph4;
+      ph4 = page_of(j + 5);
     }
     // ------------------------------------------------------------ epilogue
     if (ok && !__any_sync(0xffffffffu, !mbar_wait(&o_full, 0, ab, kDevTimeoutEpilogue))) {
@@ -858,8 +913,8 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
     if (warp == C::LOAD_WARP && lane == 0) {
       mbar_wait_drain(&q_full, 0);
       const int issued = load_items_sh;
-      for (int s = 0; s < NSLOT && s < issued; ++s)
-        mbar_wait_drain(&kv_full[s], ((issued - 1 - s) / NSLOT) & 1);
+      for (int i = issued - 1; i >= 0 && i >= issued - NSLOT; --i)
+        mbar_wait_drain(&kv_full[(i + C::SHIFT) % NSLOT], full_parity(i));
     }
     if (warp == C::MMA_WARP && lane == 0) {
       mma_commit(&drain_bar);
@@ -935,10 +990,13 @@ attn_status_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   int* status = device_status_word();
   if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
   const DecodeSplits sp = decode_splits(p.B, p.H_kv, p.max_seqlen);
+  int shift = 0;
+  while ((1 << shift) < p.page_size) ++shift;
   DecKParams kp{p.block_table, p.seq_lens, p.o_part,  p.lse_part,  status,
                 p.H,           p.H / p.H_kv, p.n_q,   (p.H / p.H_kv) * p.n_q,
                 p.max_pages,   p.page_size, box_rows, p.num_pages,
-                sp.splits,     sp.tiles_per_split, p.causal, p.scale * 1.4426950408889634f};
+                sp.splits,     sp.tiles_per_split, p.causal, p.scale * 1.4426950408889634f,
+                nullptr,       nullptr,     nullptr, p.H_kv, shift};
   kern<<<dim3(sp.splits, p.H_kv, p.B), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, kp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "decode split kernel launch");

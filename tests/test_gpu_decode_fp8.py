@@ -126,6 +126,12 @@ def test_long_sequences_split(attn):
     _check(*_run(attn, [9000, 20000], 64, 8, 2, 1, True, seed=83))
 
 
+def test_long_splits_reuse_every_ring_slot(attn):
+    # 19 sequences x 8 key/value heads fill the 152 SMs once, so each CTA takes
+    # a whole sequence: 16 tiles, 32 ring items, every slot used two or three times
+    _check(*_run(attn, [2048] * 19, 64, 8, 8, 1, True, seed=89))
+
+
 def test_fp16_and_empty_sequence(attn):
     _check(*_run(attn, [0, 513, 2], 16, 4, 2, 3, True, dtype="fp16", seed=84))
 
