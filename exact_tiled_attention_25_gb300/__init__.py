@@ -32,7 +32,8 @@ _DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 __all__ = ["AttnError", "attn_fwd", "attn_fwd_gqa", "attn_fwd_varlen", "attn_bwd",
            "attn_bwd_gqa", "attn_bwd_varlen", "attn_bwd_varlen_workspace_size",
            "attn_bwd_workspace_size",
-           "attn_fp8_quantize", "attn_fp8_quantize_rope", "attn_fwd_fp8",
+           "attn_fp8_quantize", "attn_fp8_quantize_gqa", "attn_fp8_quantize_rope", "attn_fwd_fp8",
+           "attn_fwd_fp8_gqa",
            "attn_decode_paged", "attn_decode_paged_fp8", "attn_decode_workspace_size",
            "attn_get_device_status",
            "attn_status_string", "attn_last_error", "load_library"]
@@ -318,6 +319,35 @@ def attn_fp8_quantize(q, k, v, hadamard_signs=None, per_tensor: bool = False, st
     return tuple(outs), tuple(desc)
 
 
+def attn_fp8_quantize_gqa(q, k, v, hadamard_signs=None, per_tensor: bool = False, stream=None):
+    """float32 Q [B, H, N, d] and K, V [B, H_kv, N, d] -> e4m3 codes (q8, k8, v8)
+    and float32 block descales."""
+    lib = _lib.load()
+    ins = [q, k, v] + ([hadamard_signs] if hadamard_signs is not None else [])
+    ins, host = _to_device(ins)
+    q, k, v = ins[:3]
+    signs = ins[3] if hadamard_signs is not None else None
+    B, H, N, d = _shape4(q, "q")
+    _, Hkv, _, _ = _shape4(k, "k")
+    for t, n in ((k, "k"), (v, "v")):
+        if _shape4(t, n) != (B, Hkv, N, d) or t.dtype != torch.float32:
+            raise ValueError("k and v must be float32 [B, H_kv, N, d] with q's B, N, d")
+    if q.dtype != torch.float32:
+        raise ValueError("FP8 pre-pass inputs are float32")
+    if signs is not None and (signs.dtype != torch.float32 or signs.numel() != d):
+        raise ValueError("hadamard_signs must be d float32 values")
+    nblk = (N + 127) // 128
+    outs = [torch.empty((B, h, N, d), dtype=torch.uint8, device=q.device) for h in (H, Hkv, Hkv)]
+    desc = [torch.empty((B, h, nblk), dtype=torch.float32, device=q.device) for h in (H, Hkv, Hkv)]
+    code = lib.attn_fp8_quantize_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(signs),
+                                     *[_ptr(t) for t in outs], *[_ptr(t) for t in desc],
+                                     B, H, Hkv, N, d, int(bool(per_tensor)), _stream(stream))
+    _check(code, "attn_fp8_quantize_gqa")
+    if host:
+        return tuple(t.cpu() for t in outs), tuple(t.cpu() for t in desc)
+    return tuple(outs), tuple(desc)
+
+
 def attn_fp8_quantize_rope(q, k, v, rope_cos, rope_sin, hadamard_signs=None, stream=None):
     """attn_fp8_quantize (block mode) with Q and K rotated by the tables
     rope_cos, rope_sin (float32 [N, d/2]) before the Hadamard transform."""
@@ -468,6 +498,38 @@ def attn_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, causal: bool = Fal
                             _ptr(v_descale), _ptr(o), _ptr(lse), B, H, N, d,
                             int(bool(causal)), scale, _stream(stream))
     _check(code, "attn_fwd_fp8")
+    if host:
+        return o.cpu(), lse.cpu()
+    return o, lse
+
+
+def attn_fwd_fp8_gqa(q8, k8, v8, q_descale, k_descale, v_descale, causal: bool = False,
+                     softmax_scale: float | None = None, o=None, lse=None, stream=None):
+    """FP8 forward with grouped-query heads: q8 [B, H, N, d], k8 and v8
+    [B, H_kv, N, d] (uint8 e4m3) with their block descales -> O (bfloat16), LSE."""
+    lib = _lib.load()
+    (q8, k8, v8, q_descale, k_descale, v_descale), host = _to_device(
+        [q8, k8, v8, q_descale, k_descale, v_descale])
+    B, H, N, d = _shape4(q8, "q8")
+    _, Hkv, _, _ = _shape4(k8, "k8")
+    for t, n in ((k8, "k8"), (v8, "v8")):
+        if _shape4(t, n) != (B, Hkv, N, d) or t.dtype != torch.uint8:
+            raise ValueError(f"{n} must be uint8 e4m3 codes [B, H_kv, N, d]")
+    if q8.dtype != torch.uint8:
+        raise ValueError("q8 must be uint8 e4m3 codes")
+    nblk = (N + 127) // 128
+    for t, h in ((q_descale, H), (k_descale, Hkv), (v_descale, Hkv)):
+        if t.dtype != torch.float32 or tuple(t.shape) != (B, h, nblk) or not t.is_contiguous():
+            raise ValueError("descales must be contiguous float32 [B, heads, ceil(N/128)]")
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    code = lib.attn_fwd_fp8_gqa(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_descale), _ptr(k_descale),
+                                _ptr(v_descale), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                                int(bool(causal)), scale, _stream(stream))
+    _check(code, "attn_fwd_fp8_gqa")
     if host:
         return o.cpu(), lse.cpu()
     return o, lse

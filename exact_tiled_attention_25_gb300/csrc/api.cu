@@ -340,9 +340,19 @@ attn_status_t attn_fp8_quantize(const float* q, const float* k, const float* v,
                                 uint8_t* v8, float* q_descale, float* k_descale,
                                 float* v_descale, int B, int H, int N, int d, int per_tensor,
                                 cudaStream_t stream) {
+  return attn_fp8_quantize_gqa(q, k, v, hadamard_signs, q8, k8, v8, q_descale, k_descale,
+                               v_descale, B, H, H, N, d, per_tensor, stream);
+}
+
+attn_status_t attn_fp8_quantize_gqa(const float* q, const float* k, const float* v,
+                                    const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                    uint8_t* v8, float* q_descale, float* k_descale,
+                                    float* v_descale, int B, int H, int H_kv, int N, int d,
+                                    int per_tensor, cudaStream_t stream) {
   g_last_error.clear();
   attn_status_t s;
   if ((s = check_shape(B, H, N, d, 0)) != ATTN_OK) return s;
+  if ((s = check_heads(H, H_kv)) != ATTN_OK) return s;
   if ((s = check_ptrs({q, k, v, q8, k8, v8, q_descale, k_descale, v_descale})) != ATTN_OK)
     return s;
   if (per_tensor != 0 && per_tensor != 1)
@@ -354,7 +364,7 @@ attn_status_t attn_fp8_quantize(const float* q, const float* k, const float* v,
   if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
   if ((s = check_device()) != ATTN_OK) return s;
   Fp8QuantParams p{{q, k, v}, {q8, k8, v8}, {q_descale, k_descale, v_descale}, hadamard_signs,
-                   B, H, N, d, per_tensor};
+                   B, H, N, d, per_tensor, nullptr, nullptr, H_kv};
   return launch_fp8_quantize(p, stream);
 }
 
@@ -484,9 +494,19 @@ attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* 
                            const float* q_descale, const float* k_descale,
                            const float* v_descale, void* o, float* lse, int B, int H, int N,
                            int d, int causal, float softmax_scale, cudaStream_t stream) {
+  return attn_fwd_fp8_gqa(q8, k8, v8, q_descale, k_descale, v_descale, o, lse, B, H, H, N, d,
+                          causal, softmax_scale, stream);
+}
+
+attn_status_t attn_fwd_fp8_gqa(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
+                               const float* q_descale, const float* k_descale,
+                               const float* v_descale, void* o, float* lse, int B, int H,
+                               int H_kv, int N, int d, int causal, float softmax_scale,
+                               cudaStream_t stream) {
   g_last_error.clear();
   attn_status_t s;
   if ((s = check_shape(B, H, N, d, causal)) != ATTN_OK) return s;
+  if ((s = check_heads(H, H_kv)) != ATTN_OK) return s;
   if ((s = check_ptrs({q8, k8, v8, o, lse})) != ATTN_OK) return s;
   if (!q_descale || !k_descale || !v_descale)
     return fail(ATTN_ERR_INVALID_ARG, "null descale pointer");
@@ -494,7 +514,7 @@ attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* 
   if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
   if ((s = check_device()) != ATTN_OK) return s;
   Fp8FwdParams p{q8, k8, v8, q_descale, k_descale, v_descale, o, lse, B, H, N, d, causal,
-                 softmax_scale};
+                 softmax_scale, H_kv};
   return launch_fwd_fp8(p, stream);
 }
 

@@ -82,6 +82,7 @@ struct Fp8QuantParams {
   int per_tensor;
   const float* rope_cos = nullptr;   // [N, d/2] rotary tables (block mode), or nullptr
   const float* rope_sin = nullptr;
+  int H_kv = 0;                      // heads of K and V (0: H)
 };
 
 struct Fp8FwdParams {
@@ -96,6 +97,7 @@ struct Fp8FwdParams {
   int B, H, N, d;
   int causal;
   float scale;
+  int H_kv;   // heads of K and V (H % H_kv == 0)
 };
 
 attn_status_t launch_fwd(const FwdParams& p, cudaStream_t stream);

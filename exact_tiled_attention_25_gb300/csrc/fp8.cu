@@ -42,9 +42,10 @@ __global__ void __launch_bounds__(256)
                      uint8_t* __restrict__ dst1, uint8_t* __restrict__ dst2,
                      float* __restrict__ desc0, float* __restrict__ desc1,
                      float* __restrict__ desc2, const float* __restrict__ signs, int N,
-                     int nblk) {
+                     int nblk, int kv_planes) {
   constexpr int D = 128;
   const int which = blockIdx.z;
+  if (which > 0 && static_cast<int>(blockIdx.y) >= kv_planes) return;   // K, V: B * H_kv planes
   const float* src = which == 0 ? src0 : (which == 1 ? src1 : src2);
   uint8_t* dst = which == 0 ? dst0 : (which == 1 ? dst1 : dst2);
   float* desc = which == 0 ? desc0 : (which == 1 ? desc1 : desc2);
@@ -140,9 +141,10 @@ __global__ void __launch_bounds__(256)
                      uint8_t* __restrict__ dst1, uint8_t* __restrict__ dst2,
                      float* __restrict__ desc0, float* __restrict__ desc1,
                      float* __restrict__ desc2, const float* __restrict__ signs, int N,
-                     int nblk, int* status, const float* __restrict__ rope_cos = nullptr,
+                     int nblk, int kv_planes, int* status, const float* __restrict__ rope_cos = nullptr,
                      const float* __restrict__ rope_sin = nullptr) {
   constexpr int D = 128;
+  if (blockIdx.z > 0 && static_cast<int>(blockIdx.y) >= kv_planes) return;   // K, V: B * H_kv planes
   extern __shared__ __align__(128) float sblk[];   // [QROWS][D]
   __shared__ __align__(8) uint64_t full_bar[8];    // one per warp's 16 rows
   __shared__ int abort_sh;
@@ -261,8 +263,9 @@ __global__ void __launch_bounds__(256)
 // single descale into every entry.
 __global__ void __launch_bounds__(256)
     fp8_tensor_scale_kernel(float* __restrict__ desc0, float* __restrict__ desc1,
-                            float* __restrict__ desc2, long long count) {
+                            float* __restrict__ desc2, long long q_count, long long kv_count) {
   float* desc = blockIdx.x == 0 ? desc0 : (blockIdx.x == 1 ? desc1 : desc2);
+  const long long count = blockIdx.x == 0 ? q_count : kv_count;
   __shared__ float warp_max[8];
   float m = 0.f;
   for (long long i = threadIdx.x; i < count; i += blockDim.x) m = fmaxf(m, desc[i]);
@@ -311,6 +314,7 @@ struct Fp8KParams {
   int H;
   int nblk;
   float scale_log2;
+  int H_kv;   // key/value heads; query head h reads key/value head h / (H / H_kv)
 };
 
 __device__ __forceinline__ float lg2_approx8(float x) {
@@ -352,6 +356,8 @@ __global__ void __launch_bounds__(THREADS8, 1)
                        : static_cast<int>(blockIdx.x);
   const int bh = CAUSAL ? static_cast<int>(blockIdx.x % (gridDim.x / npairs))
                         : static_cast<int>(blockIdx.z * kp.H + blockIdx.y);
+  // key/value plane (and descale row) of this query head
+  const int kvp = (bh / kp.H) * kp.H_kv + (bh % kp.H) / (kp.H / kp.H_kv);
   const int N = kp.N;
   const int nKtot = (N + BN - 1) / BN;
   int nK[NQ8];
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(THREADS8, 1)
             break;
           }
           mbar_arrive_expect_tx(&kv_full[slot], TILE8);
-          tma_load_3d(sKV + slot * TILE8, kv ? &tmV : &tmK, &kv_full[slot], 0, j * BN, bh);
+          tma_load_3d(sKV + slot * TILE8, kv ? &tmV : &tmK, &kv_full[slot], 0, j * BN, kvp);
           ++it;
         }
       }
@@ -492,8 +498,8 @@ __global__ void __launch_bounds__(THREADS8, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_addr + s_col8(t) + 64 * h;       // this half's scores
     const uint32_t tO = tmem + lane_addr + o_col8(t) + (D8 / 2) * h;  // this half's O columns
-    const float* kdesc = kp.k_descale + static_cast<size_t>(bh) * kp.nblk;
-    const float* vdesc = kp.v_descale + static_cast<size_t>(bh) * kp.nblk;
+    const float* kdesc = kp.k_descale + static_cast<size_t>(kvp) * kp.nblk;
+    const float* vdesc = kp.v_descale + static_cast<size_t>(kvp) * kp.nblk;
     float dv_max = 0.f;
     for (int b = 0; b < kp.nblk; ++b) dv_max = fmaxf(dv_max, vdesc[b]);
     const float c_q = (my_nK > 0) ? kp.scale_log2 * kp.q_descale[static_cast<size_t>(bh) * kp.nblk + qt] : 0.f;
@@ -658,6 +664,8 @@ attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) 
   const int nblk = (p.N + 127) / 128;
   if (p.B * p.H > 65535 || nblk > 2147483647 / 128)
     return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
+  const int H_kv = p.H_kv > 0 ? p.H_kv : p.H;
+  const int kv_planes = p.B * H_kv;
   dim3 grid(nblk, p.B * p.H, 3);
   if (p.rope_cos) {
     int* status = device_status_word();
@@ -667,20 +675,21 @@ attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) 
     if (s != ATTN_OK) return s;
     kern<<<grid, 256, QSMEM, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1], p.dst[2],
                                        p.descale[0], p.descale[1], p.descale[2], p.signs, p.N,
-                                       nblk, status, p.rope_cos, p.rope_sin);
+                                       nblk, kv_planes, status, p.rope_cos, p.rope_sin);
   } else if (!p.per_tensor) {
     fp8_quant_kernel<0><<<grid, 256, 0, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1],
                                                   p.dst[2], p.descale[0], p.descale[1],
-                                                  p.descale[2], p.signs, p.N, nblk);
+                                                  p.descale[2], p.signs, p.N, nblk, kv_planes);
   } else {
     fp8_quant_kernel<1><<<grid, 256, 0, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1],
                                                   p.dst[2], p.descale[0], p.descale[1],
-                                                  p.descale[2], nullptr, p.N, nblk);
+                                                  p.descale[2], nullptr, p.N, nblk, kv_planes);
     fp8_tensor_scale_kernel<<<3, 256, 0, stream>>>(p.descale[0], p.descale[1], p.descale[2],
-                                                   static_cast<long long>(p.B) * p.H * nblk);
+                                                   static_cast<long long>(p.B) * p.H * nblk,
+                                                   static_cast<long long>(kv_planes) * nblk);
     fp8_quant_kernel<2><<<grid, 256, 0, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1],
                                                   p.dst[2], p.descale[0], p.descale[1],
-                                                  p.descale[2], nullptr, p.N, nblk);
+                                                  p.descale[2], nullptr, p.N, nblk, kv_planes);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "FP8 pre-pass launch");
@@ -694,13 +703,14 @@ attn_status_t launch_fwd_fp8_t(const Fp8FwdParams& p, cudaStream_t stream) {
   if (s != ATTN_OK) return s;
   CUtensorMap tq, tk, tv;
   const uint64_t planes = static_cast<uint64_t>(p.B) * p.H;
+  const uint64_t kv_planes = static_cast<uint64_t>(p.B) * p.H_kv;
   if ((s = make_tmap_3d(&tq, p.q8, 1, D8, p.N, planes, 128, BM)) != ATTN_OK) return s;
-  if ((s = make_tmap_3d(&tk, p.k8, 1, D8, p.N, planes, 128, BN)) != ATTN_OK) return s;
-  if ((s = make_tmap_3d(&tv, p.v8, 1, D8, p.N, planes, 128, BN)) != ATTN_OK) return s;
+  if ((s = make_tmap_3d(&tk, p.k8, 1, D8, p.N, kv_planes, 128, BN)) != ATTN_OK) return s;
+  if ((s = make_tmap_3d(&tv, p.v8, 1, D8, p.N, kv_planes, 128, BN)) != ATTN_OK) return s;
   int* status = device_status_word();
   if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
   Fp8KParams kp{p.q_descale, p.k_descale, p.v_descale, p.o, p.lse, status, p.N, p.H,
-                (p.N + 127) / 128, p.scale * 1.4426950408889634f};
+                (p.N + 127) / 128, p.scale * 1.4426950408889634f, p.H_kv};
   const unsigned npairs = static_cast<unsigned>((p.N + BM * NQ8 - 1) / (BM * NQ8));
   const dim3 grid = CAUSAL ? dim3(npairs * p.H * p.B, 1, 1) : dim3(npairs, p.H, p.B);
   kern<<<grid, THREADS8, SMEM8, stream>>>(tq, tk, tv, kp);

@@ -316,6 +316,22 @@ attn_status_t attn_fp8_quantize(const float* q, const float* k, const float* v,
                                 cudaStream_t stream);
 
 /*
+ * attn_fp8_quantize_gqa -- attn_fp8_quantize for grouped-query attention: Q has
+ * H heads, K and V have H_kv (H % H_kv == 0; "FlashAttention 3 Hardware
+ * Acceleration: ...", section "GPU Compatibility and Enablement Matrix",
+ * grouped-query attention by template specialisation).
+ *   q, q8          : [B, H, N, d];  q_descale : [B, H, ceil(N/128)].
+ *   k, v, k8, v8   : [B, H_kv, N, d];  k_descale, v_descale : [B, H_kv, ceil(N/128)].
+ * Blocks, transform, per-tensor mode and errors as attn_fp8_quantize (which is
+ * this call with H_kv = H).
+ */
+attn_status_t attn_fp8_quantize_gqa(const float* q, const float* k, const float* v,
+                                    const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                    uint8_t* v8, float* q_descale, float* k_descale,
+                                    float* v_descale, int B, int H, int H_kv, int N, int d,
+                                    int per_tensor, cudaStream_t stream);
+
+/*
  * attn_fp8_quantize_rope -- attn_fp8_quantize (block mode) with the rotary
  * position embedding of Q and K fused in front of the Hadamard transform
  * ("FlashAttention-3: Hopper Asynchrony and FP8 Attention", section "FP8
@@ -348,6 +364,23 @@ attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* 
                            const float* q_descale, const float* k_descale,
                            const float* v_descale, void* o, float* lse, int B, int H, int N,
                            int d, int causal, float softmax_scale, cudaStream_t stream);
+
+/*
+ * attn_fwd_fp8_gqa -- attn_fwd_fp8 with grouped-query heads: query head h of
+ * batch b reads key/value head h / (H / H_kv) and its block descales.
+ *   q8 : [B, H, N, d] with q_descale [B, H, ceil(N/128)];
+ *   k8, v8 : [B, H_kv, N, d] with k_descale, v_descale [B, H_kv, ceil(N/128)]
+ *   (the output of attn_fp8_quantize_gqa);  o, lse as attn_fwd_fp8.
+ * attn_fwd_fp8 is this call with H_kv = H.  Source: the FP8 forward of
+ * "FlashAttention-3: Hopper Asynchrony and FP8 Attention" with the head sharing
+ * of "FlashAttention 3 Hardware Acceleration: ...", section "GPU Compatibility
+ * and Enablement Matrix".
+ */
+attn_status_t attn_fwd_fp8_gqa(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
+                               const float* q_descale, const float* k_descale,
+                               const float* v_descale, void* o, float* lse, int B, int H,
+                               int H_kv, int N, int d, int causal, float softmax_scale,
+                               cudaStream_t stream);
 
 /*
  * attn_get_device_status -- synchronises `stream`, then reads and clears the

@@ -204,3 +204,17 @@ def test_fp8_decode_is_declared_and_validates(lib):
                           (dict(signs=8), 1, "hadamard_signs"), (dict(scale=0.0), 1, "softmax_scale")):
         assert call(**kw) == code, kw
         assert why.lower() in lib.attn_last_error().decode().lower(), (kw, lib.attn_last_error())
+
+
+def test_fp8_gqa_is_declared_and_validates(lib):
+    names = declared_functions()
+    assert "attn_fp8_quantize_gqa" in names and "attn_fwd_fp8_gqa" in names
+    for H_kv, why in ((3, "H_kv"), (0, "H_kv"), (8, "H_kv")):
+        code = lib.attn_fwd_fp8_gqa(16, 16, 16, 16, 16, 16, 16, 16, 1, 4, H_kv, 256, 128, 0, 0.1,
+                                    None)
+        assert code == 1 and why.encode() in lib.attn_last_error()
+        code = lib.attn_fp8_quantize_gqa(16, 16, 16, None, 16, 16, 16, 16, 16, 16, 1, 4, H_kv,
+                                         256, 128, 0, None)
+        assert code == 1 and why.encode() in lib.attn_last_error()
+    assert lib.attn_fwd_fp8_gqa(16, 16, 16, 16, 16, 16, 16, 16, 1, 4, 2, 256, 64, 0, 0.1,
+                                None) == 2                     # d = 128 only
