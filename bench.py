@@ -451,6 +451,7 @@ def run_sweep(torch, attn, dev, stream, causal, steps=20, warmup=3):
             out[f"{name}_d{d}_h{h}"] = {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1)}
         del q, k, v, do, o, lse
     out.update(run_varlen_gqa(torch, attn, dev, stream, causal, steps, warmup))
+    out.update(run_fp8_gqa(torch, attn, dev, stream, causal, steps, warmup))
     out.update(run_prepass_rope(torch, attn, dev, stream, steps, warmup))
     out.update(run_decode(torch, attn, dev, stream, steps, warmup))
     out.update(run_decode_fp8(torch, attn, dev, stream, steps, warmup))
@@ -562,6 +563,38 @@ def run_prepass_rope(torch, attn, dev, stream, steps=20, warmup=3):
     nbytes = 3 * B * H * N * D * (4 + 1) + 3 * B * H * nblk * 4 + 2 * N * (D // 2) * 4
     return {f"fp8_prepass_rope_b{B}h{H}n{N}d{D}": {"ms": round(ms, 4),
                                                     "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}}
+
+
+def run_fp8_gqa(torch, attn, dev, stream, causal, steps=20, warmup=3):
+    """FP8 forward with grouped-query heads at the timed shape: B = 2, N = 8192,
+    H = 16 query heads sharing H_kv = 4 key/value heads, d = 128 (block scales
+    and the Hadamard transform from the pre-pass, which runs once untimed).
+    FLOP = 4*B*H*N^2*d, halved causal."""
+    g = torch.Generator(device=dev).manual_seed(12)
+    hkv = 4
+    q = torch.randn((B, H, N, D), generator=g, device=dev)
+    k, v = (torch.randn((B, hkv, N, D), generator=g, device=dev) for _ in range(2))
+    signs = torch.where(torch.rand(D, generator=g, device=dev) < 0.5, -1.0, 1.0).float()
+    (q8, k8, v8), (qd, kd, vd) = attn.attn_fp8_quantize_gqa(q, k, v, hadamard_signs=signs,
+                                                            stream=stream)
+    del q, k, v
+    o = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    fn = lambda: attn.attn_fwd_fp8_gqa(q8, k8, v8, qd, kd, vd, causal=causal, o=o, lse=lse,
+                                       stream=stream)
+    for _ in range(warmup):
+        fn()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    flop = 4.0 * B * H * N * N * D / (2 if causal else 1)
+    return {f"fp8_gqa_fwd_b{B}h{H}kv{hkv}n{N}d{D}": {"ms": round(ms, 4),
+                                                     "tflops": round(flop / (ms * 1e-3) / 1e12, 1)}}
 
 
 def run_varlen_gqa(torch, attn, dev, stream, causal, steps=20, warmup=3):

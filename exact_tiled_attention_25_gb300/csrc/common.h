@@ -101,6 +101,8 @@ struct Fp8FwdParams {
 };
 
 attn_status_t launch_fwd(const FwdParams& p, cudaStream_t stream);
+// Persistent forward (cluster launch control) for packed causal batches.
+attn_status_t launch_fwd_persistent(const FwdParams& p, cudaStream_t stream);
 attn_status_t launch_bwd(const BwdParams& p, cudaStream_t stream);
 attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream);
 attn_status_t launch_fwd_fp8(const Fp8FwdParams& p, cudaStream_t stream);

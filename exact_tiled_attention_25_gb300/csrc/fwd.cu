@@ -528,6 +528,8 @@ attn_status_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
   if (p.N > 65535 * 256 || p.H > 65535 || p.B > 65535 ||
       static_cast<long long>((p.N + 255) / 128) * p.H * p.B > 2147483647LL)
     return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
+  // packed causal batches: the persistent kernel, which measured faster there
+  if (p.cu_seqlens && p.causal) return launch_fwd_persistent(p, stream);
   switch (p.d) {
     case 64: return launch_fwd_d<64>(p, stream);
     case 128: return launch_fwd_d<128>(p, stream);
