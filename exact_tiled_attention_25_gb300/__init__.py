@@ -33,7 +33,7 @@ __all__ = ["AttnError", "attn_fwd", "attn_fwd_gqa", "attn_fwd_varlen", "attn_bwd
            "attn_bwd_gqa", "attn_bwd_varlen", "attn_bwd_varlen_workspace_size",
            "attn_bwd_workspace_size",
            "attn_fp8_quantize", "attn_fp8_quantize_gqa", "attn_fp8_quantize_rope", "attn_fwd_fp8",
-           "attn_fwd_fp8_gqa",
+           "attn_fwd_fp8_gqa", "attn_fp8_quantize_varlen", "attn_fwd_fp8_varlen",
            "attn_decode_paged", "attn_decode_paged_fp8", "attn_decode_workspace_size",
            "attn_get_device_status",
            "attn_status_string", "attn_last_error", "load_library"]
@@ -530,6 +530,72 @@ def attn_fwd_fp8_gqa(q8, k8, v8, q_descale, k_descale, v_descale, causal: bool =
                                 _ptr(v_descale), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
                                 int(bool(causal)), scale, _stream(stream))
     _check(code, "attn_fwd_fp8_gqa")
+    if host:
+        return o.cpu(), lse.cpu()
+    return o, lse
+
+
+def attn_fp8_quantize_varlen(q, k, v, cu_seqlens, max_seqlen: int, hadamard_signs=None,
+                             stream=None):
+    """Block pre-pass of a packed batch: float32 q [total, H, d], k, v
+    [total, H_kv, d], int32 cu_seqlens [B + 1] -> e4m3 codes of the same shapes
+    and float32 descales [B, heads, ceil(max_seqlen / 128)]."""
+    lib = _lib.load()
+    ins = [q, k, v, cu_seqlens] + ([hadamard_signs] if hadamard_signs is not None else [])
+    ins, host = _to_device(ins)
+    q, k, v, cu_seqlens = ins[:4]
+    signs = ins[4] if hadamard_signs is not None else None
+    total, H, d = _shape3(q, "q")
+    Hkv = k.shape[1] if k.dim() == 3 else -1
+    if _shape3(k, "k") != (total, Hkv, d) or _shape3(v, "v") != (total, Hkv, d):
+        raise ValueError("k and v must be [total, H_kv, d] with q's total and d")
+    if any(t.dtype != torch.float32 for t in (q, k, v)):
+        raise ValueError("FP8 pre-pass inputs are float32")
+    if signs is not None and (signs.dtype != torch.float32 or signs.numel() != d):
+        raise ValueError("hadamard_signs must be d float32 values")
+    B = _cu_seqlens(cu_seqlens, total)
+    nblk = (int(max_seqlen) + 127) // 128
+    outs = [torch.empty((total, h, d), dtype=torch.uint8, device=q.device) for h in (H, Hkv, Hkv)]
+    desc = [torch.empty((B, h, nblk), dtype=torch.float32, device=q.device) for h in (H, Hkv, Hkv)]
+    code = lib.attn_fp8_quantize_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(signs),
+                                        *[_ptr(t) for t in outs], *[_ptr(t) for t in desc],
+                                        _ptr(cu_seqlens), B, int(max_seqlen), total, H, Hkv, d,
+                                        _stream(stream))
+    _check(code, "attn_fp8_quantize_varlen")
+    if host:
+        return tuple(t.cpu() for t in outs), tuple(t.cpu() for t in desc)
+    return tuple(outs), tuple(desc)
+
+
+def attn_fwd_fp8_varlen(q8, k8, v8, q_descale, k_descale, v_descale, cu_seqlens,
+                        max_seqlen: int, causal: bool = False,
+                        softmax_scale: float | None = None, o=None, lse=None, stream=None):
+    """FP8 forward over a packed batch (the output of attn_fp8_quantize_varlen):
+    returns O [total, H, d] bfloat16 and LSE float32 [H, total]."""
+    lib = _lib.load()
+    (q8, k8, v8, q_descale, k_descale, v_descale, cu_seqlens), host = _to_device(
+        [q8, k8, v8, q_descale, k_descale, v_descale, cu_seqlens])
+    total, H, d = _shape3(q8, "q8")
+    Hkv = k8.shape[1] if k8.dim() == 3 else -1
+    if _shape3(k8, "k8") != (total, Hkv, d) or _shape3(v8, "v8") != (total, Hkv, d):
+        raise ValueError("k8 and v8 must be [total, H_kv, d] with q8's total and d")
+    if any(t.dtype != torch.uint8 for t in (q8, k8, v8)):
+        raise ValueError("q8, k8, v8 must be uint8 e4m3 codes")
+    B = _cu_seqlens(cu_seqlens, total)
+    nblk = (int(max_seqlen) + 127) // 128
+    for t, h in ((q_descale, H), (k_descale, Hkv), (v_descale, Hkv)):
+        if t.dtype != torch.float32 or tuple(t.shape) != (B, h, nblk) or not t.is_contiguous():
+            raise ValueError("descales must be contiguous float32 [B, heads, ceil(max_seqlen/128)]")
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    if o is None:
+        o = torch.empty((total, H, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((H, total), dtype=torch.float32, device=q8.device)
+    code = lib.attn_fwd_fp8_varlen(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_descale),
+                                   _ptr(k_descale), _ptr(v_descale), _ptr(o), _ptr(lse),
+                                   _ptr(cu_seqlens), B, int(max_seqlen), total, H, Hkv, d,
+                                   int(bool(causal)), scale, _stream(stream))
+    _check(code, "attn_fwd_fp8_varlen")
     if host:
         return o.cpu(), lse.cpu()
     return o, lse

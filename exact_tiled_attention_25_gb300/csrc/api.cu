@@ -368,6 +368,29 @@ attn_status_t attn_fp8_quantize_gqa(const float* q, const float* k, const float*
   return launch_fp8_quantize(p, stream);
 }
 
+attn_status_t attn_fp8_quantize_varlen(const float* q, const float* k, const float* v,
+                                       const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                       uint8_t* v8, float* q_descale, float* k_descale,
+                                       float* v_descale, const int* cu_seqlens, int B,
+                                       int max_seqlen, int total, int H, int H_kv, int d,
+                                       cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if ((s = check_packed(B, max_seqlen, total, H, d, 0)) != ATTN_OK) return s;
+  if ((s = check_heads(H, H_kv)) != ATTN_OK) return s;
+  if ((s = check_ptrs({q, k, v, q8, k8, v8, q_descale, k_descale, v_descale})) != ATTN_OK)
+    return s;
+  if (cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens must be a non-null, 4-byte aligned device array");
+  if (hadamard_signs && !aligned16(hadamard_signs))
+    return fail(ATTN_ERR_INVALID_ARG, "hadamard_signs not 16-byte aligned");
+  if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
+  if ((s = check_device()) != ATTN_OK) return s;
+  Fp8QuantParams p{{q, k, v}, {q8, k8, v8}, {q_descale, k_descale, v_descale}, hadamard_signs,
+                   B, H, max_seqlen, d, 0, nullptr, nullptr, H_kv, cu_seqlens, total};
+  return launch_fp8_quantize(p, stream);
+}
+
 attn_status_t attn_fp8_quantize_rope(const float* q, const float* k, const float* v,
                                      const float* rope_cos, const float* rope_sin,
                                      const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
@@ -496,6 +519,29 @@ attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* 
                            int d, int causal, float softmax_scale, cudaStream_t stream) {
   return attn_fwd_fp8_gqa(q8, k8, v8, q_descale, k_descale, v_descale, o, lse, B, H, H, N, d,
                           causal, softmax_scale, stream);
+}
+
+attn_status_t attn_fwd_fp8_varlen(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
+                                  const float* q_descale, const float* k_descale,
+                                  const float* v_descale, void* o, float* lse,
+                                  const int* cu_seqlens, int B, int max_seqlen, int total, int H,
+                                  int H_kv, int d, int causal, float softmax_scale,
+                                  cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if ((s = check_packed(B, max_seqlen, total, H, d, causal)) != ATTN_OK) return s;
+  if ((s = check_heads(H, H_kv)) != ATTN_OK) return s;
+  if ((s = check_ptrs({q8, k8, v8, o, lse})) != ATTN_OK) return s;
+  if (!q_descale || !k_descale || !v_descale)
+    return fail(ATTN_ERR_INVALID_ARG, "null descale pointer");
+  if (cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens must be a non-null, 4-byte aligned device array");
+  if ((s = check_scale(softmax_scale)) != ATTN_OK) return s;
+  if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
+  if ((s = check_device()) != ATTN_OK) return s;
+  Fp8FwdParams p{q8, k8, v8, q_descale, k_descale, v_descale, o, lse, B, H, max_seqlen, d, causal,
+                 softmax_scale, H_kv, cu_seqlens, total};
+  return launch_fwd_fp8(p, stream);
 }
 
 attn_status_t attn_fwd_fp8_gqa(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,

@@ -83,6 +83,8 @@ struct Fp8QuantParams {
   const float* rope_cos = nullptr;   // [N, d/2] rotary tables (block mode), or nullptr
   const float* rope_sin = nullptr;
   int H_kv = 0;                      // heads of K and V (0: H)
+  const int* cu_seqlens = nullptr;   // packed batch: device [B + 1] offsets (N = longest)
+  int total = 0;                     // packed batch: tokens
 };
 
 struct Fp8FwdParams {
@@ -98,6 +100,8 @@ struct Fp8FwdParams {
   int causal;
   float scale;
   int H_kv;   // heads of K and V (H % H_kv == 0)
+  const int* cu_seqlens = nullptr;   // packed batch: device [B + 1] offsets (N = longest)
+  int total = 0;                     // packed batch: tokens
 };
 
 attn_status_t launch_fwd(const FwdParams& p, cudaStream_t stream);

@@ -34,15 +34,19 @@ constexpr float kE4m3Max = 448.f;
 
 // ============================================================== pre-pass ====
 // Mode: 0 = fused block mode (amax + quantise), 1 = block amax only (into
-// descale), 2 = quantise with the descale already in place.
-template <int MODE>
+// descale), 2 = quantise with the descale already in place.  PACKED (mode 0):
+// sequences packed back to back, [total, heads, d]; N is the longest sequence
+// and a block is 128 rows of one sequence and head (descale [B, heads,
+// ceil(N / 128)], 1 for blocks past the sequence's end).
+template <int MODE, bool PACKED = false>
 __global__ void __launch_bounds__(256)
     fp8_quant_kernel(const float* __restrict__ src0, const float* __restrict__ src1,
                      const float* __restrict__ src2, uint8_t* __restrict__ dst0,
                      uint8_t* __restrict__ dst1, uint8_t* __restrict__ dst2,
                      float* __restrict__ desc0, float* __restrict__ desc1,
                      float* __restrict__ desc2, const float* __restrict__ signs, int N,
-                     int nblk, int kv_planes) {
+                     int nblk, int kv_planes, const int* __restrict__ cu_seqlens = nullptr,
+                     int total = 0, int heads_q = 0, int heads_kv = 0, int* status = nullptr) {
   constexpr int D = 128;
   const int which = blockIdx.z;
   if (which > 0 && static_cast<int>(blockIdx.y) >= kv_planes) return;   // K, V: B * H_kv planes
@@ -52,6 +56,27 @@ __global__ void __launch_bounds__(256)
   const bool hadamard = signs != nullptr && which < 2;
   const int blk = blockIdx.x;
   const int bh = blockIdx.y;
+  // row r of this (b, h) lies at element row0 + r * rstride; rows r < nrows exist
+  size_t row0 = static_cast<size_t>(bh) * N * D;
+  size_t rstride = D;
+  int nrows = N;
+  if constexpr (PACKED) {
+    const int heads = which == 0 ? heads_q : heads_kv;
+    const int b = bh / heads;
+    const int s0 = cu_seqlens[b];
+    const int end = cu_seqlens[b + 1];
+    if (s0 < 0 || end < s0 || end > total || end - s0 > N) {
+      if (threadIdx.x == 0) atomicCAS(status, 0, kDevBadSeqlens);
+      return;
+    }
+    row0 = (static_cast<size_t>(s0) * heads + bh % heads) * D;
+    rstride = static_cast<size_t>(heads) * D;
+    nrows = end - s0;
+    if (blk * 128 >= nrows) {
+      if (threadIdx.x == 0) desc[static_cast<size_t>(bh) * nblk + blk] = 1.f;
+      return;
+    }
+  }
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   __shared__ float warp_max[8];
@@ -65,7 +90,7 @@ __global__ void __launch_bounds__(256)
   for (int r = 0; r < 16; ++r) {
     const int row = blk * 128 + warp * 16 + r;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row < N) v = reinterpret_cast<const float4*>(src + (static_cast<size_t>(bh) * N + row) * D)[lane];
+    if (row < nrows) v = reinterpret_cast<const float4*>(src + row0 + row * rstride)[lane];
     if (hadamard) {
       v.x *= s4.x; v.y *= s4.y; v.z *= s4.z; v.w *= s4.w;
       // stages of span 1 and 2 inside the lane (columns 4*lane .. 4*lane+3)
@@ -111,11 +136,11 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = blk * 128 + warp * 16 + r;
-    if (row < N) {
+    if (row < nrows) {
       const float4 v = x[r];
       const uint32_t packed = cvt_pack_e4m3x4(__fdiv_rn(v.x, descale), __fdiv_rn(v.y, descale),
                                               __fdiv_rn(v.z, descale), __fdiv_rn(v.w, descale));
-      reinterpret_cast<uint32_t*>(dst + (static_cast<size_t>(bh) * N + row) * D)[lane] = packed;
+      reinterpret_cast<uint32_t*>(dst + row0 + row * rstride)[lane] = packed;
     }
   }
 }
@@ -315,6 +340,8 @@ struct Fp8KParams {
   int nblk;
   float scale_log2;
   int H_kv;   // key/value heads; query head h reads key/value head h / (H / H_kv)
+  const int* cu_seqlens;   // packed batch: device [B + 1] token offsets, else nullptr
+  int total;               // packed batch: tokens (cu_seqlens[B])
 };
 
 __device__ __forceinline__ float lg2_approx8(float x) {
@@ -323,7 +350,11 @@ __device__ __forceinline__ float lg2_approx8(float x) {
   return y;
 }
 
-template <bool CAUSAL>
+// PACKED: a batch of sequences packed back to back -- codes [total, heads, d],
+// descales [B, heads, ceil(max_seqlen / 128)] per sequence's 128-row blocks, O
+// [total, H, d], LSE [H, total]; kp.N is the longest sequence; query and key
+// tiles are read at the sequence's first token by 4-D tensor maps.
+template <bool CAUSAL, bool PACKED>
 __global__ void __launch_bounds__(THREADS8, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Fp8KParams kp) {
@@ -358,7 +389,20 @@ __global__ void __launch_bounds__(THREADS8, 1)
                         : static_cast<int>(blockIdx.z * kp.H + blockIdx.y);
   // key/value plane (and descale row) of this query head
   const int kvp = (bh / kp.H) * kp.H_kv + (bh % kp.H) / (kp.H / kp.H_kv);
-  const int N = kp.N;
+  int N = kp.N;      // this sequence's length
+  int seq0 = 0;      // packed: its first token
+  if constexpr (PACKED) {
+    const int b = bh / kp.H;
+    const int s0 = kp.cu_seqlens[b];
+    const int end = kp.cu_seqlens[b + 1];
+    if (s0 < 0 || end < s0 || end > kp.total || end - s0 > kp.N) {
+      if (threadIdx.x == 0) atomicCAS(kp.status, 0, kDevBadSeqlens);
+      return;
+    }
+    seq0 = s0;
+    N = end - s0;
+    if (g * NQ8 * BM >= N) return;   // the sequence ends before this CTA's query tiles
+  }
   const int nKtot = (N + BN - 1) / BN;
   int nK[NQ8];
   int nKmax = 0;
@@ -409,7 +453,10 @@ __global__ void __launch_bounds__(THREADS8, 1)
       for (int t = 0; t < NQ8; ++t) {
         if (nK[t] == 0) continue;
         mbar_arrive_expect_tx(&q_full[t], TILE8);
-        tma_load_3d(sQ + t * TILE8, &tmQ, &q_full[t], 0, (g * NQ8 + t) * BM, bh);
+        if constexpr (PACKED)
+          tma_load_4d(sQ + t * TILE8, &tmQ, &q_full[t], 0, seq0 + (g * NQ8 + t) * BM, bh % kp.H, 0);
+        else
+          tma_load_3d(sQ + t * TILE8, &tmQ, &q_full[t], 0, (g * NQ8 + t) * BM, bh);
       }
       int it = 0;
       bool ok = true;
@@ -422,7 +469,11 @@ __global__ void __launch_bounds__(THREADS8, 1)
             break;
           }
           mbar_arrive_expect_tx(&kv_full[slot], TILE8);
-          tma_load_3d(sKV + slot * TILE8, kv ? &tmV : &tmK, &kv_full[slot], 0, j * BN, kvp);
+          if constexpr (PACKED)
+            tma_load_4d(sKV + slot * TILE8, kv ? &tmV : &tmK, &kv_full[slot], 0, seq0 + j * BN,
+                        kvp % kp.H_kv, 0);
+          else
+            tma_load_3d(sKV + slot * TILE8, kv ? &tmV : &tmK, &kv_full[slot], 0, j * BN, kvp);
           ++it;
         }
       }
@@ -501,7 +552,7 @@ __global__ void __launch_bounds__(THREADS8, 1)
     const float* kdesc = kp.k_descale + static_cast<size_t>(kvp) * kp.nblk;
     const float* vdesc = kp.v_descale + static_cast<size_t>(kvp) * kp.nblk;
     float dv_max = 0.f;
-    for (int b = 0; b < kp.nblk; ++b) dv_max = fmaxf(dv_max, vdesc[b]);
+    for (int b = 0; b < (N + BN - 1) / BN; ++b) dv_max = fmaxf(dv_max, vdesc[b]);
     const float c_q = (my_nK > 0) ? kp.scale_log2 * kp.q_descale[static_cast<size_t>(bh) * kp.nblk + qt] : 0.f;
     float m_ref = -INFINITY;   // in log2 units of the scaled scores
     float l = 0.f;             // this half's share of the row sum
@@ -611,8 +662,9 @@ __global__ void __launch_bounds__(THREADS8, 1)
       named_bar_sync(pair_bar, 64);
       const float l_row = l + xch[my_nK & 1][t][h ^ 1][r];
       const float mul = dv_max / l_row;
-      uint16_t* orow = static_cast<uint16_t*>(kp.o) + (static_cast<size_t>(bh) * N + row_g) * D8 +
-                       (D8 / 2) * h;
+      const size_t orow_idx = PACKED ? static_cast<size_t>(seq0 + row_g) * kp.H + bh % kp.H
+                                     : static_cast<size_t>(bh) * N + row_g;
+      uint16_t* orow = static_cast<uint16_t*>(kp.o) + orow_idx * D8 + (D8 / 2) * h;
 #pragma unroll 1
       for (int c0 = 0; c0 < D8 / 64; ++c0) {
         uint32_t o[32];
@@ -630,7 +682,9 @@ __global__ void __launch_bounds__(THREADS8, 1)
         }
       }
       if (h == 0 && row_g < N)
-        kp.lse[static_cast<size_t>(bh) * N + row_g] = (m_ref + lg2_approx8(l_row)) * 0.69314718055994530942f;
+        kp.lse[PACKED ? static_cast<size_t>(bh % kp.H) * kp.total + seq0 + row_g
+                      : static_cast<size_t>(bh) * N + row_g] =
+            (m_ref + lg2_approx8(l_row)) * 0.69314718055994530942f;
     }
   }
 
@@ -667,7 +721,15 @@ attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) 
   const int H_kv = p.H_kv > 0 ? p.H_kv : p.H;
   const int kv_planes = p.B * H_kv;
   dim3 grid(nblk, p.B * p.H, 3);
-  if (p.rope_cos) {
+  if (p.cu_seqlens) {
+    if (p.rope_cos || p.per_tensor)
+      return fail(ATTN_ERR_UNSUPPORTED, "packed batches take the block pre-pass only");
+    int* status = device_status_word();
+    if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
+    fp8_quant_kernel<0, true><<<grid, 256, 0, stream>>>(
+        p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1], p.dst[2], p.descale[0], p.descale[1],
+        p.descale[2], p.signs, p.N, nblk, kv_planes, p.cu_seqlens, p.total, p.H, H_kv, status);
+  } else if (p.rope_cos) {
     int* status = device_status_word();
     if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
     auto kern = fp8_quant_staged_kernel<0, true>;
@@ -696,21 +758,35 @@ attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) 
   return ATTN_OK;
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool PACKED>
 attn_status_t launch_fwd_fp8_t(const Fp8FwdParams& p, cudaStream_t stream) {
-  auto kern = fwd_fp8_kernel<CAUSAL>;
+  auto kern = fwd_fp8_kernel<CAUSAL, PACKED>;
   attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), SMEM8);
   if (s != ATTN_OK) return s;
   CUtensorMap tq, tk, tv;
-  const uint64_t planes = static_cast<uint64_t>(p.B) * p.H;
-  const uint64_t kv_planes = static_cast<uint64_t>(p.B) * p.H_kv;
-  if ((s = make_tmap_3d(&tq, p.q8, 1, D8, p.N, planes, 128, BM)) != ATTN_OK) return s;
-  if ((s = make_tmap_3d(&tk, p.k8, 1, D8, p.N, kv_planes, 128, BN)) != ATTN_OK) return s;
-  if ((s = make_tmap_3d(&tv, p.v8, 1, D8, p.N, kv_planes, 128, BN)) != ATTN_OK) return s;
+  if constexpr (PACKED) {
+    // {d, total tokens, heads, 1}: token stride heads * d bytes, head stride d
+    const uint64_t T = static_cast<uint64_t>(p.total);
+    if ((s = make_tmap_4d(&tq, p.q8, 1, D8, T, p.H, 1, 1ull * p.H * D8, D8, T * p.H * D8, 128,
+                          BM)) != ATTN_OK)
+      return s;
+    if ((s = make_tmap_4d(&tk, p.k8, 1, D8, T, p.H_kv, 1, 1ull * p.H_kv * D8, D8, T * p.H_kv * D8,
+                          128, BN)) != ATTN_OK)
+      return s;
+    if ((s = make_tmap_4d(&tv, p.v8, 1, D8, T, p.H_kv, 1, 1ull * p.H_kv * D8, D8, T * p.H_kv * D8,
+                          128, BN)) != ATTN_OK)
+      return s;
+  } else {
+    const uint64_t planes = static_cast<uint64_t>(p.B) * p.H;
+    const uint64_t kv_planes = static_cast<uint64_t>(p.B) * p.H_kv;
+    if ((s = make_tmap_3d(&tq, p.q8, 1, D8, p.N, planes, 128, BM)) != ATTN_OK) return s;
+    if ((s = make_tmap_3d(&tk, p.k8, 1, D8, p.N, kv_planes, 128, BN)) != ATTN_OK) return s;
+    if ((s = make_tmap_3d(&tv, p.v8, 1, D8, p.N, kv_planes, 128, BN)) != ATTN_OK) return s;
+  }
   int* status = device_status_word();
   if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
   Fp8KParams kp{p.q_descale, p.k_descale, p.v_descale, p.o, p.lse, status, p.N, p.H,
-                (p.N + 127) / 128, p.scale * 1.4426950408889634f, p.H_kv};
+                (p.N + 127) / 128, p.scale * 1.4426950408889634f, p.H_kv, p.cu_seqlens, p.total};
   const unsigned npairs = static_cast<unsigned>((p.N + BM * NQ8 - 1) / (BM * NQ8));
   const dim3 grid = CAUSAL ? dim3(npairs * p.H * p.B, 1, 1) : dim3(npairs, p.H, p.B);
   kern<<<grid, THREADS8, SMEM8, stream>>>(tq, tk, tv, kp);
@@ -723,7 +799,9 @@ attn_status_t launch_fwd_fp8(const Fp8FwdParams& p, cudaStream_t stream) {
   if (p.d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
   if (p.N > 65535 * 256 || p.H > 65535 || p.B > 65535)
     return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
-  return p.causal ? launch_fwd_fp8_t<true>(p, stream) : launch_fwd_fp8_t<false>(p, stream);
+  if (p.cu_seqlens)
+    return p.causal ? launch_fwd_fp8_t<true, true>(p, stream) : launch_fwd_fp8_t<false, true>(p, stream);
+  return p.causal ? launch_fwd_fp8_t<true, false>(p, stream) : launch_fwd_fp8_t<false, false>(p, stream);
 }
 
 }  // namespace attn

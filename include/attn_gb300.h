@@ -332,6 +332,28 @@ attn_status_t attn_fp8_quantize_gqa(const float* q, const float* k, const float*
                                     int per_tensor, cudaStream_t stream);
 
 /*
+ * attn_fp8_quantize_varlen -- the block pre-pass (attn_fp8_quantize_gqa) for a
+ * packed batch of B sequences stored back to back (the layout of
+ * attn_fwd_varlen).
+ *   q : [total, H, d] float32;  k, v : [total, H_kv, d] float32;  d = 128.
+ *   q8, k8, v8 : the same shapes, e4m3 bytes (written).
+ *   q_descale : [B, H, ceil(max_seqlen/128)];  k_descale, v_descale :
+ *               [B, H_kv, ceil(max_seqlen/128)] float32 (written): a block is
+ *               128 consecutive tokens of one sequence and head, starting at the
+ *               sequence's first token; entries past a sequence's end hold 1.
+ *   cu_seqlens : DEVICE int32 [B + 1] (as attn_fwd_varlen).
+ * Block mode only (no per-tensor mode, no rotary embedding).  Offsets that are
+ * not increasing, run past `total` or hold a sequence longer than max_seqlen
+ * are reported by attn_get_device_status() as ATTN_ERR_INVALID_ARG.
+ */
+attn_status_t attn_fp8_quantize_varlen(const float* q, const float* k, const float* v,
+                                       const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                       uint8_t* v8, float* q_descale, float* k_descale,
+                                       float* v_descale, const int* cu_seqlens, int B,
+                                       int max_seqlen, int total, int H, int H_kv, int d,
+                                       cudaStream_t stream);
+
+/*
  * attn_fp8_quantize_rope -- attn_fp8_quantize (block mode) with the rotary
  * position embedding of Q and K fused in front of the Hadamard transform
  * ("FlashAttention-3: Hopper Asynchrony and FP8 Attention", section "FP8
@@ -364,6 +386,24 @@ attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* 
                            const float* q_descale, const float* k_descale,
                            const float* v_descale, void* o, float* lse, int B, int H, int N,
                            int d, int causal, float softmax_scale, cudaStream_t stream);
+
+/*
+ * attn_fwd_fp8_varlen -- FP8 forward on a packed batch (the output of
+ * attn_fp8_quantize_varlen), grouped-query heads allowed.
+ *   q8 : [total, H, d];  k8, v8 : [total, H_kv, d] e4m3;  descales as
+ *   attn_fp8_quantize_varlen writes them;  o : [total, H, d] bfloat16;
+ *   lse : [H, total] float32;  other arguments and errors as attn_fwd_varlen.
+ * Source: the FP8 forward of "FlashAttention-3: Hopper Asynchrony and FP8
+ * Attention" over the variable-length batches that "FlashAttention 3 Hardware
+ * Acceleration: ...", section "GPU Compatibility and Enablement Matrix", lists
+ * as forthcoming (as attn_fwd_varlen).
+ */
+attn_status_t attn_fwd_fp8_varlen(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
+                                  const float* q_descale, const float* k_descale,
+                                  const float* v_descale, void* o, float* lse,
+                                  const int* cu_seqlens, int B, int max_seqlen, int total, int H,
+                                  int H_kv, int d, int causal, float softmax_scale,
+                                  cudaStream_t stream);
 
 /*
  * attn_fwd_fp8_gqa -- attn_fwd_fp8 with grouped-query heads: query head h of

@@ -218,3 +218,17 @@ def test_fp8_gqa_is_declared_and_validates(lib):
         assert code == 1 and why.encode() in lib.attn_last_error()
     assert lib.attn_fwd_fp8_gqa(16, 16, 16, 16, 16, 16, 16, 16, 1, 4, 2, 256, 64, 0, 0.1,
                                 None) == 2                     # d = 128 only
+
+
+def test_fp8_varlen_is_declared_and_validates(lib):
+    names = declared_functions()
+    assert "attn_fp8_quantize_varlen" in names and "attn_fwd_fp8_varlen" in names
+    # (cu_seqlens, B, max_seqlen, total, H, H_kv, d)
+    for args, code, why in (((None, 2, 100, 200, 4, 2, 128), 1, "cu_seqlens"),
+                            ((16, 2, 100, 200, 4, 3, 128), 1, "H_kv"),
+                            ((16, 0, 100, 200, 4, 2, 128), 1, ">= 1"),
+                            ((16, 2, 100, 200, 4, 2, 64), 2, "d = 128")):
+        got = lib.attn_fwd_fp8_varlen(16, 16, 16, 16, 16, 16, 16, 16, *args, 0, 0.1, None)
+        assert got == code and why.encode() in lib.attn_last_error(), (args, lib.attn_last_error())
+        got = lib.attn_fp8_quantize_varlen(16, 16, 16, None, 16, 16, 16, 16, 16, 16, *args, None)
+        assert got == code and why.encode() in lib.attn_last_error(), (args, lib.attn_last_error())
