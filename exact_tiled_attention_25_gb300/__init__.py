@@ -34,6 +34,7 @@ __all__ = ["AttnError", "attn_fwd", "attn_fwd_gqa", "attn_fwd_varlen", "attn_bwd
            "attn_bwd_workspace_size",
            "attn_fp8_quantize", "attn_fp8_quantize_gqa", "attn_fp8_quantize_rope", "attn_fwd_fp8",
            "attn_fwd_fp8_gqa", "attn_fp8_quantize_varlen", "attn_fwd_fp8_varlen",
+           "attn_fp8_quantize_bf16",
            "attn_decode_paged", "attn_decode_paged_fp8", "attn_decode_workspace_size",
            "attn_get_device_status",
            "attn_status_string", "attn_last_error", "load_library"]
@@ -599,3 +600,32 @@ def attn_fwd_fp8_varlen(q8, k8, v8, q_descale, k_descale, v_descale, cu_seqlens,
     if host:
         return o.cpu(), lse.cpu()
     return o, lse
+
+
+def attn_fp8_quantize_bf16(q, k, v, hadamard_signs=None, per_tensor: bool = False, stream=None):
+    """The pre-pass on bfloat16 q [B, H, N, d] and k, v [B, H_kv, N, d]:
+    e4m3 codes (q8, k8, v8) and float32 block descales."""
+    lib = _lib.load()
+    ins = [q, k, v] + ([hadamard_signs] if hadamard_signs is not None else [])
+    ins, host = _to_device(ins)
+    q, k, v = ins[:3]
+    signs = ins[3] if hadamard_signs is not None else None
+    B, H, N, d = _shape4(q, "q")
+    _, Hkv, _, _ = _shape4(k, "k")
+    for t, n in ((k, "k"), (v, "v")):
+        if _shape4(t, n) != (B, Hkv, N, d):
+            raise ValueError("k and v must be [B, H_kv, N, d] with q's B, N, d")
+    if any(t.dtype != torch.bfloat16 for t in (q, k, v)):
+        raise ValueError("inputs must be bfloat16")
+    if signs is not None and (signs.dtype != torch.float32 or signs.numel() != d):
+        raise ValueError("hadamard_signs must be d float32 values")
+    nblk = (N + 127) // 128
+    outs = [torch.empty((B, h, N, d), dtype=torch.uint8, device=q.device) for h in (H, Hkv, Hkv)]
+    desc = [torch.empty((B, h, nblk), dtype=torch.float32, device=q.device) for h in (H, Hkv, Hkv)]
+    code = lib.attn_fp8_quantize_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(signs),
+                                      *[_ptr(t) for t in outs], *[_ptr(t) for t in desc],
+                                      B, H, Hkv, N, d, int(bool(per_tensor)), _stream(stream))
+    _check(code, "attn_fp8_quantize_bf16")
+    if host:
+        return tuple(t.cpu() for t in outs), tuple(t.cpu() for t in desc)
+    return tuple(outs), tuple(desc)

@@ -344,11 +344,36 @@ attn_status_t attn_fp8_quantize(const float* q, const float* k, const float* v,
                                v_descale, B, H, H, N, d, per_tensor, stream);
 }
 
+// Shared by the fixed-length pre-pass entry points (float32 or bfloat16 inputs).
+static attn_status_t fp8_quantize_common(const void* q, const void* k, const void* v,
+                                         const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                         uint8_t* v8, float* q_descale, float* k_descale,
+                                         float* v_descale, int B, int H, int H_kv, int N, int d,
+                                         int per_tensor, int in_bf16, cudaStream_t stream);
+
 attn_status_t attn_fp8_quantize_gqa(const float* q, const float* k, const float* v,
                                     const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
                                     uint8_t* v8, float* q_descale, float* k_descale,
                                     float* v_descale, int B, int H, int H_kv, int N, int d,
                                     int per_tensor, cudaStream_t stream) {
+  return fp8_quantize_common(q, k, v, hadamard_signs, q8, k8, v8, q_descale, k_descale, v_descale,
+                             B, H, H_kv, N, d, per_tensor, 0, stream);
+}
+
+attn_status_t attn_fp8_quantize_bf16(const void* q, const void* k, const void* v,
+                                     const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                     uint8_t* v8, float* q_descale, float* k_descale,
+                                     float* v_descale, int B, int H, int H_kv, int N, int d,
+                                     int per_tensor, cudaStream_t stream) {
+  return fp8_quantize_common(q, k, v, hadamard_signs, q8, k8, v8, q_descale, k_descale, v_descale,
+                             B, H, H_kv, N, d, per_tensor, 1, stream);
+}
+
+static attn_status_t fp8_quantize_common(const void* q, const void* k, const void* v,
+                                         const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                         uint8_t* v8, float* q_descale, float* k_descale,
+                                         float* v_descale, int B, int H, int H_kv, int N, int d,
+                                         int per_tensor, int in_bf16, cudaStream_t stream) {
   g_last_error.clear();
   attn_status_t s;
   if ((s = check_shape(B, H, N, d, 0)) != ATTN_OK) return s;
@@ -364,7 +389,7 @@ attn_status_t attn_fp8_quantize_gqa(const float* q, const float* k, const float*
   if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
   if ((s = check_device()) != ATTN_OK) return s;
   Fp8QuantParams p{{q, k, v}, {q8, k8, v8}, {q_descale, k_descale, v_descale}, hadamard_signs,
-                   B, H, N, d, per_tensor, nullptr, nullptr, H_kv};
+                   B, H, N, d, per_tensor, nullptr, nullptr, H_kv, nullptr, 0, in_bf16};
   return launch_fp8_quantize(p, stream);
 }
 

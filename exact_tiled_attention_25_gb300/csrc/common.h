@@ -74,7 +74,7 @@ struct BwdParams {
 };
 
 struct Fp8QuantParams {
-  const float* src[3];
+  const void* src[3];                // float32, or bfloat16 when in_bf16
   uint8_t* dst[3];
   float* descale[3];
   const float* signs;
@@ -85,6 +85,7 @@ struct Fp8QuantParams {
   int H_kv = 0;                      // heads of K and V (0: H)
   const int* cu_seqlens = nullptr;   // packed batch: device [B + 1] offsets (N = longest)
   int total = 0;                     // packed batch: tokens
+  int in_bf16 = 0;                   // inputs are bfloat16 (block and per-tensor modes)
 };
 
 struct Fp8FwdParams {

@@ -726,16 +726,11 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
       for (int i = 0; i < D; ++i) am[i & 3] = fmaxf(am[i & 3], fabsf(x[i]));
       const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
       // descale = amax / 448 and code = e4m3(x / descale) with x / descale
-      // rounded as an IEEE float32 division (the block quantiser's rule).
-      // One division gives y = RN(1 / dq); each quotient is then
-      // q0 = RN(x y) corrected by one step of Markstein's method (P. Markstein,
-      // IBM J. Res. Dev. 34(1), 1990): r = x - dq q0 exactly by FMA, q = RN(q0 + r y).
+      // rounded as an IEEE float32 division (the block quantiser's rule): one
+      // division for y = RN(1 / dq), then a corrected product per value.
       const float dq = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
       const float y = __fdiv_rn(1.f, dq);
-      auto quot = [&](float v) -> float {
-        const float q0 = v * y;
-        return fmaf(fmaf(-dq, q0, v), y, q0);
-      };
+      auto quot = [&](float v) -> float { return div_by_recip(v, dq, y); };
       c_q = kp.scale_log2 * dq;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {

@@ -38,10 +38,11 @@ constexpr float kE4m3Max = 448.f;
 // sequences packed back to back, [total, heads, d]; N is the longest sequence
 // and a block is 128 rows of one sequence and head (descale [B, heads,
 // ceil(N / 128)], 1 for blocks past the sequence's end).
-template <int MODE, bool PACKED = false>
+// BF16IN: the inputs are bfloat16 (widened exactly to float32 on load).
+template <int MODE, bool PACKED = false, bool BF16IN = false>
 __global__ void __launch_bounds__(256)
-    fp8_quant_kernel(const float* __restrict__ src0, const float* __restrict__ src1,
-                     const float* __restrict__ src2, uint8_t* __restrict__ dst0,
+    fp8_quant_kernel(const void* __restrict__ src0, const void* __restrict__ src1,
+                     const void* __restrict__ src2, uint8_t* __restrict__ dst0,
                      uint8_t* __restrict__ dst1, uint8_t* __restrict__ dst2,
                      float* __restrict__ desc0, float* __restrict__ desc1,
                      float* __restrict__ desc2, const float* __restrict__ signs, int N,
@@ -50,7 +51,7 @@ __global__ void __launch_bounds__(256)
   constexpr int D = 128;
   const int which = blockIdx.z;
   if (which > 0 && static_cast<int>(blockIdx.y) >= kv_planes) return;   // K, V: B * H_kv planes
-  const float* src = which == 0 ? src0 : (which == 1 ? src1 : src2);
+  const void* src = which == 0 ? src0 : (which == 1 ? src1 : src2);
   uint8_t* dst = which == 0 ? dst0 : (which == 1 ? dst1 : dst2);
   float* desc = which == 0 ? desc0 : (which == 1 ? desc1 : desc2);
   const bool hadamard = signs != nullptr && which < 2;
@@ -90,7 +91,17 @@ __global__ void __launch_bounds__(256)
   for (int r = 0; r < 16; ++r) {
     const int row = blk * 128 + warp * 16 + r;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row < nrows) v = reinterpret_cast<const float4*>(src + row0 + row * rstride)[lane];
+    if (row < nrows) {
+      if constexpr (BF16IN) {
+        // four bfloat16 values; each is the upper half of its float32
+        const uint2 w = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(src) + row0 +
+                                                        row * rstride)[lane];
+        v = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                        __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+      } else {
+        v = reinterpret_cast<const float4*>(static_cast<const float*>(src) + row0 + row * rstride)[lane];
+      }
+    }
     if (hadamard) {
       v.x *= s4.x; v.y *= s4.y; v.z *= s4.z; v.w *= s4.w;
       // stages of span 1 and 2 inside the lane (columns 4*lane .. 4*lane+3)
@@ -133,13 +144,15 @@ __global__ void __launch_bounds__(256)
     descale = bmax > 0.f ? __fdiv_rn(bmax, kE4m3Max) : 1.f;
     if (threadIdx.x == 0) desc[static_cast<size_t>(bh) * nblk + blk] = descale;
   }
+  // code = e4m3(x / descale), the quotient rounded as an IEEE division would
+  const float rdesc = __fdiv_rn(1.f, descale);
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = blk * 128 + warp * 16 + r;
     if (row < nrows) {
       const float4 v = x[r];
-      const uint32_t packed = cvt_pack_e4m3x4(__fdiv_rn(v.x, descale), __fdiv_rn(v.y, descale),
-                                              __fdiv_rn(v.z, descale), __fdiv_rn(v.w, descale));
+      const uint32_t packed = cvt_pack_e4m3x4(div_by_recip(v.x, descale, rdesc), div_by_recip(v.y, descale, rdesc),
+                                              div_by_recip(v.z, descale, rdesc), div_by_recip(v.w, descale, rdesc));
       reinterpret_cast<uint32_t*>(dst + row0 + row * rstride)[lane] = packed;
     }
   }
@@ -273,13 +286,14 @@ __global__ void __launch_bounds__(256)
     descale = bmax > 0.f ? __fdiv_rn(bmax, kE4m3Max) : 1.f;
     if (threadIdx.x == 0) desc[static_cast<size_t>(bh) * nblk + blk] = descale;
   }
+  const float rdesc = __fdiv_rn(1.f, descale);
 #pragma unroll 4
   for (int r = 0; r < 16; ++r) {
     const int lr = warp * 16 + r;
     if (lr >= rows) break;
     const float4 v = reinterpret_cast<const float4*>(sblk + lr * D)[lane];
-    const uint32_t packed = cvt_pack_e4m3x4(__fdiv_rn(v.x, descale), __fdiv_rn(v.y, descale),
-                                            __fdiv_rn(v.z, descale), __fdiv_rn(v.w, descale));
+    const uint32_t packed = cvt_pack_e4m3x4(div_by_recip(v.x, descale, rdesc), div_by_recip(v.y, descale, rdesc),
+                                            div_by_recip(v.z, descale, rdesc), div_by_recip(v.w, descale, rdesc));
     reinterpret_cast<uint32_t*>(dst + (static_cast<size_t>(bh) * N + blk * QROWS + lr) * D)[lane] = packed;
   }
 }
@@ -711,6 +725,27 @@ __global__ void __launch_bounds__(THREADS8, 1)
   }
 }
 
+// Block mode, or the per-tensor comparator (block amaxes, one reduction, codes).
+template <bool BF16IN>
+void launch_quant_modes(const Fp8QuantParams& p, dim3 grid, int nblk, int kv_planes,
+                        cudaStream_t stream) {
+  if (!p.per_tensor) {
+    fp8_quant_kernel<0, false, BF16IN><<<grid, 256, 0, stream>>>(
+        p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1], p.dst[2], p.descale[0], p.descale[1],
+        p.descale[2], p.signs, p.N, nblk, kv_planes);
+    return;
+  }
+  fp8_quant_kernel<1, false, BF16IN><<<grid, 256, 0, stream>>>(
+      p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1], p.dst[2], p.descale[0], p.descale[1],
+      p.descale[2], nullptr, p.N, nblk, kv_planes);
+  fp8_tensor_scale_kernel<<<3, 256, 0, stream>>>(p.descale[0], p.descale[1], p.descale[2],
+                                                 static_cast<long long>(p.B) * p.H * nblk,
+                                                 static_cast<long long>(kv_planes) * nblk);
+  fp8_quant_kernel<2, false, BF16IN><<<grid, 256, 0, stream>>>(
+      p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1], p.dst[2], p.descale[0], p.descale[1],
+      p.descale[2], nullptr, p.N, nblk, kv_planes);
+}
+
 }  // namespace
 
 attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) {
@@ -721,6 +756,8 @@ attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) 
   const int H_kv = p.H_kv > 0 ? p.H_kv : p.H;
   const int kv_planes = p.B * H_kv;
   dim3 grid(nblk, p.B * p.H, 3);
+  if ((p.cu_seqlens || p.rope_cos) && p.in_bf16)
+    return fail(ATTN_ERR_UNSUPPORTED, "bfloat16 inputs take the fixed-length pre-pass without rotation");
   if (p.cu_seqlens) {
     if (p.rope_cos || p.per_tensor)
       return fail(ATTN_ERR_UNSUPPORTED, "packed batches take the block pre-pass only");
@@ -735,23 +772,14 @@ attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) 
     auto kern = fp8_quant_staged_kernel<0, true>;
     attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), QSMEM);
     if (s != ATTN_OK) return s;
-    kern<<<grid, 256, QSMEM, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1], p.dst[2],
+    kern<<<grid, 256, QSMEM, stream>>>(static_cast<const float*>(p.src[0]), static_cast<const float*>(p.src[1]),
+                                       static_cast<const float*>(p.src[2]), p.dst[0], p.dst[1], p.dst[2],
                                        p.descale[0], p.descale[1], p.descale[2], p.signs, p.N,
                                        nblk, kv_planes, status, p.rope_cos, p.rope_sin);
-  } else if (!p.per_tensor) {
-    fp8_quant_kernel<0><<<grid, 256, 0, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1],
-                                                  p.dst[2], p.descale[0], p.descale[1],
-                                                  p.descale[2], p.signs, p.N, nblk, kv_planes);
+  } else if (p.in_bf16) {
+    launch_quant_modes<true>(p, grid, nblk, kv_planes, stream);
   } else {
-    fp8_quant_kernel<1><<<grid, 256, 0, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1],
-                                                  p.dst[2], p.descale[0], p.descale[1],
-                                                  p.descale[2], nullptr, p.N, nblk, kv_planes);
-    fp8_tensor_scale_kernel<<<3, 256, 0, stream>>>(p.descale[0], p.descale[1], p.descale[2],
-                                                   static_cast<long long>(p.B) * p.H * nblk,
-                                                   static_cast<long long>(kv_planes) * nblk);
-    fp8_quant_kernel<2><<<grid, 256, 0, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1],
-                                                  p.dst[2], p.descale[0], p.descale[1],
-                                                  p.descale[2], nullptr, p.N, nblk, kv_planes);
+    launch_quant_modes<false>(p, grid, nblk, kv_planes, stream);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "FP8 pre-pass launch");

@@ -428,6 +428,17 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// x / b rounded as an IEEE float32 division rounds it, given y = RN(1 / b) (one
+// IEEE division per divisor): q0 = RN(x y), the residual r = x - b q0 exactly by
+// FMA, q = RN(q0 + r y) -- one correction step of Markstein's method (P.
+// Markstein, IBM J. Res. Dev. 34(1), 1990), correctly rounded for a normal
+// divisor and a normal quotient.  Used where a quantiser divides many values by
+// one descale.
+__device__ __forceinline__ float div_by_recip(float x, float b, float y) {
+  const float q0 = x * y;
+  return fmaf(fmaf(-b, q0, x), y, q0);
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float m;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));

@@ -332,6 +332,19 @@ attn_status_t attn_fp8_quantize_gqa(const float* q, const float* k, const float*
                                     int per_tensor, cudaStream_t stream);
 
 /*
+ * attn_fp8_quantize_bf16 -- attn_fp8_quantize_gqa on bfloat16 inputs: q
+ * [B, H, N, d], k and v [B, H_kv, N, d] bfloat16 (each value widened exactly to
+ * float32, then transformed and quantised as there); the same outputs, modes
+ * and errors.  This is the pre-pass for activations held in bfloat16, e.g. the
+ * very tensors the BF16 forward reads.
+ */
+attn_status_t attn_fp8_quantize_bf16(const void* q, const void* k, const void* v,
+                                     const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                     uint8_t* v8, float* q_descale, float* k_descale,
+                                     float* v_descale, int B, int H, int H_kv, int N, int d,
+                                     int per_tensor, cudaStream_t stream);
+
+/*
  * attn_fp8_quantize_varlen -- the block pre-pass (attn_fp8_quantize_gqa) for a
  * packed batch of B sequences stored back to back (the layout of
  * attn_fwd_varlen).

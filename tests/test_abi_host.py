@@ -232,3 +232,13 @@ def test_fp8_varlen_is_declared_and_validates(lib):
         assert got == code and why.encode() in lib.attn_last_error(), (args, lib.attn_last_error())
         got = lib.attn_fp8_quantize_varlen(16, 16, 16, None, 16, 16, 16, 16, 16, 16, *args, None)
         assert got == code and why.encode() in lib.attn_last_error(), (args, lib.attn_last_error())
+
+
+def test_fp8_bf16_prepass_is_declared_and_validates(lib):
+    assert "attn_fp8_quantize_bf16" in declared_functions()
+    code = lib.attn_fp8_quantize_bf16(16, 16, 16, None, 16, 16, 16, 16, 16, 16, 1, 4, 3, 256, 128,
+                                      0, None)
+    assert code == 1 and b"H_kv" in lib.attn_last_error()
+    code = lib.attn_fp8_quantize_bf16(16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 4, 2, 256, 128,
+                                      1, None)
+    assert code == 1 and b"Hadamard" in lib.attn_last_error()

@@ -156,3 +156,55 @@ def test_fp8_forward_with_rope_matches_rotated_attention(attn):
     ref_o, _ = oracle.attention_forward(rq, rk, v, 1 / np.sqrt(d), True)
     err = o.float().cpu().numpy() - ref_o
     assert np.sqrt(np.mean(err ** 2)) <= FP8_RMSE
+
+
+def _bf16_inputs(seed, shapes):
+    """Seeded float32 arrays rounded to bfloat16: torch tensors and their exact
+    float32 values."""
+    xs = [workloads.round_to(x, "bf16") for x in
+          (workloads.normal_with_outliers(seed + i, s, 1) for i, s in enumerate(shapes))]
+    return xs, [x.float().numpy() for x in xs]
+
+
+@pytest.mark.parametrize("H_kv", [4, 2])
+@pytest.mark.parametrize("per_tensor", [False, True])
+def test_bf16_quantiser_bit_exact(attn, H_kv, per_tensor):
+    """bfloat16 inputs are quantised exactly as their float32 values are."""
+    ts, xs = _bf16_inputs(31, [(2, 4, 300, 128), (2, H_kv, 300, 128), (2, H_kv, 300, 128)])
+    codes, desc = attn.attn_fp8_quantize_bf16(*(t.to(dev()) for t in ts), per_tensor=per_tensor)
+    check_status(attn)
+    for x, c, d in zip(xs, codes, desc):
+        rc, rd = oracle.quantize_e4m3_blocks(x, per_tensor=per_tensor)
+        np.testing.assert_array_equal(d.cpu().numpy(), rd)
+        np.testing.assert_array_equal(c.cpu().numpy(), rc)
+
+
+def test_bf16_prepass_matches_float32_prepass(attn):
+    """With the transform, the bfloat16 pre-pass gives the float32 pre-pass's bits
+    on the same values (both widen to float32 before the transform)."""
+    ts, xs = _bf16_inputs(32, [(1, 4, 700, 128)] * 3)
+    signs = torch.from_numpy(workloads.random_signs(5, 128)).to(dev())
+    a = attn.attn_fp8_quantize_bf16(*(t.to(dev()) for t in ts), hadamard_signs=signs)
+    b = attn.attn_fp8_quantize(*(torch.from_numpy(x).to(dev()) for x in xs), hadamard_signs=signs)
+    check_status(attn)
+    for ta, tb in zip(a[0] + a[1], b[0] + b[1]):
+        assert torch.equal(ta, tb)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_prepass_forward_matches_dequantised_oracle(attn, causal):
+    ts, xs = _bf16_inputs(33, [(1, 2, 384, 128)] * 3)
+    signs = workloads.random_signs(6, 128)
+    (q8, k8, v8), (qd, kd, vd) = attn.attn_fp8_quantize_bf16(
+        *(t.to(dev()) for t in ts), hadamard_signs=torch.from_numpy(signs).to(dev()))
+    o, lse = attn.attn_fwd_fp8(q8, k8, v8, qd, kd, vd, causal=causal, softmax_scale=1 / np.sqrt(128))
+    check_status(attn)
+    deq = [oracle.dequantize_e4m3_blocks(c.cpu().numpy(), s.cpu().numpy())
+           for c, s in ((q8, qd), (k8, kd), (v8, vd))]
+    ref_o, ref_l = oracle.attention_forward(*deq, 1 / np.sqrt(128), causal)
+    diff = o.float().cpu().numpy() - ref_o
+    assert np.sqrt(np.mean(diff ** 2)) <= 1e-2 * max(1.0, np.sqrt(np.mean(ref_o ** 2)))
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=2e-3)
+    # total error against exact attention of the bfloat16 inputs
+    exact, _ = oracle.attention_forward(*(x.astype(np.float64) for x in xs), 1 / np.sqrt(128), causal)
+    assert np.sqrt(np.mean((o.float().cpu().numpy() - exact) ** 2)) <= FP8_RMSE
