@@ -42,8 +42,8 @@ WORKLOAD = "attention step (bf16 fwd + bf16 bwd + fp8 pre-pass + fp8 fwd), B=2 H
 NCU_TRAFFIC = {
     "fwd_bf16": 247_067_648,      # fwd_kernel: 201.7 MB read + 45.4 MB write
     "bwd_bf16": 627_049_728,      # bwd_main_kernel: 405.1 MB read + 221.9 MB write
-    "fwd_fp8": None,              # fwd_fp8_kernel changed since its last capture
-    "fp8_prepass": None,          # fp8_quant_kernel now reads bfloat16; not yet captured
+    "fwd_fp8": 133_292_800,       # fwd_fp8_kernel: 100.9 MB read + 32.4 MB write
+    "fp8_prepass": 271_258_624,   # fp8_quant_kernel (bf16 in): 201.4 MB read + 69.9 MB write
 }
 KERNEL_OF = {"fwd_bf16": "fwd_kernel", "bwd_bf16": "bwd_main_kernel (timed as the whole attn_bwd call)",
              "fwd_fp8": "fwd_fp8_kernel", "fp8_prepass": "fp8_quant_kernel"}
