@@ -816,7 +816,7 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
       // error; the running maximum of a decode row rises on few tiles, so the
       // extra O rescales cost little.
       const float m_new = fmaxf(m_ref, mt);
-      const bool need = (m_new - m_ref) > 8.f;   // EXPERIMENT lazy
+      const bool need = m_new > m_ref;
       float alpha = 1.f;
       if (need) {
         alpha = ex2_approx(m_ref - m_new);
