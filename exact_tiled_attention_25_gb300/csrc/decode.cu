@@ -90,9 +90,9 @@ __device__ __forceinline__ float lg2_dec(float x) {
 // next window is read while the current one is in use: no table read waits in
 // front of a copy.  When a window comes into use its entries are checked and,
 // for an e4m3 cache, the descales of its pages are prefetched into L2 for the
-// softmax warps.  Lane 0 waits for free ring slots; lanes 0 .. nbox-1 issue
-// the copies of a tile's boxes together; the keys and values of a tile use the
-// same pages.  Item i (K_j = 2j, V_j = 2j + 1)
+// softmax warps.  Lane 0 waits for free ring slots; one lane per (box, 64-column
+// chunk) issues the tile's copies together; the keys and values of a tile use
+// the same pages.  Item i (K_j = 2j, V_j = 2j + 1)
 // goes to ring slot (i + SHIFT) % NSLOT: the first SHIFT slots may start out
 // holding other data, released through their empty barrier like a used slot.
 template <int NSLOT, int CH, int CHUNK, int TILE, int SHIFT>
@@ -150,16 +150,16 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap* tmK, const CUt
         ok = false;
         break;
       }
-      // lane x < nbox issues box x (one instruction for all boxes of the tile;
-      // lane 0 registered the expected bytes above, before any lane issues)
+      // lane x * CH + c issues column chunk c of box x (one instruction for the
+      // whole tile; lane 0 registered the expected bytes above, before any lane
+      // issues); nbox * CH <= 32
       uint8_t* dst = sKV + slot * TILE;
-      const int phys = __shfl_sync(0xffffffffu, win, (j * nbox + lane) & 31);
-      if (lane < nbox) {
-        const int tok = (j0 + j) * DBN + lane * kp.box_rows;
-#pragma unroll
-        for (int c = 0; c < CH; ++c)
-          tma_load_4d(dst + c * CHUNK + lane * kp.box_rows * 128, kv ? tmV : tmK, &kv_full[slot],
-                      c * 64, tok & (kp.page_size - 1), hk, phys);
+      const int x = lane / CH, c = lane - x * CH;
+      const int phys = __shfl_sync(0xffffffffu, win, (j * nbox + x) & 31);
+      if (x < nbox) {
+        const int tok = (j0 + j) * DBN + x * kp.box_rows;
+        tma_load_4d(dst + c * CHUNK + x * kp.box_rows * 128, kv ? tmV : tmK, &kv_full[slot], c * 64,
+                    tok & (kp.page_size - 1), hk, phys);
       }
       ++it;
     }
