@@ -29,7 +29,11 @@ ATTN_ERR_TIMEOUT = 5
 
 _DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 
-__all__ = ["AttnError", "attn_fwd", "attn_fwd_gqa", "attn_fwd_varlen", "attn_bwd",
+ATTN_SCHED_DEFAULT = 0
+ATTN_SCHED_ONE_TILE = 1
+ATTN_SCHED_EAGER_RESCALE = 2
+
+__all__ = ["AttnError", "attn_fwd", "attn_fwd_schedule", "attn_fwd_gqa", "attn_fwd_varlen", "attn_bwd",
            "attn_bwd_gqa", "attn_bwd_varlen", "attn_bwd_varlen_workspace_size",
            "attn_bwd_workspace_size",
            "attn_fp8_quantize", "attn_fp8_quantize_gqa", "attn_fp8_quantize_rope", "attn_fwd_fp8",
@@ -117,6 +121,30 @@ def attn_fwd(q, k, v, causal: bool = False, softmax_scale: float | None = None,
     code = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
                         int(bool(causal)), scale, _DTYPES[q.dtype], _stream(stream))
     _check(code, "attn_fwd")
+    if host:
+        return o.cpu(), lse.cpu()
+    return o, lse
+
+
+def attn_fwd_schedule(q, k, v, schedule: int, causal: bool = False,
+                      softmax_scale: float | None = None, o=None, lse=None, stream=None):
+    """attn_fwd with a schedule variant (ATTN_SCHED_* flags), for measurement."""
+    lib = _lib.load()
+    (q, k, v), host = _to_device([q, k, v])
+    B, H, N, d = _shape4(q, "q")
+    if _shape4(k, "k") != (B, H, N, d) or _shape4(v, "v") != (B, H, N, d):
+        raise ValueError("q, k, v must have the same shape")
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must all be bfloat16 or all float16")
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    code = lib.attn_fwd_schedule(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                 int(bool(causal)), scale, _DTYPES[q.dtype], int(schedule),
+                                 _stream(stream))
+    _check(code, "attn_fwd_schedule")
     if host:
         return o.cpu(), lse.cpu()
     return o, lse

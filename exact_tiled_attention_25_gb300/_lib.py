@@ -20,6 +20,9 @@ c_char_p = ctypes.c_char_p
 SIGNATURES = {
     "attn_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                          c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p]),
+    "attn_fwd_schedule": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                  c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
+                                  c_void_p]),
     "attn_fwd_gqa": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p]),
     "attn_fwd_varlen": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,

@@ -36,8 +36,7 @@ EncodeTiledFn encode_fn() {
 }
 
 constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices];
-int g_arch_ok[kMaxDevices];   // 0 unknown, 1 ok, 2 wrong arch
+int g_arch_ok[kMaxDevices];   // 0 unknown, 1 ok, 2 wrong arch (a property of the device)
 std::mutex g_dev_mutex;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -88,7 +87,10 @@ attn_status_t check_scale(float s) {
   return ATTN_OK;
 }
 
-// Device checks: compute capability 10.3 and the status word address.
+}  // namespace
+
+// Device check: compute capability 10.3, cached per device ordinal (the
+// architecture does not change with the context).
 attn_status_t check_device() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -102,22 +104,11 @@ attn_status_t check_device() {
     e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
     g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
-    if (g_arch_ok[dev] == 1) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_device_status);
-      if (e != cudaSuccess) {
-        g_arch_ok[dev] = 0;
-        return fail_cuda(e, "cudaGetSymbolAddress(status word)");
-      }
-      g_status_ptr[dev] = static_cast<int*>(p);
-    }
   }
   if (g_arch_ok[dev] != 1)
     return fail(ATTN_ERR_ARCH, "this library runs on compute capability 10.3 (GB300) only");
   return ATTN_OK;
 }
-
-}  // namespace
 
 attn_status_t fail(attn_status_t code, const std::string& msg) {
   g_last_error = msg;
@@ -130,10 +121,13 @@ attn_status_t fail_cuda(cudaError_t err, const char* what) {
   return ATTN_ERR_CUDA;
 }
 
+// Looked up on every call rather than cached per device ordinal, so the
+// address always belongs to the current context (a cached one would go stale
+// after cudaDeviceReset or under another context on the same device).
 int* device_status_word() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  return g_status_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
 }
 
 attn_status_t make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
@@ -241,6 +235,25 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        int H, int N, int d, int causal, float softmax_scale, attn_dtype_t dtype,
                        cudaStream_t stream) {
   return attn_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, softmax_scale, dtype, stream);
+}
+
+attn_status_t attn_fwd_schedule(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int N, int d, int causal, float softmax_scale,
+                                attn_dtype_t dtype, int schedule, cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if ((s = check_shape(B, H, N, d, causal)) != ATTN_OK) return s;
+  if ((s = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return s;
+  if ((s = check_scale(softmax_scale)) != ATTN_OK) return s;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16)
+    return fail(ATTN_ERR_INVALID_ARG, "dtype must be ATTN_BF16 or ATTN_FP16");
+  if (schedule < 0 || schedule > (ATTN_SCHED_ONE_TILE | ATTN_SCHED_EAGER_RESCALE))
+    return fail(ATTN_ERR_INVALID_ARG, "schedule must combine ATTN_SCHED_* flags");
+  if (dtype != ATTN_BF16 || d == 256)
+    return fail(ATTN_ERR_UNSUPPORTED, "schedule variants: bfloat16, d = 64 or 128");
+  if ((s = check_device()) != ATTN_OK) return s;
+  FwdParams p{q, k, v, o, lse, B, H, N, d, H, nullptr, 0, causal, softmax_scale, 0};
+  return launch_fwd_sched(p, schedule, stream);
 }
 
 attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -596,6 +609,7 @@ attn_status_t attn_selftest_wait_timeout(unsigned limit_us, cudaStream_t stream)
     return fail(ATTN_ERR_INVALID_ARG, "limit_us must be in [1, 1000000]");
   if ((s = check_device()) != ATTN_OK) return s;
   int* status = device_status_word();
+  if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
   selftest_wait_kernel<<<1, 32, 0, stream>>>(status, static_cast<uint64_t>(limit_us) * 1000ull);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "self-test launch");
@@ -609,6 +623,7 @@ attn_status_t attn_get_device_status(cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
   int* word = device_status_word();
+  if (!word) return fail(ATTN_ERR_CUDA, "status word unavailable");
   int value = 0;
   e = cudaMemcpy(&value, word, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return fail_cuda(e, "reading the status word");

@@ -16,8 +16,12 @@ namespace attn {
 attn_status_t fail(attn_status_t code, const std::string& msg);
 attn_status_t fail_cuda(cudaError_t err, const char* what);
 
-// Device address of the status word of the current device.
+// Device address of the status word in the current context (nullptr if the
+// lookup fails).
 int* device_status_word();
+
+// Compute capability 10.3 check of the current device (ATTN_ERR_ARCH if not).
+attn_status_t check_device();
 
 // 3-D tensor map over a contiguous [planes][rows][inner] array with a
 // (box_inner x box_rows x 1) box and 128-byte swizzle.  elem_bytes is 1 or 2.
@@ -106,6 +110,8 @@ struct Fp8FwdParams {
 };
 
 attn_status_t launch_fwd(const FwdParams& p, cudaStream_t stream);
+// Schedule variants of the forward kernel (ATTN_SCHED_* flags), for measurement.
+attn_status_t launch_fwd_sched(const FwdParams& p, int sched, cudaStream_t stream);
 // Persistent forward (cluster launch control) for packed causal batches.
 attn_status_t launch_fwd_persistent(const FwdParams& p, cudaStream_t stream);
 attn_status_t launch_bwd(const BwdParams& p, cudaStream_t stream);

@@ -38,9 +38,17 @@ constexpr int BM = 128;   // query rows per tile
 constexpr int BN = 128;   // keys per tile
 constexpr int kSmemLimit = 232448;
 
-template <int D>
+// Schedule variants of the forward kernel, kept for measurement (the pages'
+// pipeline ablation): the default alternates two query tiles per CTA and
+// rescales lazily.
+enum : int {
+  kSchedOneTile = 1,   // one query tile per CTA: no second tile to fill the softmax window
+  kSchedEager = 2,     // rescale O whenever the row max grows (no 2^8 slack)
+};
+
+template <int D, int NQ_ = (D <= 128) ? 2 : 1>
 struct FwdCfg {
-  static constexpr int NQ = (D <= 128) ? 2 : 1;
+  static constexpr int NQ = NQ_;
   static constexpr int CH = D / 64;                  // 128-byte column chunks per row
   static constexpr int CHUNK_BYTES = BM * 128;       // one 128-row x 128-byte chunk
   static constexpr int TILE_BYTES = BM * D * 2;      // a Q, K or V tile
@@ -87,11 +95,13 @@ __device__ __forceinline__ float lg2_approx(float x) {
 
 // PACKED: a batch of sequences packed back to back ([total, H, d], LSE
 // [H, total], offsets cu_seqlens); otherwise [B, H, N, d] and LSE [B, H, N].
-template <int D, bool CAUSAL, bool FP16, bool PACKED>
-__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+// SCHED: 0, or kSchedOneTile / kSchedEager (measurement variants).
+template <int D, bool CAUSAL, bool FP16, bool PACKED, int SCHED = 0,
+          int NQ_ = ((SCHED & kSchedOneTile) || D > 128) ? 1 : 2>
+__global__ void __launch_bounds__(FwdCfg<D, NQ_>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdKParams kp) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, NQ_>;
   constexpr int NQ = C::NQ;
   constexpr int NSLOT = C::NSLOT;
 
@@ -350,8 +360,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       named_bar_sync(pair_bar, 64);
       const float m_new = fmaxf(m_ref, fmaxf(m_half, xch[j & 1][t][h ^ 1][r]));
       // Move the exponent reference only when the max grew by more than 2^8
-      // (both halves of a row take the same decision).
-      const bool need = (m_new - m_ref) * c2 > 8.f;
+      // (both halves of a row take the same decision); the eager variant
+      // moves it whenever the max grows.
+      const bool need = (SCHED & kSchedEager) ? (m_new > m_ref) : (m_new - m_ref) * c2 > 8.f;
       float alpha = 1.f;
       if (need) {
         alpha = ex2_approx((m_ref - m_new) * c2);
@@ -467,10 +478,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool FP16, bool PACKED>
+template <int D, bool CAUSAL, bool FP16, bool PACKED, int SCHED = 0>
 attn_status_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
-  using C = FwdCfg<D>;
-  auto kern = fwd_kernel<D, CAUSAL, FP16, PACKED>;
+  using C = FwdCfg<D, ((SCHED & kSchedOneTile) || D > 128) ? 1 : 2>;
+  auto kern = fwd_kernel<D, CAUSAL, FP16, PACKED, SCHED>;
   attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (s != ATTN_OK) return s;
   CUtensorMap tq, tk, tv;
@@ -536,6 +547,30 @@ attn_status_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
     case 256: return launch_fwd_d<256>(p, stream);
   }
   return fail(ATTN_ERR_INVALID_ARG, "d must be 64, 128 or 256");
+}
+
+// Measurement variants (bfloat16, fixed length, d = 64 or 128).
+attn_status_t launch_fwd_sched(const FwdParams& p, int sched, cudaStream_t stream) {
+  if (p.fp16 || p.cu_seqlens || p.H_kv != p.H || (p.d != 64 && p.d != 128))
+    return fail(ATTN_ERR_UNSUPPORTED,
+                "schedule variants: bfloat16, fixed length, H_kv = H, d = 64 or 128");
+  if (p.N > 65535 * 128 || p.H > 65535 || p.B > 65535)
+    return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
+#define ATTN_SCHED_CASE(S)                                                                   \
+  case S:                                                                                    \
+    if (p.d == 64)                                                                           \
+      return p.causal ? launch_fwd_t<64, true, false, false, S>(p, stream)                   \
+                      : launch_fwd_t<64, false, false, false, S>(p, stream);                 \
+    return p.causal ? launch_fwd_t<128, true, false, false, S>(p, stream)                    \
+                    : launch_fwd_t<128, false, false, false, S>(p, stream);
+  switch (sched) {
+    ATTN_SCHED_CASE(0)
+    ATTN_SCHED_CASE(kSchedOneTile)
+    ATTN_SCHED_CASE(kSchedEager)
+    ATTN_SCHED_CASE(kSchedOneTile | kSchedEager)
+  }
+#undef ATTN_SCHED_CASE
+  return fail(ATTN_ERR_INVALID_ARG, "schedule must be a combination of ATTN_SCHED_ONE_TILE and ATTN_SCHED_EAGER_RESCALE");
 }
 
 }  // namespace attn

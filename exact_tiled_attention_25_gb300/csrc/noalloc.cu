@@ -4,8 +4,6 @@
 // the caller's behalf.  The scratch attn_bwd needs (float32 dQ accumulator and
 // the two padded row vectors) comes from a fixed array compiled into this
 // library instead of a caller-provided workspace.
-#include <mutex>
-
 #include "common.h"
 
 namespace attn {
@@ -17,26 +15,17 @@ constexpr size_t kNoAllocScratchBytes = 64ull << 20;   // 64 MiB
 
 __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];
-std::mutex g_scratch_mutex;
-
-// Device address of g_bwd_scratch on the current device.  In host code the
-// symbol itself is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// Device address of g_bwd_scratch in the current context.  In host code the
+// symbol itself is only a host-side stand-in, so the address is looked up with
+// the device current.  The lookup runs on every call (it is cheap once the
+// module is loaded) instead of being cached per device ordinal: a cached
+// address would go stale after cudaDeviceReset or under another context on the
+// same device.
 attn_status_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device ordinal out of range");
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_bwd_scratch);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(built-in scratch)");
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_bwd_scratch);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(built-in scratch)");
+  *out = p;
   return ATTN_OK;
 }
 
@@ -57,8 +46,12 @@ extern "C" attn_status_t attn_bwd_noalloc(const void* q, const void* k, const vo
                 "problem needs " + std::to_string(need) +
                     " bytes of backward scratch; the built-in scratch of attn_bwd_noalloc holds " +
                     std::to_string(kNoAllocScratchBytes) + " bytes (use attn_bwd with a workspace)");
+  // the device check first, so a device of the wrong architecture gets
+  // ATTN_ERR_ARCH rather than a failed symbol lookup
+  attn_status_t s = check_device();
+  if (s != ATTN_OK) return s;
   void* scratch = nullptr;
-  attn_status_t s = scratch_address(&scratch);
+  s = scratch_address(&scratch);
   if (s != ATTN_OK) return s;
   return attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch, kNoAllocScratchBytes, B, H, N, d,
                   causal, softmax_scale, dtype, stream);

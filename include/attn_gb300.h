@@ -80,6 +80,35 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        attn_dtype_t dtype, cudaStream_t stream);
 
 /*
+ * Schedule variants of attn_fwd, for measurement only (the ablation of the
+ * forward pipeline); flags combine with bitwise or.
+ */
+enum {
+  ATTN_SCHED_DEFAULT = 0,
+  ATTN_SCHED_ONE_TILE = 1,       /* one 128-row query tile per CTA: while its softmax
+                                    runs, the tensor core has no second tile to work on */
+  ATTN_SCHED_EAGER_RESCALE = 2   /* rescale the output accumulator whenever the row max
+                                    grows, instead of only when it grows by more than 2^8 */
+};
+
+/*
+ * attn_fwd_schedule -- attn_fwd with a schedule variant.  `schedule` is a
+ * combination of the ATTN_SCHED_* flags; ATTN_SCHED_DEFAULT is exactly attn_fwd.
+ * Every variant computes the same O and LSE (up to rounding); only the order of
+ * work on the GPU changes.  Limits: bfloat16, d = 64 or 128 (other shapes return
+ * ATTN_ERR_UNSUPPORTED); an unknown flag returns ATTN_ERR_INVALID_ARG.  Other
+ * arguments, errors and semantics as attn_fwd.
+ * Source: "FlashAttention-3: Hopper Asynchrony and FP8 Attention", sections
+ * "How we know: H100 attention benchmarks" (the pipeline ablation: throughput
+ * with and without the overlap of softmax and matrix multiplies),
+ * "Ping-pong scheduling" (a second tile's matrix multiplies under one tile's
+ * softmax) and "Symbol Map" (the numerator rescale when the running max grows).
+ */
+attn_status_t attn_fwd_schedule(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int N, int d, int causal, float softmax_scale,
+                                attn_dtype_t dtype, int schedule, cudaStream_t stream);
+
+/*
  * attn_fwd_gqa -- attn_fwd with grouped-query attention: the H query heads
  * share H_kv key/value heads (1 <= H_kv <= H, H % H_kv == 0); query head h
  * reads key/value head h / (H / H_kv).  H_kv = H is attn_fwd, H_kv = 1 is
@@ -123,7 +152,15 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
  * attn_bwd_workspace_size -- bytes of device scratch attn_bwd needs:
  * a float32 dQ accumulator [B, H, N, d] and two float32 row vectors (-L * log2(e)
  * and -D, D = rowsum(dO * O)) padded to a multiple of 128 rows per head, each
- * part 256-byte aligned.  Returns 0 for invalid sizes.
+ * part 256-byte aligned.  Returns 0 for invalid sizes.  Pure arithmetic on the
+ * sizes: no CUDA call, usable before any device is chosen.
+ * Source: the global dQ that "FlashAttention-3: Hopper Asynchrony and FP8
+ * Attention", section "Backward warp specialization", has the dQ-writer add
+ * local tiles into (here a float32 accumulator, converted at the end); the
+ * caller allocates it once up front, as "FlashAttention 3 Hardware Acceleration:
+ * Hopper GPU Strategies for Long-Context Enterprise Inference Optimization",
+ * sections "Poor Memory Allocation" (pre-allocated workspace buffers) and
+ * "Memory Fragmentation" (workspace kept apart from long-lived buffers) advise.
  */
 size_t attn_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -197,8 +234,10 @@ attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const
  *   - Problems whose attn_bwd_workspace_size() exceeds 64 MiB are rejected with
  *     ATTN_ERR_INVALID_ARG and a message naming the sizes.
  *   - No device memory is allocated or freed by this call.
- *   - The first call on a device looks up the array's device address (with that
- *     device current) and caches it; make that first call before any stream
+ *   - Each call checks the device (compute capability 10.3, else ATTN_ERR_ARCH)
+ *     and then looks up the array's device address in the current context,
+ *     with that device current.  The first lookup in a context loads the
+ *     library's device code there; make that first call before any stream
  *     capture.
  *   - Every call shares the one array.  Calls whose work overlaps on the GPU
  *     (different streams, or different host threads on the same device) race on
@@ -393,7 +432,16 @@ attn_status_t attn_fp8_quantize_rope(const float* q, const float* k, const float
  *   *_descale  : [B, H, ceil(N/128)] float32 block descales.
  *   o          : [B, H, N, d] bfloat16 (written); lse: [B, H, N] float32 (written).
  * Scores use the block descales of their query and key blocks; the
- * probabilities are rounded to e4m3 for the P V product.
+ * probabilities are rounded to e4m3 for the P V product.  causal, softmax_scale,
+ * the asynchronous launch on `stream` and the errors are those of attn_fwd;
+ * descales must be positive and finite (the pre-pass writes them so).
+ * Source: "FlashAttention-3: Hopper Asynchrony and FP8 Attention", sections
+ * "Symbol Map" (the same O and L as attn_fwd), "FP8 accuracy controls" (one
+ * scale per Q, K or V block; Q and K may carry the transform M, which the
+ * scores do not see since (QM)(KM)^T = QK^T) and "FP8 layout conformance" (the
+ * P V product on FP8 operands); "FlashAttention 3 Hardware Acceleration: ...",
+ * section "FP8 Assumptions": quantisation happens before the call and every
+ * FP8 tensor travels with its scales.
  */
 attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
                            const float* q_descale, const float* k_descale,
@@ -438,7 +486,15 @@ attn_status_t attn_fwd_fp8_gqa(const uint8_t* q8, const uint8_t* k8, const uint8
 /*
  * attn_get_device_status -- synchronises `stream`, then reads and clears the
  * current device's status word.  ATTN_OK, ATTN_ERR_TIMEOUT (a kernel gave up
- * on an internal wait; attn_last_error() names the role), or ATTN_ERR_CUDA.
+ * on an internal wait; attn_last_error() names the role), ATTN_ERR_INVALID_ARG
+ * (a packed or paged call met offsets, lengths or pages out of range and
+ * skipped them), ATTN_ERR_ARCH, or ATTN_ERR_CUDA.
+ * Source: the pages list failure modes ("FlashAttention-3: Hopper Asynchrony
+ * and FP8 Attention", section "Where It Breaks") and ask that problems be
+ * reported as explicit errors rather than silently degraded ("FlashAttention 3
+ * Hardware Acceleration: ...", section "Unsupported GPU Architecture"); this
+ * device-side report is the library's own way of doing so for errors found
+ * while kernels run.
  */
 attn_status_t attn_get_device_status(cudaStream_t stream);
 
@@ -455,7 +511,10 @@ attn_status_t attn_get_device_status(cudaStream_t stream);
  */
 attn_status_t attn_selftest_wait_timeout(unsigned limit_us, cudaStream_t stream);
 
-/* Static description of a status code. */
+/* Static description of a status code (a string literal; never NULL).  The
+ * codes are the library's own explicit errors, in the sense of "FlashAttention
+ * 3 Hardware Acceleration: ...", section "Unsupported GPU Architecture"
+ * (explicit errors rather than silent degradation). */
 const char* attn_status_string(attn_status_t s);
 
 /* Detail of the last error returned on this host thread ("" if none). */

@@ -72,3 +72,14 @@ def guarded(shape, dtype, fill):
             (lambda t: torch.all(t == fill).item())
         assert same(head) and same(tail), "write outside the output tensor"
     return view, check
+
+
+def timed_step_inputs(seed=3, shape=(2, 16, 8192, 128)):
+    """The benchmark's own inputs for the timed step, drawn the same way on the
+    device: Q, K, V, dO i.i.d. N(0, 1) float32 from one seeded torch generator,
+    rounded to bfloat16, then the Hadamard signs from the same generator."""
+    g = torch.Generator(device=dev()).manual_seed(seed)
+    q, k, v, do = (torch.randn(shape, generator=g, device=dev(), dtype=torch.float32)
+                   for _ in range(4))
+    signs = torch.where(torch.rand(shape[-1], generator=g, device=dev()) < 0.5, -1.0, 1.0).float()
+    return tuple(t.to(torch.bfloat16) for t in (q, k, v, do)) + (signs,)

@@ -242,3 +242,23 @@ def test_fp8_bf16_prepass_is_declared_and_validates(lib):
     code = lib.attn_fp8_quantize_bf16(16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 4, 2, 256, 128,
                                       1, None)
     assert code == 1 and b"Hadamard" in lib.attn_last_error()
+
+
+def test_noalloc_refuses_oversized_problems_before_any_cuda_call(lib):
+    """attn_bwd_noalloc checks the problem against its built-in scratch first,
+    so the refusal needs no GPU and names the limit."""
+    assert "attn_bwd_noalloc" in declared_functions()
+    B, H, N, d = 2, 16, 4096, 128
+    assert lib.attn_bwd_workspace_size(B, H, N, d) > 64 << 20
+    code = lib.attn_bwd_noalloc(16, 16, 16, 16, 16, 16, 16, 16, 16, B, H, N, d, 1, 0.1, 0, None)
+    assert code == 1                          # ATTN_ERR_INVALID_ARG
+    assert b"built-in scratch" in lib.attn_last_error()
+
+
+def test_noalloc_reaches_the_device_check_without_a_gpu(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # a problem that fits: the device check comes before the symbol lookup
+    code = lib.attn_bwd_noalloc(16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 2, 256, 64, 0, 0.1, 0, None)
+    assert code in (3, 4)

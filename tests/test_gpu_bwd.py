@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_util import GRAD_REL_RMSE, check_status, dev, guarded, lib, rel_rmse
+from gpu_util import GRAD_REL_RMSE, check_status, dev, guarded, lib, rel_rmse, timed_step_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -100,3 +100,21 @@ def test_workspace_is_reusable_and_results_repeat(attn):
     check_status(attn)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])     # dK, dV: no atomics
     assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2
+
+
+def test_timed_config_noncausal_whole_heads(attn):
+    """The backward exactly as the benchmark times it: B=2, H=16, N=8192,
+    d=128, non-causal -- every CTA walks 64 query tiles and 64 CTAs add into
+    each dQ row.  Whole heads (every dQ, dK, dV entry) of three heads against
+    the oracle, and on every head sum_j dV_j = sum_i dO_i and sum_j dK_j = 0."""
+    w = workloads.LONG_FWD
+    assert (w.B, w.H, w.N, w.d, w.causal) == (2, 16, 8192, 128, False)
+    tq, tk, tv, tdo = (t.cpu() for t in timed_step_inputs(w.seed, (w.B, w.H, w.N, w.d))[:4])
+    dq, dk, dv, errs = _run(attn, tq, tk, tv, tdo, w.causal,
+                            heads=[(0, 0), (1, 15), (1, 7)])
+    _assert(errs)
+    sdv = dv.double().sum(dim=2).cpu().numpy()
+    sdo = workloads.as_f64(tdo).sum(axis=2)
+    assert np.abs(sdv - sdo).max() <= 2e-2 * np.abs(sdo).max() + 0.5
+    sdk = dk.double().sum(dim=2).cpu().numpy()
+    assert np.abs(sdk).max() <= 2e-2 * dk.double().abs().sum(dim=2).max().item()

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_util import FP8_RMSE, check_status, dev, lib
+from gpu_util import FP8_RMSE, check_status, dev, lib, timed_step_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -106,7 +106,8 @@ def test_fp8_outlier_config_rmse(attn):
         rmse[name] = float(np.sqrt(np.mean(err ** 2)))
     print("fp8 rmse", rmse)
     assert rmse["block"] <= FP8_RMSE and rmse["block_hadamard"] <= FP8_RMSE
-    assert rmse["block_hadamard"] < rmse["per_tensor"]
+    # the ordering the oracle's own quantiser gives on this workload
+    assert rmse["block_hadamard"] < rmse["block"] < rmse["per_tensor"]
 
 
 @pytest.mark.parametrize("with_hadamard", [False, True])
@@ -208,3 +209,58 @@ def test_bf16_prepass_forward_matches_dequantised_oracle(attn, causal):
     # total error against exact attention of the bfloat16 inputs
     exact, _ = oracle.attention_forward(*(x.astype(np.float64) for x in xs), 1 / np.sqrt(128), causal)
     assert np.sqrt(np.mean((o.float().cpu().numpy() - exact) ** 2)) <= FP8_RMSE
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_timed_fp8_chain_full_size(attn, causal):
+    """The FP8 stages exactly as the benchmark times them, at B=2, H=16,
+    N=8192, d=128 on the same seeded bfloat16 inputs: the bfloat16 pre-pass
+    (block scales, Hadamard on Q and K) then the FP8 forward.
+    * Sampled rows of three heads against exact attention on the dequantised
+      codes (the forward kernel's own error: e4m3 P and float32 sums).
+    * The same rows against exact attention of the bfloat16 inputs: RMSE within
+      the FP8 bar.
+    * The sampled heads' codes against the oracle quantiser (at most one e4m3
+      step apart, rarely: the transform runs in float32 on the GPU)."""
+    w = workloads.LONG_FWD
+    *gs, _, gsigns = timed_step_inputs(w.seed, (w.B, w.H, w.N, w.d))
+    (q8, k8, v8), (qd, kd, vd) = attn.attn_fp8_quantize_bf16(*gs, hadamard_signs=gsigns)
+    o, lse = attn.attn_fwd_fp8(q8, k8, v8, qd, kd, vd, causal=causal, softmax_scale=w.scale)
+    check_status(attn)
+    rng = np.random.default_rng(99)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 129, 4095, 8190, 8191],
+                                     rng.integers(0, w.N, 40)]))
+    got_o = o.float().cpu().numpy()
+    got_l = lse.cpu().numpy()
+    ts = [t.cpu() for t in gs]
+    signs = gsigns.cpu().numpy()
+    codes = [c.cpu().numpy() for c in (q8, k8, v8)]
+    descs = [d.cpu().numpy() for d in (qd, kd, vd)]
+    err_deq, err_exact = [], []
+    for b, h in ((0, 0), (1, 15), (0, 7)):
+        deq = [oracle.dequantize_e4m3_blocks(c[b:b + 1, h:h + 1], d[b:b + 1, h:h + 1])[0, 0]
+               for c, d in zip(codes, descs)]
+        ref_o, ref_l = oracle.attention_forward_rows(*deq, w.scale, causal, rows)
+        err_deq.append(got_o[b, h, rows] - ref_o)
+        np.testing.assert_allclose(got_l[b, h, rows], ref_l, atol=2e-3)
+        x = [workloads.as_f64(t[b, h]) for t in ts]
+        ex_o, _ = oracle.attention_forward_rows(*x, w.scale, causal, rows)
+        err_exact.append(got_o[b, h, rows] - ex_o)
+        # the quantiser on this head
+        for which in range(3):
+            xi = workloads.as_f64(ts[which][b:b + 1, h:h + 1]).astype(np.float32)
+            rc, rd = oracle.quantize_e4m3_blocks(xi, signs=signs if which < 2 else None)
+            np.testing.assert_allclose(descs[which][b:b + 1, h:h + 1], rd, rtol=2e-6)
+            c = codes[which][b:b + 1, h:h + 1]
+            if which == 2:
+                np.testing.assert_array_equal(c, rc)
+                continue
+            gv, rv = oracle.e4m3_decode(c), oracle.e4m3_decode(rc)
+            step = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(rv), 2.0 ** -6))) - 3)
+            assert np.all(np.abs(gv - rv) <= step * 1.0001)
+            assert np.mean(c != rc) < 1e-3
+    e = np.concatenate([x.ravel() for x in err_deq])
+    assert np.sqrt(np.mean(e ** 2)) <= 1e-2 and np.abs(e).max() <= 0.25, \
+        (np.sqrt(np.mean(e ** 2)), np.abs(e).max())
+    e = np.concatenate([x.ravel() for x in err_exact])
+    assert np.sqrt(np.mean(e ** 2)) <= FP8_RMSE, np.sqrt(np.mean(e ** 2))

@@ -129,3 +129,51 @@ def test_long_config_sampled_rows(attn, w):
         assert np.abs(diff).max() <= FWD_MAX_ABS
         assert np.sqrt(np.mean(diff ** 2)) <= FWD_RMSE
         assert np.abs(got_l - ref_l).max() <= LSE_ABS
+
+
+@pytest.mark.parametrize("sched", [1, 2, 3], ids=["one_tile", "eager", "one_tile_eager"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 129, 300, 1000])
+def test_schedule_variants(attn, sched, d, causal, N):
+    """The measurement variants of the forward (one query tile per CTA, eager
+    rescaling) compute the same attention: parity with the oracle, on scores
+    spread wide enough that the running max moves often."""
+    q, k, v = workloads.normal(500 + N + d, (1, 2, N, d), 3)
+    tq, tk, tv = (workloads.round_to(x, "bf16") for x in (2 * q, 2 * k, v))
+    scale = 1 / np.sqrt(d)
+    o, lse = attn.attn_fwd_schedule(tq.to(dev()), tk.to(dev()), tv.to(dev()), sched,
+                                    causal=causal, softmax_scale=scale)
+    check_status(attn)
+    ref_o, ref_l = oracle.attention_forward(*(workloads.as_f64(t) for t in (tq, tk, tv)),
+                                            scale, causal)
+    assert_fwd_close(o, lse, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("sched", [1, 2], ids=["one_tile", "eager"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_schedule_variants_timed_shape(attn, sched, causal):
+    """The variants at the shape the benchmark times them (B=2, H=16, N=8192,
+    d=128): sampled rows against the oracle, and the default schedule's output
+    to within one bfloat16 rounding."""
+    w = workloads.LONG_FWD_CAUSAL if causal else workloads.LONG_FWD
+    gen = torch.Generator(device=dev()).manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.d)
+    q, k, v = (torch.randn(shape, generator=gen, device=dev(), dtype=torch.float32)
+               .to(torch.bfloat16) for _ in range(3))
+    o, lse = attn.attn_fwd_schedule(q, k, v, sched, causal=causal, softmax_scale=w.scale)
+    o0, lse0 = attn.attn_fwd(q, k, v, causal=causal, softmax_scale=w.scale)
+    check_status(attn)
+    # float32 sums in a different order can move a bfloat16 output by one unit
+    # in the last place (2^-8 relative)
+    assert torch.all((o.float() - o0.float()).abs() <= 2 ** -7 * o0.float().abs() + 1e-4)
+    assert (lse - lse0).abs().max().item() <= 1e-4
+    if sched == 1:       # the same per-row arithmetic in the same order: same bits
+        assert torch.equal(o, o0) and torch.equal(lse, lse0)
+    rows = np.array([0, 1, 127, 128, 4097, w.N - 1])
+    for (b, h) in [(0, 0), (1, 15)]:
+        qh, kh, vh = (t[b, h].double().cpu().numpy() for t in (q, k, v))
+        ref_o, ref_l = oracle.attention_forward_rows(qh, kh, vh, w.scale, causal, rows)
+        diff = o[b, h, rows].double().cpu().numpy() - ref_o
+        assert np.abs(diff).max() <= FWD_MAX_ABS and np.sqrt(np.mean(diff ** 2)) <= FWD_RMSE
+        assert np.abs(lse[b, h, rows].double().cpu().numpy() - ref_l).max() <= LSE_ABS
