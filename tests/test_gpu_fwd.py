@@ -154,8 +154,8 @@ def test_schedule_variants(attn, sched, d, causal, N):
 @pytest.mark.parametrize("causal", [False, True])
 def test_schedule_variants_timed_shape(attn, sched, causal):
     """The variants at the shape the benchmark times them (B=2, H=16, N=8192,
-    d=128): sampled rows against the oracle, and the default schedule's output
-    to within one bfloat16 rounding."""
+    d=128): sampled rows against the oracle, and whole tensors against the
+    default schedule's output."""
     w = workloads.LONG_FWD_CAUSAL if causal else workloads.LONG_FWD
     gen = torch.Generator(device=dev()).manual_seed(w.seed)
     shape = (w.B, w.H, w.N, w.d)
@@ -164,9 +164,12 @@ def test_schedule_variants_timed_shape(attn, sched, causal):
     o, lse = attn.attn_fwd_schedule(q, k, v, sched, causal=causal, softmax_scale=w.scale)
     o0, lse0 = attn.attn_fwd(q, k, v, causal=causal, softmax_scale=w.scale)
     check_status(attn)
-    # float32 sums in a different order can move a bfloat16 output by one unit
-    # in the last place (2^-8 relative)
-    assert torch.all((o.float() - o0.float()).abs() <= 2 ** -7 * o0.float().abs() + 1e-4)
+    # Eager rescaling rounds P to bfloat16 against another exponent reference
+    # (not a power of two apart), so outputs differ by P rounding: whole tensors
+    # agree within the forward tolerances.
+    diff = (o.float() - o0.float())
+    assert diff.abs().max().item() <= FWD_MAX_ABS
+    assert diff.pow(2).mean().sqrt().item() <= FWD_RMSE
     assert (lse - lse0).abs().max().item() <= 1e-4
     if sched == 1:       # the same per-row arithmetic in the same order: same bits
         assert torch.equal(o, o0) and torch.equal(lse, lse0)
