@@ -16,16 +16,17 @@
 //  2. main: one CTA per (key/value tile j, head, batch).  K_j and V_j stay in
 //     shared memory; dK_j and dV_j accumulate in tensor memory.  Per query tile
 //     i (causal: i >= j) the MMA thread issues, on tcgen05,
-//        S^T = K_j Q_i^T, then dP^T = V_j dO_i^T,
-//     the compute warpgroup (thread = key row) forms P^T while dP^T runs and
-//     writes it back to tensor memory, so
-//        dV += P^T dO_i
-//     runs while the same warpgroup forms dS^T = P^T (dP^T - D) (tensor memory
-//     for dK, shared memory for dQ), then
-//        dK += dS^T Q_i,   dQ_i = dS K_j  (at d = 128 as dQ_i^T = K_j^T dS^T)
-//     and the reduce warpgroup reads dQ_i from tensor memory and adds it into
-//     the float32 accumulator.  At d = 128, dQ_i^T has one head dimension per
-//     TMEM lane, so each warp-wide reduction covers a whole 128-byte line.
+//        dP^T = V_j dO_i^T  (it needs nothing from this step's softmax),
+//     while the compute warpgroups (thread = key row) form P^T from S^T = K_j
+//     Q_i^T (issued the step before) and write it back to tensor memory; then
+//        dV += P^T dO_i,   S^T(next) = K_j Q_{i+1}^T,
+//     while the same warpgroups form dS^T = P^T (dP^T - D) (into tensor memory
+//     for dK, into shared memory for dQ); then
+//        dK += dS^T Q_i,   dQ_i = dS K_j  (into tensor memory, one query per lane).
+//     The dQ-writer warps (two reduce warpgroups) copy dQ_i out of tensor
+//     memory, stage it in 4 KB boxes in shared memory and add each box into
+//     the float32 accumulator with a TMA reduce-add, so the reduction runs in
+//     the TMA unit and L2 instead of as per-thread atomics.
 //  3. convert: dQ = scale * accumulator, rounded to the 16-bit type.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -50,27 +51,37 @@ struct BwdCfg {
   static constexpr int CH = D / 64;              // 128-byte chunks per row
   static constexpr int CHUNK = 128 * 128;        // one 128-row x 128-byte chunk
   static constexpr int TILE = 128 * D * 2;       // a K, V, Q or dO tile
-  static constexpr int NST = 2;                  // Q/dO ring stages
+  // Q_i (with its row vectors) and dO_i have rings of their own: Q_i is read
+  // by S^T(i) early and dK late, dO_i only by dP^T(i) and dV.  At d = 128 one
+  // dO slot is all that fits next to the dQ staging buffers.
+  static constexpr int NQS = 2;                  // Q ring slots
+  static constexpr int NDS = (D == 128) ? 1 : 2; // dO ring slots
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = TILE;
-  static constexpr int OFF_RING = 2 * TILE;      // stage s: Q at +2*TILE*s, dO at +TILE
-  static constexpr int OFF_DS = OFF_RING + NST * 2 * TILE;   // dS^T, 128 keys x 128 queries
-  static constexpr int OFF_LD = OFF_DS + 2 * CHUNK;           // per stage: L*log2e[128], D[128]
-  static constexpr int OFF_BAR = OFF_LD + NST * 1024;
+  static constexpr int OFF_Q = 2 * TILE;
+  static constexpr int OFF_DO = OFF_Q + NQS * TILE;
+  static constexpr int OFF_DS = OFF_DO + NDS * TILE;      // dS^T, 128 keys x 128 queries
+  // dQ staging: one 32-query x 32-column float32 box (4 KB, 128-byte swizzle)
+  // per reduce warp, handed to a TMA reduce-add into the float32 accumulator
+  static constexpr int STG_BOX = 32 * 32 * 4;
+  static constexpr int OFF_STG = OFF_DS + 2 * CHUNK;
+  static constexpr int OFF_LD = OFF_STG + 8 * STG_BOX;    // per Q slot: L*log2e[128], D[128]
+  static constexpr int OFF_BAR = OFF_LD + NQS * 1024;
   static constexpr int NEED = OFF_BAR + 256;
   static constexpr int SMEM_BYTES = cmin(kSmemLimit, NEED + 1024);
   static constexpr int SLACK = SMEM_BYTES - NEED;   // room to align the base to 1024
   // TMEM columns: S^T/P^T [0,128), dP^T/dS^T [128,256), dV, dK.  At d = 128
-  // there is no room left, so dQ^T reuses the dP^T columns (after dK has read
-  // dS^T there); at d = 64 dQ has its own columns.
-  static constexpr bool DQ_T = (D == 128);          // dQ computed transposed, in the dP columns
+  // there is no room left, so dQ reuses the dP^T columns (after dK has read
+  // dS^T there); at d = 64 dQ has its own columns.  dQ is stored with one
+  // query per TMEM lane.
+  static constexpr bool DQ_IN_DP = (D == 128);
   static constexpr uint32_t S_COL = 0;
   static constexpr uint32_t DP_COL = 128;
   static constexpr uint32_t DV_COL = 256;
   static constexpr uint32_t DK_COL = 256 + D;
-  static constexpr uint32_t DQ_COL = DQ_T ? DP_COL : 256 + 2 * D;
+  static constexpr uint32_t DQ_COL = DQ_IN_DP ? DP_COL : 256 + 2 * D;
   // Warps 0-7: two compute warpgroups (one per half of the 128 query columns);
-  // warps 8-15: two reduce warpgroups (one per half of the dQ tile's columns);
+  // warps 8-15: two reduce warpgroups (one per half of dQ's columns);
   // warp 16: TMA producer; warp 17: MMA issuer.
   static constexpr int THREADS = 576;
   static constexpr int LOAD_WARP = 16;
@@ -83,12 +94,15 @@ struct BwdCfg {
   }
   static_assert(DQ_COL + D <= 512 && DK_COL + D <= 512, "TMEM overflow");
   static_assert(SLACK >= 0, "shared memory overflow");
+  static_assert(OFF_STG % 1024 == 0, "staging boxes need 1024-byte alignment (swizzle atoms)");
 };
 
 struct Bars {
   uint64_t kv_full;
-  uint64_t stage_full[2];
-  uint64_t stage_empty[2];
+  uint64_t q_full[2];
+  uint64_t q_empty[2];
+  uint64_t do_full[2];
+  uint64_t do_empty[2];
   uint64_t s_full;
   uint64_t dp_full;
   uint64_t p_ready;
@@ -99,7 +113,8 @@ struct Bars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int load_items;
+  int q_items;     // Q slots the producer filled (for draining after an abort)
+  int do_items;    // dO slots the producer filled
 };
 
 struct BwdKParams {
@@ -226,7 +241,7 @@ template <int D, bool CAUSAL, bool FP16, bool PACKED>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const BwdKParams kp) {
+                    const __grid_constant__ CUtensorMap tmDQ, const BwdKParams kp) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -269,9 +284,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.kv_full, 1);
-    for (int s = 0; s < C::NST; ++s) {
-      mbar_init(&bars.stage_full[s], 1);
-      mbar_init(&bars.stage_empty[s], 1);
+    for (int s = 0; s < C::NQS; ++s) {
+      mbar_init(&bars.q_full[s], 1);
+      mbar_init(&bars.q_empty[s], 1);
+    }
+    for (int s = 0; s < C::NDS; ++s) {
+      mbar_init(&bars.do_full[s], 1);
+      mbar_init(&bars.do_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
@@ -282,7 +301,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(&bars.dkv_full, 1);
     mbar_init(&bars.drain, 1);
     bars.abort_flag = 0;
-    bars.load_items = 0;
+    bars.q_items = 0;
+    bars.do_items = 0;
     fence_mbar_init();
   }
   if (warp == C::MMA_WARP) {
@@ -314,32 +334,49 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tma_load_3d(smem + C::OFF_V + c * C::CHUNK, &tmV, &bars.kv_full, c * 64, j * C::BN, bhk);
         }
       }
-      int n = 0;
+      int nq = 0, nd = 0;                  // Q and dO loads issued
       int i = i0, h = h0;                  // query tile and query head of step n
-      for (; n < nsteps; ++n, (++i == nQ) ? (i = i0, ++h) : 0) {
-        const int st = n % C::NST;
-        const int use = n / C::NST;
-        if (use >= 1 && !mbar_wait(&bars.stage_empty[st], (use - 1) & 1, ab, kDevTimeoutLoad))
-          break;
-        uint8_t* sq = smem + C::OFF_RING + st * 2 * C::TILE;
-        uint8_t* sdo = sq + C::TILE;
-        float* sld = reinterpret_cast<float*>(smem + C::OFF_LD + st * 1024);
-        mbar_arrive_expect_tx(&bars.stage_full[st], 2 * C::TILE + 1024);
+      for (int n = 0; n < nsteps; ++n, (++i == nQ) ? (i = i0, ++h) : 0) {
+        // Q_i with its row vectors -L*log2(e) and -D into Q slot n % NQS, freed
+        // by dK of step n - NQS
+        {
+          const int st = n % C::NQS;
+          const int use = n / C::NQS;
+          if (use >= 1 && !mbar_wait(&bars.q_empty[st], (use - 1) & 1, ab, kDevTimeoutLoad)) break;
+          uint8_t* sq = smem + C::OFF_Q + st * C::TILE;
+          float* sld = reinterpret_cast<float*>(smem + C::OFF_LD + st * 1024);
+          mbar_arrive_expect_tx(&bars.q_full[st], C::TILE + 1024);
 #pragma unroll
-        for (int c = 0; c < C::CH; ++c) {
-          if constexpr (PACKED) {
-            tma_load_4d(sq + c * C::CHUNK, &tmQ, &bars.stage_full[st], c * 64, seq0 + i * C::BM, h, 0);
-            tma_load_4d(sdo + c * C::CHUNK, &tmDO, &bars.stage_full[st], c * 64, seq0 + i * C::BM, h, 0);
-          } else {
-            tma_load_3d(sq + c * C::CHUNK, &tmQ, &bars.stage_full[st], c * 64, i * C::BM, b * kp.H + h);
-            tma_load_3d(sdo + c * C::CHUNK, &tmDO, &bars.stage_full[st], c * 64, i * C::BM, b * kp.H + h);
+          for (int c = 0; c < C::CH; ++c) {
+            if constexpr (PACKED)
+              tma_load_4d(sq + c * C::CHUNK, &tmQ, &bars.q_full[st], c * 64, seq0 + i * C::BM, h, 0);
+            else
+              tma_load_3d(sq + c * C::CHUNK, &tmQ, &bars.q_full[st], c * 64, i * C::BM, b * kp.H + h);
           }
+          const size_t roff = (static_cast<size_t>(b) * kp.H + h) * kp.Npad + static_cast<size_t>(i) * C::BM;
+          bulk_load(sld, kp.lse2 + roff, 512, &bars.q_full[st]);
+          bulk_load(sld + 128, kp.delta + roff, 512, &bars.q_full[st]);
+          ++nq;
         }
-        const size_t roff = (static_cast<size_t>(b) * kp.H + h) * kp.Npad + static_cast<size_t>(i) * C::BM;
-        bulk_load(sld, kp.lse2 + roff, 512, &bars.stage_full[st]);
-        bulk_load(sld + 128, kp.delta + roff, 512, &bars.stage_full[st]);
+        // dO_i into dO slot n % NDS, freed once dP^T and dV of step n - NDS completed
+        {
+          const int st = n % C::NDS;
+          const int use = n / C::NDS;
+          if (use >= 1 && !mbar_wait(&bars.do_empty[st], (use - 1) & 1, ab, kDevTimeoutLoad)) break;
+          uint8_t* sdo = smem + C::OFF_DO + st * C::TILE;
+          mbar_arrive_expect_tx(&bars.do_full[st], C::TILE);
+#pragma unroll
+          for (int c = 0; c < C::CH; ++c) {
+            if constexpr (PACKED)
+              tma_load_4d(sdo + c * C::CHUNK, &tmDO, &bars.do_full[st], c * 64, seq0 + i * C::BM, h, 0);
+            else
+              tma_load_3d(sdo + c * C::CHUNK, &tmDO, &bars.do_full[st], c * 64, i * C::BM, b * kp.H + h);
+          }
+          ++nd;
+        }
       }
-      bars.load_items = n;
+      bars.q_items = nq;
+      bars.do_items = nd;
     }
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
@@ -347,9 +384,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       constexpr Elt E = FP16 ? Elt::F16 : Elt::BF16;
       constexpr uint32_t idSP = idesc_f16(E, 128, 128, false, false);   // S^T and dP^T
       constexpr uint32_t idKV = idesc_f16(E, 128, D, false, true);      // dV and dK (A in TMEM)
-      // dQ: rows = queries (d = 64) or, transposed, rows = head dim (d = 128);
-      // both operands MN-major from shared memory
-      constexpr uint32_t idQ = idesc_f16(E, 128, C::DQ_T ? 128 : D, true, true);
+      // dQ_i = dS K_j: rows = queries; A = dS (the dS^T buffer read MN-major),
+      // B = K_j MN-major
+      constexpr uint32_t idQ = idesc_f16(E, 128, D, true, true);
       const uint32_t sK = smem_u32(smem + C::OFF_K);
       const uint32_t sV = smem_u32(smem + C::OFF_V);
       const uint32_t sDS = smem_u32(smem + C::OFF_DS);
@@ -379,25 +416,38 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         mma_commit(&bars.dp_full);
       };
-      auto stage_q = [&](int n) { return smem_u32(smem + C::OFF_RING + (n % C::NST) * 2 * C::TILE); };
+      auto slot_q = [&](int n) { return smem_u32(smem + C::OFF_Q + (n % C::NQS) * C::TILE); };
+      auto slot_do = [&](int n) { return smem_u32(smem + C::OFF_DO + (n % C::NDS) * C::TILE); };
+      auto wait_q = [&](int n) {
+        return mbar_wait(&bars.q_full[n % C::NQS], (n / C::NQS) & 1, ab, kDevTimeoutMma);
+      };
+      auto wait_do = [&](int n) {
+        return mbar_wait(&bars.do_full[n % C::NDS], (n / C::NDS) & 1, ab, kDevTimeoutMma);
+      };
       // Issue order per step n (each MMA waits only for what it reads):
-      //   dV(n) [P^T(n) ready]   dP^T(n) [n > 0; at d = 128 after dQ(n-1) was read
-      //   out of the shared columns]   S^T(n+1) [stage n+1 loaded]
-      //   dK(n) [dS^T(n) ready]   dQ(n)
-      // so reading dQ(n-1) out of tensor memory overlaps dV(n), the dS phase of
-      // step n overlaps S^T(n+1), and the P phase of step n+1 overlaps dK(n), dQ(n).
-      bool ok = mbar_wait(&bars.kv_full, 0, ab, kDevTimeoutMma) &&
-                mbar_wait(&bars.stage_full[0], 0, ab, kDevTimeoutMma);
+      //   dP^T(n) [dO_n loaded; at d = 128 after dQ(n-1) was read out of the
+      //   shared columns]   dV(n) [P^T(n) ready]   S^T(n+1) [Q_{n+1} loaded]
+      //   dK(n) [dS(n) ready]   dQ(n)
+      // dP^T(n) needs nothing from step n's softmax, so it runs while the compute
+      // warpgroups form P^T(n), and their dS phase starts as soon as P^T(n) is
+      // written; the P phase of step n+1 overlaps dK(n), dQ(n).
+      bool ok = mbar_wait(&bars.kv_full, 0, ab, kDevTimeoutMma) && wait_q(0);
       if (ok) {
         tc_fence_after_sync();
-        issue_s(stage_q(0));
-        issue_dp(stage_q(0) + C::TILE);
+        issue_s(slot_q(0));
       }
       for (int n = 0; n < nsteps && ok; ++n) {
-        const int st = n % C::NST;
-        const uint32_t sQ = stage_q(n);
-        const uint32_t sDO = sQ + C::TILE;
-        // dV += P^T dO_i  (A = P^T from tensor memory)
+        const uint32_t sQ = slot_q(n);
+        const uint32_t sDO = slot_do(n);
+        // dP^T(n); its completion also means dQ(n-1) has finished reading the
+        // dS^T buffer, which the dS phase of step n overwrites
+        if (C::DQ_IN_DP && n > 0) {
+          if (!(ok = mbar_wait(&bars.dq_free, (n - 1) & 1, ab, kDevTimeoutMma))) break;
+        }
+        if (!(ok = wait_do(n))) break;
+        tc_fence_after_sync();
+        issue_dp(sDO);
+        // dV += P^T dO_i  (A = P^T from tensor memory); dO_i is free after it
         if (!(ok = mbar_wait(&bars.p_ready, n & 1, ab, kDevTimeoutMma))) break;
         tc_fence_after_sync();
         const uint64_t mDO = opaque(sdesc_sw128(sDO, C::CHUNK, 1024));
@@ -405,23 +455,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int kk = 0; kk < C::BM / 16; ++kk)
           mma_f16_ts(tmem + C::DV_COL, tmem + C::S_COL + C::half_col(kk), sdesc_add(mDO, kk * 16 * 128),
                      idKV, (n > 0 || kk > 0) ? 1u : 0u);
-        // dP^T of this step (step 0's was issued with S^T(0))
-        if (n > 0) {
-          if (C::DQ_T) {
-            if (!(ok = mbar_wait(&bars.dq_free, (n - 1) & 1, ab, kDevTimeoutMma))) break;
-            tc_fence_after_sync();
-          }
-          issue_dp(sDO);
-        }
+        if (n + C::NDS < nsteps) mma_commit(&bars.do_empty[n % C::NDS]);
         // S^T of the next step (its columns now only hold P^T(n), read by dV above)
         if (n + 1 < nsteps) {
-          if (!(ok = mbar_wait(&bars.stage_full[(n + 1) % C::NST], ((n + 1) / C::NST) & 1, ab,
-                               kDevTimeoutMma)))
-            break;
+          if (!(ok = wait_q(n + 1))) break;
           tc_fence_after_sync();
-          issue_s(stage_q(n + 1));
+          issue_s(slot_q(n + 1));
         }
-        // dK += dS^T Q_i  (A = dS^T from tensor memory); the stage is free after it
+        // dK += dS^T Q_i  (A = dS^T from tensor memory); the Q slot is free after it
         if (!(ok = mbar_wait(&bars.ds_ready, n & 1, ab, kDevTimeoutMma))) break;
         tc_fence_after_sync();
         const uint64_t mQ = opaque(sdesc_sw128(sQ, C::CHUNK, 1024));
@@ -429,21 +470,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int kk = 0; kk < C::BM / 16; ++kk)
           mma_f16_ts(tmem + C::DK_COL, tmem + C::DP_COL + C::half_col(kk), sdesc_add(mQ, kk * 16 * 128),
                      idKV, (n > 0 || kk > 0) ? 1u : 0u);
-        if (n + C::NST < nsteps) mma_commit(&bars.stage_empty[st]);
-        // dQ_i = dS K_j (d = 64), or dQ_i^T = K_j^T dS^T (d = 128, into the dP^T columns)
-        if (!C::DQ_T && n > 0) {
+        if (n + C::NQS < nsteps) mma_commit(&bars.q_empty[n % C::NQS]);
+        // dQ_i = dS K_j into its columns (at d = 64 once dQ(n-1) was read out)
+        if (!C::DQ_IN_DP && n > 0) {
           if (!(ok = mbar_wait(&bars.dq_free, (n - 1) & 1, ab, kDevTimeoutMma))) break;
           tc_fence_after_sync();
         }
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          const uint64_t dds = sdesc_add(mDS, kk * 16 * 128);
-          const uint64_t dk = sdesc_add(mK, kk * 16 * 128);
-          if (C::DQ_T)
-            mma_f16_ss(tmem + C::DQ_COL, dk, dds, idQ, kk > 0 ? 1u : 0u);
-          else
-            mma_f16_ss(tmem + C::DQ_COL, dds, dk, idQ, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_f16_ss(tmem + C::DQ_COL, sdesc_add(mDS, kk * 16 * 128), sdesc_add(mK, kk * 16 * 128),
+                     idQ, kk > 0 ? 1u : 0u);
         mma_commit(&bars.dq_full);
       }
       if (ok) mma_commit(&bars.dkv_full);
@@ -461,7 +497,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bool ok = true;
     int i = i0;                                      // query tile of step n
     for (int n = 0; n < nsteps; ++n, i = (i + 1 == nQ) ? i0 : i + 1) {
-      const int st = n % C::NST;
+      const int st = n % C::NQS;
       const float4* nlse4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + st * 1024);  // -L log2 e
       const float4* ndvec4 = nlse4 + 32;                                                  // -D
       const bool diag = CAUSAL && i == j;
@@ -471,11 +507,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       uint32_t pb[32];                               // this half's P^T, packed pairs
       const uint64_t cc = pack2(c2, c2);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {                  // queries [64 h + 16 c, +16)
-        const int qb = 64 * h + 16 * c;
-        uint32_t sv[16];
-        tmem_ld16(tmem + lane_addr + C::S_COL + qb, sv);
+      for (int c2 = 0; c2 < 2; ++c2) {               // queries [64 h + 32 c2, +32): one load, one wait
+        uint32_t svv[32];
+        tmem_ld32(tmem + lane_addr + C::S_COL + 64 * h + 32 * c2, svv);
         tmem_ld_wait();
+#pragma unroll
+      for (int c = 2 * c2; c < 2 * c2 + 2; ++c) {    // queries [64 h + 16 c, +16)
+        const int qb = 64 * h + 16 * c;
+        const uint32_t* sv = svv + 16 * (c - 2 * c2);
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
           const int q0 = qb + e;
@@ -497,20 +536,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tmem_st_x8(tmem + lane_addr + C::S_COL + 64 * h + 8 * c,
                    *reinterpret_cast<const uint32_t(*)[8]>(&pb[8 * c]));
       }
+      }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&bars.p_ready);
-      // phase B: dS^T = P^T (dP^T - D), from the 16-bit P^T kept in registers
-      // dP^T(n) is issued after dQ(n-1), so its completion also means dQ(n-1)
-      // has finished reading the dS^T buffer that this phase overwrites
+      // phase B: dS^T = P^T (dP^T - D), from the 16-bit P^T kept in registers,
+      // into tensor memory (for dK) and the shared dS^T buffer (for dQ).  dP^T(n)
+      // is issued after dQ(n-1), so its completion also means dQ(n-1) has
+      // finished reading the buffer this phase overwrites
       if (!(ok = mbar_wait(&bars.dp_full, n & 1, ab, kDevTimeoutSoftmax))) break;
       tc_fence_after_sync();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {                  // queries [64 h + 16 c, +16)
-        const int qb = 64 * h + 16 * c;
-        uint32_t dpv[16];
-        tmem_ld16(tmem + lane_addr + C::DP_COL + qb, dpv);
+      for (int c2 = 0; c2 < 2; ++c2) {               // queries [64 h + 32 c2, +32): one load, one wait
+        uint32_t dpvv[32];
+        tmem_ld32(tmem + lane_addr + C::DP_COL + 64 * h + 32 * c2, dpvv);
         tmem_ld_wait();
+#pragma unroll
+      for (int c = 2 * c2; c < 2 * c2 + 2; ++c) {    // queries [64 h + 16 c, +16)
+        const int qb = 64 * h + 16 * c;
+        const uint32_t* dpv = dpvv + 16 * (c - 2 * c2);
         uint32_t dd[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
@@ -546,6 +590,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           st_shared_v4(sDSrow + ((piece ^ (k & 7)) * 16), dd[4 * pc], dd[4 * pc + 1],
                        dd[4 * pc + 2], dd[4 * pc + 3]);
         }
+      }
       }
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -584,20 +629,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ reduce WGs
-    // TMEM lane r: head-dim index (d = 128, transposed tile) or query (d = 64).
-    // Reduce warpgroup g handles half the tile's columns.
+    // TMEM lane = query row of the tile; reduce warpgroup g takes dQ columns
+    // [g HC, g HC + HC).  Each warp copies its 32 rows x HC columns out of
+    // tensor memory, hands the columns back, then moves them 32 columns at a
+    // time through its 4 KB staging box (128-byte swizzle: row r's 16-byte piece
+    // c sits at piece c ^ (r % 8)) and adds the box into the float32
+    // accumulator with a TMA reduce-add, which skips rows outside the tensor.
     const int g = (warp - 8) >> 2;
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    constexpr int HC = (C::DQ_T ? C::BM : D) / 2;    // columns per reduce warpgroup
+    constexpr int HC = D / 2;                        // columns per reduce warpgroup
+    uint8_t* const stg = smem + C::OFF_STG + (warp - 8) * C::STG_BOX;
+    const uint32_t stg_row = smem_u32(stg) + lane * 128;
     int i = i0, hq = h0;                             // query tile and head of step n
-    // dQ rows: [B, H, N, d], or [total, H, d] for a packed batch
-    const size_t qstride = PACKED ? static_cast<size_t>(kp.H) * D : D;
+    bool pending = false;                            // a reduce from `stg` may be reading it
     for (int n = 0; n < nsteps; ++n, (++i == nQ) ? (i = i0, ++hq) : 0) {
       if (!mbar_wait(&bars.dq_full, n & 1, ab, kDevTimeoutReduce)) break;
       tc_fence_after_sync();
-      // read this half of the tile, hand the columns back, then reduce
       uint32_t v[HC];
 #pragma unroll
       for (int c0 = 0; c0 < HC / 32; ++c0)
@@ -606,34 +654,33 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tmem_ld_wait();
       tc_fence_before_sync();
       mbar_arrive(&bars.dq_free);
-      const int q_base = i * C::BM;
-      float* const qrow0 = kp.dq_acc + (PACKED ? (static_cast<size_t>(seq0) * kp.H + hq) * D
-                                               : (static_cast<size_t>(b) * kp.H + hq) * N * D);
-      if (C::DQ_T) {
-        // column q = query q_base + g HC + q: the warp's 32 lanes cover 32
-        // consecutive floats of one dQ row (one 128-byte line per reduction)
-        const int q0 = q_base + g * HC;
-        float* col = qrow0 + q0 * qstride + r;
-        if (q0 + HC <= N) {
+      const int row0 = i * C::BM + quarter * 32;     // first query row of this warp's box
 #pragma unroll
-          for (int q = 0; q < HC; ++q) red_add_f32(col + q * qstride, __uint_as_float(v[q]));
-        } else {
-#pragma unroll
-          for (int q = 0; q < HC; ++q)
-            if (q0 + q < N) red_add_f32(col + q * qstride, __uint_as_float(v[q]));
+      for (int bx = 0; bx < HC / 32; ++bx) {
+        if (pending) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
         }
-      } else {
-        // lane r = query; columns g HC .. g HC + HC of its dQ row
-        const int q_g = q_base + r;
-        if (q_g < N) {
-          float* dst = qrow0 + q_g * qstride + g * HC;
 #pragma unroll
-          for (int e = 0; e < HC; e += 4)
-            red_add_v4(dst + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                       __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(stg_row + ((c ^ (lane & 7)) * 16), v[32 * bx + 4 * c], v[32 * bx + 4 * c + 1],
+                       v[32 * bx + 4 * c + 2], v[32 * bx + 4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int col = g * HC + 32 * bx;
+          if constexpr (PACKED)
+            tma_reduce_add_4d(&tmDQ, stg, col, seq0 + row0, hq, 0);
+          else
+            tma_reduce_add_3d(&tmDQ, stg, col, row0, b * kp.H + hq);
+          bulk_commit_group();
         }
+        pending = true;
       }
     }
+    // every reduce this warp issued has finished before the CTA ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   // ------------------------------------------------------------ teardown
@@ -642,9 +689,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   if (bars.abort_flag) {
     if (warp == C::LOAD_WARP && lane == 0) {
       mbar_wait_drain(&bars.kv_full, 0);
-      const int issued = bars.load_items;
-      for (int s = 0; s < C::NST && s < issued; ++s)
-        mbar_wait_drain(&bars.stage_full[s], ((issued - 1 - s) / C::NST) & 1);
+      const int nq = bars.q_items;
+      for (int s = 0; s < C::NQS && s < nq; ++s)
+        mbar_wait_drain(&bars.q_full[s], ((nq - 1 - s) / C::NQS) & 1);
+      const int nd = bars.do_items;
+      for (int s = 0; s < C::NDS && s < nd; ++s)
+        mbar_wait_drain(&bars.do_full[s], ((nd - 1 - s) / C::NDS) & 1);
     }
     if (warp == C::MMA_WARP && lane == 0) {
       mma_commit(&bars.drain);
@@ -678,7 +728,7 @@ attn_status_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
     auto kern = bwd_main_kernel<D, CAUSAL, FP16, PACKED>;
     attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
     if (s != ATTN_OK) return s;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if constexpr (PACKED) {
       // {d, total tokens, heads, 1}: token stride heads * d, head stride d
       const uint64_t T = static_cast<uint64_t>(p.total);
@@ -690,6 +740,10 @@ attn_status_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
         return s;
       if ((s = make_tmap_4d(&tv, p.v, 2, D, T, p.H_kv, 1, kvr, 2ull * D, T * kvr, 64, 128)) != ATTN_OK)
         return s;
+      // float32 dQ accumulator [total, H, d]: reduce boxes of 32 rows x 32 columns
+      const uint64_t ar = 4ull * p.H * D;
+      if ((s = make_tmap_4d(&tdq, p.dq_acc, 4, D, T, p.H, 1, ar, 4ull * D, T * ar, 32, 32)) != ATTN_OK)
+        return s;
     } else {
       // {d, N, B * heads}
       const uint64_t pq = static_cast<uint64_t>(p.B) * p.H, pkv = static_cast<uint64_t>(p.B) * p.H_kv;
@@ -697,6 +751,8 @@ attn_status_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
       if ((s = make_tmap_3d(&tdo, p.dout, 2, D, p.N, pq, 64, 128)) != ATTN_OK) return s;
       if ((s = make_tmap_3d(&tk, p.k, 2, D, p.N, pkv, 64, 128)) != ATTN_OK) return s;
       if ((s = make_tmap_3d(&tv, p.v, 2, D, p.N, pkv, 64, 128)) != ATTN_OK) return s;
+      // float32 dQ accumulator [B * H, N, d]: reduce boxes of 32 rows x 32 columns
+      if ((s = make_tmap_3d(&tdq, p.dq_acc, 4, D, p.N, pq, 32, 32)) != ATTN_OK) return s;
     }
     int* status = device_status_word();
     if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
@@ -705,7 +761,7 @@ attn_status_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
                   p.scale * kLog2e};
     const unsigned ntiles = static_cast<unsigned>((p.N + 127) / 128);
     const dim3 grid = CAUSAL ? dim3(ntiles * p.H_kv * p.B, 1, 1) : dim3(ntiles, p.H_kv, p.B);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, kp);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e, "backward main launch");
   }

@@ -24,7 +24,8 @@ int* device_status_word();
 attn_status_t check_device();
 
 // 3-D tensor map over a contiguous [planes][rows][inner] array with a
-// (box_inner x box_rows x 1) box and 128-byte swizzle.  elem_bytes is 1 or 2.
+// (box_inner x box_rows x 1) box and 128-byte swizzle.  elem_bytes is 1 or 2
+// (raw bytes / 16-bit words), or 4 (float32, the type a reduce-add needs).
 attn_status_t make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
                            uint64_t rows, uint64_t planes, uint32_t box_inner,
                            uint32_t box_rows);
