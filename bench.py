@@ -42,10 +42,10 @@ WORKLOAD = "attention step (bf16 fwd + bf16 bwd + fp8 pre-pass + fp8 fwd), B=2 H
 # kernel's source files when the capture was taken; once they change, the
 # figure no longer describes the kernel and the line reports traffic as null.
 NCU_TRAFFIC = {
-    "fwd_bf16": {"bytes": 247_391_232, "src": "7adb41e55b6db581"},      # 201.4 MB read + 46.0 MB write
-    "bwd_bf16": {"bytes": 622_883_328, "src": "607f42aa0d0c770c"},      # 404.9 MB read + 218.0 MB write
-    "fwd_fp8": {"bytes": 130_830_848, "src": "29942f781a455ab6"},       # 100.9 MB read + 29.9 MB write
-    "fp8_prepass": {"bytes": 268_395_264, "src": "29942f781a455ab6"},   # 201.4 MB read + 67.0 MB write
+    "fwd_bf16": {"bytes": 247_716_608, "src": "533a5703aca929b9"},      # 201.4 MB read + 46.3 MB write
+    "bwd_bf16": {"bytes": 623_137_536, "src": "ce67d0247e0c40db"},      # 405.0 MB read + 218.1 MB write
+    "fwd_fp8": {"bytes": 130_528_512, "src": "95917a811a77b3f6"},       # 100.8 MB read + 29.7 MB write
+    "fp8_prepass": {"bytes": 268_293_120, "src": "95917a811a77b3f6"},   # 201.4 MB read + 66.9 MB write
 }
 KERNEL_SOURCES = {"fwd_bf16": "fwd.cu", "bwd_bf16": "bwd.cu", "fwd_fp8": "fp8.cu",
                   "fp8_prepass": "fp8.cu"}
