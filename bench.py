@@ -470,7 +470,8 @@ def run_ablation(torch, attn, stream, causal, scale, q, k, v):
     (two query tiles per CTA alternating on the tensor core, lazy rescaling)
     against one query tile per CTA (nothing fills the tensor core while a
     tile's softmax runs) and eager rescaling (the output accumulator rescaled
-    whenever the row max grows).  TFLOP/s of the same algorithmic FLOP."""
+    whenever the row max grows); and the FP8 forward with a quarter of its
+    exponentials evaluated on the FMA pipe.  TFLOP/s of the same algorithmic FLOP."""
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     flop = fwd_flop(causal)
@@ -479,6 +480,15 @@ def run_ablation(torch, attn, stream, causal, scale, q, k, v):
                         ("one_tile_eager_rescale", 3)):
         fn = lambda: attn.attn_fwd_schedule(q, k, v, sched, causal=causal, softmax_scale=scale,
                                             o=o, lse=lse, stream=stream)
+        ms = time_call(torch, stream, fn)
+        out[name] = {"ms": round(ms, 4), "tflops": round(flop / (ms * 1e-3) / 1e12, 1)}
+    # FP8 forward with a quarter of its exponentials on the FMA pipe
+    signs = torch.where(torch.arange(q.shape[-1], device=q.device) % 3 == 0, -1.0, 1.0).float()
+    (q8, k8, v8), (qs, ks, vs) = attn.attn_fp8_quantize_bf16(q, k, v, signs, stream=stream)
+    o8 = torch.empty_like(q)
+    for name, sched in (("fp8_default", 0), ("fp8_exp2_poly_quarter", attn.ATTN_SCHED_EXP2_POLY)):
+        fn = lambda: attn.attn_fwd_fp8_schedule(q8, k8, v8, qs, ks, vs, sched, causal=causal,
+                                                softmax_scale=scale, o=o8, lse=lse, stream=stream)
         ms = time_call(torch, stream, fn)
         out[name] = {"ms": round(ms, 4), "tflops": round(flop / (ms * 1e-3) / 1e12, 1)}
     assert attn.attn_get_device_status() == 0, attn.attn_last_error()

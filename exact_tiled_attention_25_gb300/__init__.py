@@ -32,12 +32,13 @@ _DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 ATTN_SCHED_DEFAULT = 0
 ATTN_SCHED_ONE_TILE = 1
 ATTN_SCHED_EAGER_RESCALE = 2
+ATTN_SCHED_EXP2_POLY = 4
 
 __all__ = ["AttnError", "attn_fwd", "attn_fwd_schedule", "attn_fwd_gqa", "attn_fwd_varlen", "attn_bwd",
            "attn_bwd_gqa", "attn_bwd_varlen", "attn_bwd_varlen_workspace_size",
            "attn_bwd_workspace_size",
            "attn_fp8_quantize", "attn_fp8_quantize_gqa", "attn_fp8_quantize_rope", "attn_fwd_fp8",
-           "attn_fwd_fp8_gqa", "attn_fp8_quantize_varlen", "attn_fwd_fp8_varlen",
+           "attn_fwd_fp8_gqa", "attn_fwd_fp8_schedule", "attn_selftest_exp2", "attn_fp8_quantize_varlen", "attn_fwd_fp8_varlen",
            "attn_fp8_quantize_bf16",
            "attn_decode_paged", "attn_decode_paged_fp8", "attn_decode_workspace_size",
            "attn_get_device_status",
@@ -530,6 +531,38 @@ def attn_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, causal: bool = Fal
     if host:
         return o.cpu(), lse.cpu()
     return o, lse
+
+
+def attn_fwd_fp8_schedule(q8, k8, v8, q_descale, k_descale, v_descale, schedule: int,
+                          causal: bool = False, softmax_scale: float | None = None, o=None,
+                          lse=None, stream=None):
+    """attn_fwd_fp8 with a schedule variant (0 or ATTN_SCHED_EXP2_POLY), for measurement."""
+    lib = _lib.load()
+    B, H, N, d = _shape4(q8, "q8")
+    for t, n in ((k8, "k8"), (v8, "v8")):
+        if _shape4(t, n) != (B, H, N, d):
+            raise ValueError("q8, k8, v8 must have the same shape")
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    code = lib.attn_fwd_fp8_schedule(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_descale),
+                                     _ptr(k_descale), _ptr(v_descale), _ptr(o), _ptr(lse), B, H, N,
+                                     d, int(bool(causal)), scale, int(schedule), _stream(stream))
+    _check(code, "attn_fwd_fp8_schedule")
+    return o, lse
+
+
+def attn_selftest_exp2(x, stream=None):
+    """(2^x by the FMA-pipe polynomial, 2^x by ex2.approx) for a float32 device tensor x."""
+    lib = _lib.load()
+    if x.dtype != torch.float32 or not x.is_contiguous() or x.device.type != "cuda":
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    y_poly, y_mufu = torch.empty_like(x), torch.empty_like(x)
+    code = lib.attn_selftest_exp2(_ptr(x), _ptr(y_poly), _ptr(y_mufu), x.numel(), _stream(stream))
+    _check(code, "attn_selftest_exp2")
+    return y_poly, y_mufu
 
 
 def attn_fwd_fp8_gqa(q8, k8, v8, q_descale, k_descale, v_descale, causal: bool = False,

@@ -561,6 +561,38 @@ attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* 
                           causal, softmax_scale, stream);
 }
 
+attn_status_t attn_fwd_fp8_schedule(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
+                                    const float* q_descale, const float* k_descale,
+                                    const float* v_descale, void* o, float* lse, int B, int H,
+                                    int N, int d, int causal, float softmax_scale, int schedule,
+                                    cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if ((s = check_shape(B, H, N, d, causal)) != ATTN_OK) return s;
+  if ((s = check_ptrs({q8, k8, v8, o, lse})) != ATTN_OK) return s;
+  if (!q_descale || !k_descale || !v_descale)
+    return fail(ATTN_ERR_INVALID_ARG, "null descale pointer");
+  if ((s = check_scale(softmax_scale)) != ATTN_OK) return s;
+  if (schedule != 0 && schedule != ATTN_SCHED_EXP2_POLY)
+    return fail(ATTN_ERR_INVALID_ARG, "schedule must be 0 or ATTN_SCHED_EXP2_POLY");
+  if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
+  if ((s = check_device()) != ATTN_OK) return s;
+  Fp8FwdParams p{q8, k8, v8, q_descale, k_descale, v_descale, o, lse, B, H, N, d, causal,
+                 softmax_scale, H};
+  p.exp2_poly = schedule == ATTN_SCHED_EXP2_POLY ? 1 : 0;
+  return launch_fwd_fp8(p, stream);
+}
+
+attn_status_t attn_selftest_exp2(const float* x, float* y_poly, float* y_mufu, long long n,
+                                 cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if (n < 1 || n > (1ll << 30)) return fail(ATTN_ERR_INVALID_ARG, "n must be in [1, 2^30]");
+  if (!x || !y_poly || !y_mufu) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if ((s = check_device()) != ATTN_OK) return s;
+  return launch_exp2_selftest(x, y_poly, y_mufu, n, stream);
+}
+
 attn_status_t attn_fwd_fp8_varlen(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
                                   const float* q_descale, const float* k_descale,
                                   const float* v_descale, void* o, float* lse,

@@ -108,9 +108,13 @@ struct Fp8FwdParams {
   int H_kv;   // heads of K and V (H % H_kv == 0)
   const int* cu_seqlens = nullptr;   // packed batch: device [B + 1] offsets (N = longest)
   int total = 0;                     // packed batch: tokens
+  int exp2_poly = 0;                 // a quarter of the exponentials on the FMA pipe (measurement variant)
 };
 
 attn_status_t launch_fwd(const FwdParams& p, cudaStream_t stream);
+// exp2_poly2 and ex2.approx on the same n inputs (diagnostic).
+attn_status_t launch_exp2_selftest(const float* x, float* y_poly, float* y_mufu, long long n,
+                                   cudaStream_t stream);
 // Schedule variants of the forward kernel (ATTN_SCHED_* flags), for measurement.
 attn_status_t launch_fwd_sched(const FwdParams& p, int sched, cudaStream_t stream);
 // Persistent forward (cluster launch control) for packed causal batches.

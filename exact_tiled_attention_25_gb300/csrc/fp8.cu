@@ -368,7 +368,11 @@ __device__ __forceinline__ float lg2_approx8(float x) {
 // descales [B, heads, ceil(max_seqlen / 128)] per sequence's 128-row blocks, O
 // [total, H, d], LSE [H, total]; kp.N is the longest sequence; query and key
 // tiles are read at the sequence's first token by 4-D tensor maps.
-template <bool CAUSAL, bool PACKED>
+// POLY: the first of every four 4-key groups of a softmax thread (a quarter
+// of its exponentials) is evaluated by exp2_poly2 on the FMA pipe instead of
+// the MUFU unit -- a measurement variant (it measured slower: the softmax
+// here is bound by instruction issue, not by the MUFU rate).
+template <bool CAUSAL, bool PACKED, bool POLY = false>
 __global__ void __launch_bounds__(THREADS8, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Fp8KParams kp) {
@@ -633,10 +637,20 @@ __global__ void __launch_bounds__(THREADS8, 1)
           const int c = c0 * 32 + 4 * i;
           const uint64_t y0 = ffma2(pack2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), cc, nn);
           const uint64_t y1 = ffma2(pack2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), cc, nn);
-          const float p0 = ex2_approx(lo2(y0));
-          const float p1 = ex2_approx(hi2(y0));
-          const float p2 = ex2_approx(lo2(y1));
-          const float p3 = ex2_approx(hi2(y1));
+          float p0, p1, p2, p3;
+          if (POLY && (i & 3) == 0) {
+            const uint64_t e0 = exp2_poly2(lo2(y0), hi2(y0));
+            const uint64_t e1 = exp2_poly2(lo2(y1), hi2(y1));
+            p0 = lo2(e0);
+            p1 = hi2(e0);
+            p2 = lo2(e1);
+            p3 = hi2(e1);
+          } else {
+            p0 = ex2_approx(lo2(y0));
+            p1 = ex2_approx(hi2(y0));
+            p2 = ex2_approx(lo2(y1));
+            p3 = ex2_approx(hi2(y1));
+          }
           acc0 = fadd2(acc0, pack2(p0, p1));
           acc1 = fadd2(acc1, pack2(p2, p3));
           pk[i] = cvt_pack_e4m3x4(p0, p1, p2, p3);
@@ -725,6 +739,23 @@ __global__ void __launch_bounds__(THREADS8, 1)
   }
 }
 
+// Evaluates exp2_poly2 and ex2.approx on the same inputs (diagnostic entry
+// point attn_selftest_exp2).
+__global__ void exp2_selftest_kernel(const float* __restrict__ x, float* __restrict__ y_poly,
+                                     float* __restrict__ y_mufu, long long n) {
+  const long long i = 2 * (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float a = x[i];
+  const float b = (i + 1 < n) ? x[i + 1] : 0.f;
+  const uint64_t e = exp2_poly2(a, b);
+  y_poly[i] = lo2(e);
+  y_mufu[i] = ex2_approx(a);
+  if (i + 1 < n) {
+    y_poly[i + 1] = hi2(e);
+    y_mufu[i + 1] = ex2_approx(b);
+  }
+}
+
 // Block mode, or the per-tensor comparator (block amaxes, one reduction, codes).
 template <bool BF16IN>
 void launch_quant_modes(const Fp8QuantParams& p, dim3 grid, int nblk, int kv_planes,
@@ -747,6 +778,16 @@ void launch_quant_modes(const Fp8QuantParams& p, dim3 grid, int nblk, int kv_pla
 }
 
 }  // namespace
+
+attn_status_t launch_exp2_selftest(const float* x, float* y_poly, float* y_mufu, long long n,
+                                   cudaStream_t stream) {
+  const long long pairs = (n + 1) / 2;
+  exp2_selftest_kernel<<<static_cast<unsigned>((pairs + 255) / 256), 256, 0, stream>>>(x, y_poly,
+                                                                                        y_mufu, n);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "exp2 self-test launch");
+  return ATTN_OK;
+}
 
 attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) {
   if (p.d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
@@ -786,9 +827,9 @@ attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) 
   return ATTN_OK;
 }
 
-template <bool CAUSAL, bool PACKED>
+template <bool CAUSAL, bool PACKED, bool POLY = false>
 attn_status_t launch_fwd_fp8_t(const Fp8FwdParams& p, cudaStream_t stream) {
-  auto kern = fwd_fp8_kernel<CAUSAL, PACKED>;
+  auto kern = fwd_fp8_kernel<CAUSAL, PACKED, POLY>;
   attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), SMEM8);
   if (s != ATTN_OK) return s;
   CUtensorMap tq, tk, tv;
@@ -827,6 +868,11 @@ attn_status_t launch_fwd_fp8(const Fp8FwdParams& p, cudaStream_t stream) {
   if (p.d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
   if (p.N > 65535 * 256 || p.H > 65535 || p.B > 65535)
     return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
+  if (p.exp2_poly) {
+    if (p.cu_seqlens) return fail(ATTN_ERR_UNSUPPORTED, "the exp2 variant takes fixed-length batches");
+    return p.causal ? launch_fwd_fp8_t<true, false, true>(p, stream)
+                    : launch_fwd_fp8_t<false, false, true>(p, stream);
+  }
   if (p.cu_seqlens)
     return p.causal ? launch_fwd_fp8_t<true, true>(p, stream) : launch_fwd_fp8_t<false, true>(p, stream);
   return p.causal ? launch_fwd_fp8_t<true, false>(p, stream) : launch_fwd_fp8_t<false, false>(p, stream);

@@ -501,6 +501,32 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// 2^x for two packed float32 lanes on the FMA and integer pipes instead of the
+// MUFU unit, for x <= 126 (the softmax only sees x <= 8); x <= -127 (and -inf)
+// gives exactly +0.  Method: round-to-nearest range reduction x = j + f, |f| <=
+// 1/2, through the float32 "magic constant" 1.5 * 2^23 (after t = x + 1.5 * 2^23
+// the low bits of t hold j and t - 1.5 * 2^23 = j exactly); 2^f by a cubic
+// 1 + f (c1 + f (c2 + f c3)) whose coefficients were fitted for this library by
+// a minimax (Lawson-reweighted least squares) fit of the relative error on
+// [-1/2, 1/2] with the constant term fixed at 1 -- maximum relative error
+// 1.02e-4 evaluated in float32, below the rounding of P to 16 or 8 bits; then
+// 2^j by adding j << 23 to the exponent field of 2^f (bits(t) << 23 is j << 23
+// modulo 2^32, since the magic constant's low 9 bits are zero).  With
+// x = -127: j = -127, f = 0, 2^f = 1 exactly, and the exponent field becomes 0.
+__device__ __forceinline__ uint64_t exp2_poly2(float xlo, float xhi) {
+  constexpr float kMagic = 12582912.0f;                       // 1.5 * 2^23
+  const uint64_t x = pack2(fmaxf(xlo, -127.f), fmaxf(xhi, -127.f));
+  const uint64_t t = fadd2(x, pack2(kMagic, kMagic));          // low bits: round(x)
+  const uint64_t r = fadd2(t, pack2(-kMagic, -kMagic));        // round(x), exactly
+  const uint64_t f = ffma2(r, pack2(-1.f, -1.f), x);           // x - round(x), exactly
+  uint64_t p = ffma2(f, pack2(0x1.c2a0c4p-5f, 0x1.c2a0c4p-5f), pack2(0x1.f00b7cp-3f, 0x1.f00b7cp-3f));
+  p = ffma2(p, f, pack2(0x1.62f5f8p-1f, 0x1.62f5f8p-1f));
+  p = ffma2(p, f, pack2(1.f, 1.f));
+  const uint32_t lo = static_cast<uint32_t>(p) + (static_cast<uint32_t>(t) << 23);
+  const uint32_t hi = static_cast<uint32_t>(p >> 32) + (static_cast<uint32_t>(t >> 32) << 23);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 // Two fp32 -> packed 16-bit pair, round to nearest even; `lo` lands in the low half.
 __device__ __forceinline__ uint32_t cvt_pack_bf16(float lo, float hi) {
   uint32_t r;

@@ -87,8 +87,10 @@ enum {
   ATTN_SCHED_DEFAULT = 0,
   ATTN_SCHED_ONE_TILE = 1,       /* one 128-row query tile per CTA: while its softmax
                                     runs, the tensor core has no second tile to work on */
-  ATTN_SCHED_EAGER_RESCALE = 2   /* rescale the output accumulator whenever the row max
+  ATTN_SCHED_EAGER_RESCALE = 2,  /* rescale the output accumulator whenever the row max
                                     grows, instead of only when it grows by more than 2^8 */
+  ATTN_SCHED_EXP2_POLY = 4       /* FP8 forward only: a quarter of the exponentials on the
+                                    FMA pipe (a fitted cubic) instead of the MUFU unit */
 };
 
 /*
@@ -447,6 +449,35 @@ attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* 
                            const float* q_descale, const float* k_descale,
                            const float* v_descale, void* o, float* lse, int B, int H, int N,
                            int d, int causal, float softmax_scale, cudaStream_t stream);
+
+/*
+ * attn_fwd_fp8_schedule -- attn_fwd_fp8 with a schedule variant, for
+ * measurement.  `schedule` is 0 (exactly attn_fwd_fp8) or ATTN_SCHED_EXP2_POLY:
+ * a quarter of each softmax thread's exponentials are evaluated on the FMA
+ * pipe by range reduction and a cubic (relative error <= 1.1e-4, below the
+ * e4m3 rounding of P) instead of by the MUFU unit.  Other values return
+ * ATTN_ERR_INVALID_ARG.  Arguments, layout and errors as attn_fwd_fp8.
+ * Source: "FlashAttention-3: Hopper Asynchrony and FP8 Attention", section
+ * "Why This Exists" (FP8 doubles the matrix-multiply rate but not the rate of
+ * exponentials).
+ */
+attn_status_t attn_fwd_fp8_schedule(const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
+                                    const float* q_descale, const float* k_descale,
+                                    const float* v_descale, void* o, float* lse, int B, int H,
+                                    int N, int d, int causal, float softmax_scale, int schedule,
+                                    cudaStream_t stream);
+
+/*
+ * attn_selftest_exp2 -- diagnostic: evaluates, for n float32 inputs x, the
+ * FMA-pipe exponential of ATTN_SCHED_EXP2_POLY (y_poly) and the MUFU
+ * approximation the kernels otherwise use (y_mufu), both 2^x.  x, y_poly and
+ * y_mufu are device arrays of n floats; the call is asynchronous on `stream`.
+ * Defined for x <= 126; x <= -127 (and -inf) give exactly 0 in y_poly.  The
+ * pages give no such routine; it exists so the approximation can be checked
+ * against the exact function on the GPU.
+ */
+attn_status_t attn_selftest_exp2(const float* x, float* y_poly, float* y_mufu, long long n,
+                                 cudaStream_t stream);
 
 /*
  * attn_fwd_fp8_varlen -- FP8 forward on a packed batch (the output of

@@ -264,3 +264,54 @@ def test_timed_fp8_chain_full_size(attn, causal):
         (np.sqrt(np.mean(e ** 2)), np.abs(e).max())
     e = np.concatenate([x.ravel() for x in err_exact])
     assert np.sqrt(np.mean(e ** 2)) <= FP8_RMSE, np.sqrt(np.mean(e ** 2))
+
+
+def test_exp2_polynomial_error_on_the_gpu(attn):
+    """The FMA-pipe exponential of the ATTN_SCHED_EXP2_POLY variant against the
+    exact 2^x (float64) and against the MUFU ex2.approx on the GPU: relative
+    error <= 1.1e-4 over the softmax's range, exactly 0 at and below -127 and
+    at -inf, and 1 at 0."""
+    xs = np.concatenate([np.linspace(-126.0, 8.0, 2_000_001), np.arange(-126, 9, dtype=np.float64),
+                         np.arange(-126, 8, dtype=np.float64) + 0.5,
+                         [-np.inf, -1e30, -200.0, -127.0, -127.0 + 1e-3, -126.75, 0.0, -0.0]])
+    x = torch.from_numpy(xs.astype(np.float32)).to(dev())
+    y_poly, y_mufu = attn.attn_selftest_exp2(x)
+    check_status(attn)
+    xf = x.double().cpu().numpy()
+    yp = y_poly.double().cpu().numpy()
+    ym = y_mufu.double().cpu().numpy()
+    exact = np.exp2(xf)
+    normal = (xf >= -126.0) & (xf <= 8.0)
+    rel = np.abs(yp[normal] / exact[normal] - 1.0)
+    assert rel.max() <= 1.1e-4, rel.max()
+    # the MUFU path as the kernels use it, for reference: far tighter
+    assert np.abs(ym[normal & (xf >= -125.0)] / exact[normal & (xf >= -125.0)] - 1.0).max() <= 1e-6
+    assert np.all(yp[xf <= -127.0] == 0.0)
+    tiny = (xf > -127.0) & (xf < -126.0)
+    assert np.all((yp[tiny] >= 0.0) & (yp[tiny] <= 2.0 ** -126))
+    assert np.all(yp[xf == 0.0] == 1.0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [129, 640])
+def test_fp8_exp2_poly_variant_matches_dequantised_oracle(attn, N, causal):
+    """The forward with a quarter of its exponentials on the FMA pipe computes
+    the same attention (the polynomial's error is far below the e4m3 rounding of P)."""
+    B, H, d = 1, 2, 128
+    q, k, v = workloads.normal_with_outliers(60 + N, (B, H, N, d), 3)
+    signs = workloads.random_signs(5, d)
+    gq, gk, gv = (torch.from_numpy(x).to(dev()) for x in (q, k, v))
+    (q8, k8, v8), (qd, kd, vd) = attn.attn_fp8_quantize(gq, gk, gv,
+                                                        hadamard_signs=torch.from_numpy(signs).to(dev()))
+    o, lse = attn.attn_fwd_fp8_schedule(q8, k8, v8, qd, kd, vd, attn.ATTN_SCHED_EXP2_POLY,
+                                        causal=causal, softmax_scale=1 / np.sqrt(d))
+    o0, _ = attn.attn_fwd_fp8(q8, k8, v8, qd, kd, vd, causal=causal, softmax_scale=1 / np.sqrt(d))
+    check_status(attn)
+    deq = [oracle.dequantize_e4m3_blocks(c.cpu().numpy(), s.cpu().numpy())
+           for c, s in ((q8, qd), (k8, kd), (v8, vd))]
+    ref_o, ref_l = oracle.attention_forward(*deq, 1 / np.sqrt(d), causal)
+    diff = o.float().cpu().numpy() - ref_o
+    assert np.sqrt(np.mean(diff ** 2)) <= 1e-2 * max(1.0, np.sqrt(np.mean(ref_o ** 2)))
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_l, atol=2e-3)
+    # and close to the MUFU-only forward
+    assert (o.float() - o0.float()).pow(2).mean().sqrt().item() <= 2e-3
