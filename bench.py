@@ -171,6 +171,11 @@ def run_ours(args, rank, world):
     qs, ks, vs = (torch.empty((B, H, nblk), dtype=torch.float32, device=dev) for _ in range(3))
     o8 = torch.empty_like(q)
     lse8 = torch.empty_like(lse)
+    rope = None
+    if args.rope:
+        # rotary tables: model constants, resident on the device like weights
+        import workloads
+        rope = tuple(torch.from_numpy(t).to(dev) for t in workloads.rope_tables(N, D))
 
     parts = {}
 
@@ -183,6 +188,15 @@ def run_ours(args, rank, world):
 
     def part_quant():
         lib = attn.load_library()
+        if rope is not None:
+            code = lib.attn_fp8_quantize_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), 1,
+                                            rope[0].data_ptr(), rope[1].data_ptr(), signs.data_ptr(),
+                                            q8.data_ptr(), k8.data_ptr(), v8.data_ptr(),
+                                            qs.data_ptr(), ks.data_ptr(), vs.data_ptr(), None,
+                                            B, N, 0, H, H, D, 0, stream.cuda_stream)
+            if code:
+                raise attn.AttnError(code, "attn_fp8_quantize_ex")
+            return
         code = lib.attn_fp8_quantize_bf16(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                           signs.data_ptr(), q8.data_ptr(), k8.data_ptr(),
                                           v8.data_ptr(), qs.data_ptr(), ks.data_ptr(), vs.data_ptr(),
@@ -213,6 +227,8 @@ def run_ours(args, rank, world):
 
     # prepass algorithmic bytes: read 3 bf16 tensors, write 3 e4m3 tensors + descales
     prepass_bytes = 3 * B * H * N * D * (2 + 1) + 3 * B * H * nblk * 4
+    if rope is not None:
+        prepass_bytes += 2 * N * (D // 2) * 4
 
     for _ in range(args.warmup):
         for _, fn, _, _ in step_parts:
@@ -287,7 +303,7 @@ def run_ours(args, rank, world):
     roof["peak_source"] = (f"{pk['source']} MEASURED_PEAKS.json bf16_tflops (burst: the kernel is "
                            "timed alone, well under a second, at full clocks); fp8 = 2x bf16")
 
-    e2e = run_e2e(args, torch, attn, dev, stream, step_parts, causal, scale, q, k, v, do, signs)
+    e2e = run_e2e(args, torch, attn, dev, stream, step_parts, causal, scale, q, k, v, do, signs, rope)
     ablation = run_ablation(torch, attn, stream, causal, scale, q, k, v) if args.sweep else None
     sweep = run_sweep(torch, attn, dev, stream, causal) if args.sweep else None
     fp8_acc = run_fp8_accuracy(torch, attn, dev) if args.sweep else None
@@ -300,6 +316,7 @@ def run_ours(args, rank, world):
         "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D, "causal": causal,
                    "global_batch": B * world, "seq_len": N, "parallelism": f"replicas{world}",
                    "step": [n for n, *_ in step_parts], "not_built": skipped,
+                   "fp8_prepass_rotary": bool(args.rope),
                    "l2": "no flush: Q/K/V/dO/O (bf16, 67 MB each) exceed the 129 MB L2"},
         "breakdown": breakdown,
         "roofline": roof,
@@ -318,7 +335,7 @@ def run_ours(args, rank, world):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, torch, attn, dev, stream, step_parts, causal, scale, q, k, v, do, signs):
+def run_e2e(args, torch, attn, dev, stream, step_parts, causal, scale, q, k, v, do, signs, rope=None):
     """The same step through the public API with inputs in pinned host memory:
     host-to-device copies of every step's inputs and device-to-host copies of
     every output are inside the timed region.
@@ -367,8 +384,12 @@ def run_e2e(args, torch, attn, dev, stream, step_parts, causal, scale, q, k, v, 
                           causal=causal, softmax_scale=scale, dq=outs["dq"], dk=outs["dk"],
                           dv=outs["dv"], workspace=outs["ws"], stream=s)
         if "fp8_prepass" in names:
-            (q8, k8, v8), (qs, ks, vs) = attn.attn_fp8_quantize_bf16(
-                d_in["q"], d_in["k"], d_in["v"], d_in["signs"], stream=s)
+            if rope is not None:
+                (q8, k8, v8), (qs, ks, vs) = attn.attn_fp8_quantize_ex(
+                    d_in["q"], d_in["k"], d_in["v"], rope[0], rope[1], d_in["signs"], stream=s)
+            else:
+                (q8, k8, v8), (qs, ks, vs) = attn.attn_fp8_quantize_bf16(
+                    d_in["q"], d_in["k"], d_in["v"], d_in["signs"], stream=s)
             if "fwd_fp8" in names:
                 attn.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=causal, softmax_scale=scale,
                                   o=outs["o8"], lse=outs["lse8"], stream=s)
@@ -558,6 +579,7 @@ def run_sweep(torch, attn, dev, stream, causal, steps=20, warmup=3):
     out.update(run_varlen_gqa(torch, attn, dev, stream, causal, steps, warmup))
     out.update(run_fp8_gqa(torch, attn, dev, stream, causal, steps, warmup))
     out.update(run_prepass_rope(torch, attn, dev, stream, steps, warmup))
+    out.update(run_prepass_rope_bf16(torch, attn, dev, stream, steps, warmup))
     out.update(run_decode(torch, attn, dev, stream, steps, warmup))
     out.update(run_decode_fp8(torch, attn, dev, stream, steps, warmup))
     assert attn.attn_get_device_status() == 0, attn.attn_last_error()
@@ -668,6 +690,24 @@ def run_prepass_rope(torch, attn, dev, stream, steps=20, warmup=3):
     nbytes = 3 * B * H * N * D * (4 + 1) + 3 * B * H * nblk * 4 + 2 * N * (D // 2) * 4
     return {f"fp8_prepass_rope_b{B}h{H}n{N}d{D}": {"ms": round(ms, 4),
                                                     "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}}
+
+
+def run_prepass_rope_bf16(torch, attn, dev, stream, steps=20, warmup=3):
+    """The FP8 pre-pass on bfloat16 inputs with rotary embedding and the
+    Hadamard transform (attn_fp8_quantize_ex) at the timed shape: GB/s of
+    algorithmic bytes (read 3 bfloat16 tensors and the two [N, d/2] tables,
+    write 3 e4m3 tensors and the descales)."""
+    import workloads
+    g = torch.Generator(device=dev).manual_seed(13)
+    q, k, v = (torch.randn((B, H, N, D), generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+    cos, sin = (torch.from_numpy(t).to(dev) for t in workloads.rope_tables(N, D))
+    signs = torch.where(torch.rand(D, generator=g, device=dev) < 0.5, -1.0, 1.0).float()
+    fn = lambda: attn.attn_fp8_quantize_ex(q, k, v, cos, sin, hadamard_signs=signs, stream=stream)
+    ms = time_call(torch, stream, fn, steps, warmup)
+    nblk = (N + 127) // 128
+    nbytes = 3 * B * H * N * D * (2 + 1) + 3 * B * H * nblk * 4 + 2 * N * (D // 2) * 4
+    return {f"fp8_prepass_rope_bf16_b{B}h{H}n{N}d{D}": {"ms": round(ms, 4),
+                                                         "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}}
 
 
 def run_fp8_gqa(torch, attn, dev, stream, causal, steps=20, warmup=3):
@@ -808,6 +848,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--rope", action="store_true",
+                    help="the step's FP8 pre-pass also applies rotary embedding to Q and K")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false",
                     help="skip the head-dimension sweep")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")

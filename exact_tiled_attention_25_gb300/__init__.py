@@ -39,7 +39,7 @@ __all__ = ["AttnError", "attn_fwd", "attn_fwd_schedule", "attn_fwd_gqa", "attn_f
            "attn_bwd_workspace_size",
            "attn_fp8_quantize", "attn_fp8_quantize_gqa", "attn_fp8_quantize_rope", "attn_fwd_fp8",
            "attn_fwd_fp8_gqa", "attn_fwd_fp8_schedule", "attn_selftest_exp2", "attn_fp8_quantize_varlen", "attn_fwd_fp8_varlen",
-           "attn_fp8_quantize_bf16",
+           "attn_fp8_quantize_bf16", "attn_fp8_quantize_ex",
            "attn_decode_paged", "attn_decode_paged_fp8", "attn_decode_workspace_size",
            "attn_get_device_status",
            "attn_status_string", "attn_last_error", "load_library"]
@@ -689,4 +689,48 @@ def attn_fp8_quantize_bf16(q, k, v, hadamard_signs=None, per_tensor: bool = Fals
     _check(code, "attn_fp8_quantize_bf16")
     if host:
         return tuple(t.cpu() for t in outs), tuple(t.cpu() for t in desc)
+    return tuple(outs), tuple(desc)
+
+
+def attn_fp8_quantize_ex(q, k, v, rope_cos=None, rope_sin=None, hadamard_signs=None,
+                         cu_seqlens=None, max_seqlen: int | None = None, per_tensor: bool = False,
+                         stream=None):
+    """The FP8 pre-pass with every option: float32 or bfloat16 inputs (from the
+    tensors' dtype), optional rotary tables [N, d/2], optional Hadamard signs,
+    grouped-query heads (k, v with fewer heads), and fixed-length [B, H, N, d]
+    or packed [total, H, d] batches (with int32 cu_seqlens [B + 1] and
+    max_seqlen).  Returns (q8, k8, v8), (q_descale, k_descale, v_descale)."""
+    lib = _lib.load()
+    if q.dtype not in (torch.float32, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must all be float32 or all bfloat16")
+    for t in (q, k, v, rope_cos, rope_sin, hadamard_signs, cu_seqlens):
+        if t is not None and (t.device.type != "cuda" or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    if cu_seqlens is None:
+        B, H, N, d = _shape4(q, "q")
+        Hkv = k.shape[1]
+        total = 0
+        nblk = (N + 127) // 128
+        shapes = [(B, H, N, d), (B, Hkv, N, d), (B, Hkv, N, d)]
+        dshapes = [(B, H, nblk), (B, Hkv, nblk), (B, Hkv, nblk)]
+    else:
+        if max_seqlen is None:
+            raise ValueError("a packed batch needs max_seqlen")
+        total, H, d = _shape3(q, "q")
+        Hkv = k.shape[1]
+        B, N = cu_seqlens.numel() - 1, int(max_seqlen)
+        nblk = (N + 127) // 128
+        shapes = [(total, H, d), (total, Hkv, d), (total, Hkv, d)]
+        dshapes = [(B, H, nblk), (B, Hkv, nblk), (B, Hkv, nblk)]
+    for t, shp, n in ((q, shapes[0], "q"), (k, shapes[1], "k"), (v, shapes[2], "v")):
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{n} has shape {tuple(t.shape)}, expected {shp}")
+    outs = [torch.empty(shp, dtype=torch.uint8, device=q.device) for shp in shapes]
+    desc = [torch.empty(shp, dtype=torch.float32, device=q.device) for shp in dshapes]
+    code = lib.attn_fp8_quantize_ex(_ptr(q), _ptr(k), _ptr(v), int(q.dtype == torch.bfloat16),
+                                    _ptr(rope_cos), _ptr(rope_sin), _ptr(hadamard_signs),
+                                    *[_ptr(t) for t in outs], *[_ptr(t) for t in desc],
+                                    _ptr(cu_seqlens), B, N, total, H, Hkv, d,
+                                    int(bool(per_tensor)), _stream(stream))
+    _check(code, "attn_fp8_quantize_ex")
     return tuple(outs), tuple(desc)

@@ -452,6 +452,46 @@ attn_status_t attn_fp8_quantize_rope(const float* q, const float* k, const float
   return launch_fp8_quantize(p, stream);
 }
 
+attn_status_t attn_fp8_quantize_ex(const void* q, const void* k, const void* v, int input_bf16,
+                                   const float* rope_cos, const float* rope_sin,
+                                   const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                   uint8_t* v8, float* q_descale, float* k_descale,
+                                   float* v_descale, const int* cu_seqlens, int B, int N,
+                                   int total, int H, int H_kv, int d, int per_tensor,
+                                   cudaStream_t stream) {
+  g_last_error.clear();
+  attn_status_t s;
+  if (input_bf16 != 0 && input_bf16 != 1)
+    return fail(ATTN_ERR_INVALID_ARG, "input_bf16 must be 0 or 1");
+  if (cu_seqlens) {
+    if ((s = check_packed(B, N, total, H, d, 0)) != ATTN_OK) return s;
+    if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)
+      return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
+  } else {
+    if ((s = check_shape(B, H, N, d, 0)) != ATTN_OK) return s;
+  }
+  if ((s = check_heads(H, H_kv)) != ATTN_OK) return s;
+  if ((s = check_ptrs({q, k, v, q8, k8, v8, q_descale, k_descale, v_descale})) != ATTN_OK)
+    return s;
+  if ((rope_cos == nullptr) != (rope_sin == nullptr))
+    return fail(ATTN_ERR_INVALID_ARG, "give both rope_cos and rope_sin, or neither");
+  if (rope_cos && (!aligned16(rope_cos) || !aligned16(rope_sin)))
+    return fail(ATTN_ERR_INVALID_ARG, "rope tables must be 16-byte aligned");
+  if (hadamard_signs && !aligned16(hadamard_signs))
+    return fail(ATTN_ERR_INVALID_ARG, "hadamard_signs not 16-byte aligned");
+  if (per_tensor != 0 && per_tensor != 1)
+    return fail(ATTN_ERR_INVALID_ARG, "per_tensor must be 0 or 1");
+  if (per_tensor && (hadamard_signs || rope_cos || cu_seqlens))
+    return fail(ATTN_ERR_INVALID_ARG,
+                "the per-tensor comparator takes fixed-length inputs without Hadamard or rotation");
+  if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
+  if ((s = check_device()) != ATTN_OK) return s;
+  Fp8QuantParams p{{q, k, v}, {q8, k8, v8}, {q_descale, k_descale, v_descale}, hadamard_signs,
+                   B, H, N, d, per_tensor, rope_cos, rope_sin, H_kv, cu_seqlens,
+                   cu_seqlens ? total : 0, input_bf16};
+  return launch_fp8_quantize(p, stream);
+}
+
 size_t attn_decode_workspace_size(int B, int H, int H_kv, int n_q, int d, int max_seqlen) {
   if (B < 1 || H < 1 || H_kv < 1 || n_q < 1 || d < 1 || max_seqlen < 1) return 0;
   return decode_workspace_bytes(B, H, H_kv, n_q, d, max_seqlen);

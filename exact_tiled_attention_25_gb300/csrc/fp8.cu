@@ -39,7 +39,11 @@ constexpr float kE4m3Max = 448.f;
 // and a block is 128 rows of one sequence and head (descale [B, heads,
 // ceil(N / 128)], 1 for blocks past the sequence's end).
 // BF16IN: the inputs are bfloat16 (widened exactly to float32 on load).
-template <int MODE, bool PACKED = false, bool BF16IN = false>
+// ROPE (mode 0): Q and K rows are rotated first, from caller tables rope_cos,
+// rope_sin [N, d/2] indexed by the row's position in its sequence: the pair
+// (x_i, x_{i+d/2}) becomes (x_i c - x_{i+d/2} s, x_{i+d/2} c + x_i s).  A lane
+// holds columns 4 lane .. 4 lane + 3, so lanes l and l ^ 16 hold partners.
+template <int MODE, bool PACKED = false, bool BF16IN = false, bool ROPE = false>
 __global__ void __launch_bounds__(256)
     fp8_quant_kernel(const void* __restrict__ src0, const void* __restrict__ src1,
                      const void* __restrict__ src2, uint8_t* __restrict__ dst0,
@@ -47,7 +51,9 @@ __global__ void __launch_bounds__(256)
                      float* __restrict__ desc0, float* __restrict__ desc1,
                      float* __restrict__ desc2, const float* __restrict__ signs, int N,
                      int nblk, int kv_planes, const int* __restrict__ cu_seqlens = nullptr,
-                     int total = 0, int heads_q = 0, int heads_kv = 0, int* status = nullptr) {
+                     int total = 0, int heads_q = 0, int heads_kv = 0, int* status = nullptr,
+                     const float* __restrict__ rope_cos = nullptr,
+                     const float* __restrict__ rope_sin = nullptr) {
   constexpr int D = 128;
   const int which = blockIdx.z;
   if (which > 0 && static_cast<int>(blockIdx.y) >= kv_planes) return;   // K, V: B * H_kv planes
@@ -55,6 +61,7 @@ __global__ void __launch_bounds__(256)
   uint8_t* dst = which == 0 ? dst0 : (which == 1 ? dst1 : dst2);
   float* desc = which == 0 ? desc0 : (which == 1 ? desc1 : desc2);
   const bool hadamard = signs != nullptr && which < 2;
+  const bool rotate = ROPE && which < 2;
   const int blk = blockIdx.x;
   const int bh = blockIdx.y;
   // row r of this (b, h) lies at element row0 + r * rstride; rows r < nrows exist
@@ -101,6 +108,21 @@ __global__ void __launch_bounds__(256)
       } else {
         v = reinterpret_cast<const float4*>(static_cast<const float*>(src) + row0 + row * rstride)[lane];
       }
+    }
+    if (rotate) {
+      // position = row index in the sequence (rows past the end are zero and
+      // stay zero; their table row is clamped so every load is in bounds and
+      // can be issued early)
+      const float ox = __shfl_xor_sync(0xffffffffu, v.x, 16);
+      const float oy = __shfl_xor_sync(0xffffffffu, v.y, 16);
+      const float oz = __shfl_xor_sync(0xffffffffu, v.z, 16);
+      const float ow = __shfl_xor_sync(0xffffffffu, v.w, 16);
+      const size_t tix = static_cast<size_t>(min(row, nrows - 1)) * (D / 2) + 4 * (lane & 15);
+      const float4 c4 = __ldg(reinterpret_cast<const float4*>(rope_cos + tix));
+      const float4 sn = __ldg(reinterpret_cast<const float4*>(rope_sin + tix));
+      const float sg = (lane < 16) ? -1.f : 1.f;   // first half: x c - partner s
+      v = make_float4(fmaf(sg * ox, sn.x, v.x * c4.x), fmaf(sg * oy, sn.y, v.y * c4.y),
+                      fmaf(sg * oz, sn.z, v.z * c4.z), fmaf(sg * ow, sn.w, v.w * c4.w));
     }
     if (hadamard) {
       v.x *= s4.x; v.y *= s4.y; v.z *= s4.z; v.w *= s4.w;
@@ -797,26 +819,43 @@ attn_status_t launch_fp8_quantize(const Fp8QuantParams& p, cudaStream_t stream) 
   const int H_kv = p.H_kv > 0 ? p.H_kv : p.H;
   const int kv_planes = p.B * H_kv;
   dim3 grid(nblk, p.B * p.H, 3);
-  if ((p.cu_seqlens || p.rope_cos) && p.in_bf16)
-    return fail(ATTN_ERR_UNSUPPORTED, "bfloat16 inputs take the fixed-length pre-pass without rotation");
-  if (p.cu_seqlens) {
-    if (p.rope_cos || p.per_tensor)
-      return fail(ATTN_ERR_UNSUPPORTED, "packed batches take the block pre-pass only");
+  const bool rope = p.rope_cos != nullptr;
+  if (rope && p.per_tensor) return fail(ATTN_ERR_UNSUPPORTED, "rotation takes the block pre-pass only");
+  if (p.cu_seqlens && p.per_tensor)
+    return fail(ATTN_ERR_UNSUPPORTED, "packed batches take the block pre-pass only");
+  if (p.cu_seqlens || rope) {
     int* status = device_status_word();
     if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
-    fp8_quant_kernel<0, true><<<grid, 256, 0, stream>>>(
-        p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1], p.dst[2], p.descale[0], p.descale[1],
-        p.descale[2], p.signs, p.N, nblk, kv_planes, p.cu_seqlens, p.total, p.H, H_kv, status);
-  } else if (p.rope_cos) {
-    int* status = device_status_word();
-    if (!status) return fail(ATTN_ERR_CUDA, "status word unavailable");
-    auto kern = fp8_quant_staged_kernel<0, true>;
-    attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), QSMEM);
-    if (s != ATTN_OK) return s;
-    kern<<<grid, 256, QSMEM, stream>>>(static_cast<const float*>(p.src[0]), static_cast<const float*>(p.src[1]),
-                                       static_cast<const float*>(p.src[2]), p.dst[0], p.dst[1], p.dst[2],
-                                       p.descale[0], p.descale[1], p.descale[2], p.signs, p.N,
-                                       nblk, kv_planes, status, p.rope_cos, p.rope_sin);
+    if (rope && !p.cu_seqlens && !p.in_bf16) {
+      // float32 rows staged in shared memory by bulk copies (measured faster
+      // than holding a rotated block in registers)
+      auto kern = fp8_quant_staged_kernel<0, true>;
+      attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), QSMEM);
+      if (s != ATTN_OK) return s;
+      kern<<<grid, 256, QSMEM, stream>>>(static_cast<const float*>(p.src[0]),
+                                         static_cast<const float*>(p.src[1]),
+                                         static_cast<const float*>(p.src[2]), p.dst[0], p.dst[1],
+                                         p.dst[2], p.descale[0], p.descale[1], p.descale[2], p.signs,
+                                         p.N, nblk, kv_planes, status, p.rope_cos, p.rope_sin);
+    } else {
+      // register-staged block pre-pass: {packed, bfloat16 input, rotation}
+      auto kern = fp8_quant_kernel<0, false, false, false>;
+      const int sel = (p.cu_seqlens ? 4 : 0) | (p.in_bf16 ? 2 : 0) | (rope ? 1 : 0);
+      switch (sel) {
+        case 1: kern = fp8_quant_kernel<0, false, false, true>; break;
+        case 2: kern = fp8_quant_kernel<0, false, true, false>; break;
+        case 3: kern = fp8_quant_kernel<0, false, true, true>; break;
+        case 4: kern = fp8_quant_kernel<0, true, false, false>; break;
+        case 5: kern = fp8_quant_kernel<0, true, false, true>; break;
+        case 6: kern = fp8_quant_kernel<0, true, true, false>; break;
+        case 7: kern = fp8_quant_kernel<0, true, true, true>; break;
+        default: break;
+      }
+      kern<<<grid, 256, 0, stream>>>(p.src[0], p.src[1], p.src[2], p.dst[0], p.dst[1], p.dst[2],
+                                     p.descale[0], p.descale[1], p.descale[2], p.signs, p.N, nblk,
+                                     kv_planes, p.cu_seqlens, p.total, p.H, H_kv, status,
+                                     p.rope_cos, p.rope_sin);
+    }
   } else if (p.in_bf16) {
     launch_quant_modes<true>(p, grid, nblk, kv_planes, stream);
   } else {

@@ -429,6 +429,45 @@ attn_status_t attn_fp8_quantize_rope(const float* q, const float* k, const float
                                      cudaStream_t stream);
 
 /*
+ * attn_fp8_quantize_ex -- the FP8 pre-pass with every option in one call:
+ * float32 or bfloat16 inputs, rotary embedding of Q and K, the Hadamard
+ * transform, grouped-query heads, and fixed-length or packed batches.
+ *   q, k, v        : input_bf16 = 0: float32; 1: bfloat16.
+ *                    cu_seqlens == NULL: q [B, H, N, d], k and v [B, H_kv, N, d];
+ *                    else a packed batch (the layout of attn_fwd_varlen): q
+ *                    [total, H, d], k and v [total, H_kv, d], N = the longest
+ *                    sequence (max_seqlen), cu_seqlens DEVICE int32 [B + 1].
+ *   rope_cos,
+ *   rope_sin       : DEVICE float32 [N, d/2] or both NULL (no rotation).  A row
+ *                    at position n of its sequence (n = 0 at the sequence's first
+ *                    token) has each pair (x_i, x_{i+d/2}), i < d/2, rotated to
+ *                    (x_i c - x_{i+d/2} s, x_{i+d/2} c + x_i s), c, s =
+ *                    rope_cos[n][i], rope_sin[n][i]; Q and K only, before the
+ *                    Hadamard transform.  16-byte aligned.
+ *   hadamard_signs : as attn_fp8_quantize, or NULL.
+ *   q8, k8, v8     : e4m3 codes in the inputs' layout (written).
+ *   *_descale      : fixed length: [B, H or H_kv, ceil(N/128)]; packed: as
+ *                    attn_fp8_quantize_varlen (entries past a sequence's end hold 1).
+ *   per_tensor     : 1 = the per-tensor comparator (fixed length, no rotation, no
+ *                    Hadamard); else 0.
+ * d = 128.  The codes are those of attn_fp8_quantize_gqa / _bf16 / _varlen /
+ * _rope with the same options; the packed offsets are checked on the device
+ * (reported by attn_get_device_status as ATTN_ERR_INVALID_ARG).
+ * Source: "FlashAttention-3: Hopper Asynchrony and FP8 Attention", section "FP8
+ * accuracy controls" (block scales; the transform "can be fused with rotary
+ * embedding"); "FlashAttention 3 Hardware Acceleration: ...", sections "Torch
+ * Compile" (rotary embedding fused with the transform) and "GPU Compatibility
+ * and Enablement Matrix" (grouped-query heads, variable-length batches).
+ */
+attn_status_t attn_fp8_quantize_ex(const void* q, const void* k, const void* v, int input_bf16,
+                                   const float* rope_cos, const float* rope_sin,
+                                   const float* hadamard_signs, uint8_t* q8, uint8_t* k8,
+                                   uint8_t* v8, float* q_descale, float* k_descale,
+                                   float* v_descale, const int* cu_seqlens, int B, int N,
+                                   int total, int H, int H_kv, int d, int per_tensor,
+                                   cudaStream_t stream);
+
+/*
  * attn_fwd_fp8 -- FP8 e4m3 forward on the output of attn_fp8_quantize.
  *   q8, k8, v8 : [B, H, N, d] e4m3; d must be 128.
  *   *_descale  : [B, H, ceil(N/128)] float32 block descales.

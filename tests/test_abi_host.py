@@ -262,3 +262,17 @@ def test_noalloc_reaches_the_device_check_without_a_gpu(lib):
     # a problem that fits: the device check comes before the symbol lookup
     code = lib.attn_bwd_noalloc(16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 2, 256, 64, 0, 0.1, 0, None)
     assert code in (3, 4)
+
+
+def test_fp8_quantize_ex_validates(lib):
+    assert "attn_fp8_quantize_ex" in declared_functions()
+
+    def call(bf=1, cos=16, sin=16, signs=None, cu=None, B=1, N=256, total=0, H=4, H_kv=2, d=128, pt=0):
+        return lib.attn_fp8_quantize_ex(16, 16, 16, bf, cos, sin, signs, 16, 16, 16, 16, 16, 16, cu,
+                                        B, N, total, H, H_kv, d, pt, None)
+    for kw, code, why in ((dict(bf=2), 1, "input_bf16"), (dict(sin=None), 1, "rope_sin"),
+                          (dict(cos=8), 1, "16-byte"), (dict(pt=1), 1, "per-tensor"),
+                          (dict(H_kv=3), 1, "H_kv"), (dict(d=64), 2, "d = 128"),
+                          (dict(cu=18, total=300), 1, "cu_seqlens"), (dict(cu=16, total=0), 1, ">= 1")):
+        assert call(**kw) == code, kw
+        assert why.lower() in lib.attn_last_error().decode().lower(), (kw, lib.attn_last_error())
