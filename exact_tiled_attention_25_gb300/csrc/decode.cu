@@ -51,9 +51,10 @@ struct DecCfg {
   static constexpr int NSLOT_FIT = (kSmemLimit - 2048 - TILE) / TILE;
   static constexpr int NSLOT = NSLOT_FIT > 8 ? 8 : NSLOT_FIT;
   static constexpr int SMEM = 1024 + TILE + NSLOT * TILE;
-  static constexpr int THREADS = 6 * 32;              // 4 softmax warps, producer, MMA
+  static constexpr int THREADS = 7 * 32;   // 4 softmax warps, key producer, MMA, value producer
   static constexpr int LOAD_WARP = 4;
   static constexpr int MMA_WARP = 5;
+  static constexpr int LOAD_V_WARP = 6;
   __host__ __device__ static constexpr uint32_t S_COL(int buf) { return 128u * buf; }
   static constexpr uint32_t O_COL = 256;
   static_assert(NSLOT >= 4, "ring too short");
@@ -84,23 +85,28 @@ __device__ __forceinline__ float lg2_dec(float x) {
   return y;
 }
 
-// Producer of one split.  The whole warp runs the loop.  The physical pages
+// Producer of one split, run by two warps: one issues the key tiles, the other
+// the value tiles (kv = 0 / 1).  A warp stalls on each tensor copy it issues
+// until the copy engine has taken it; measured on GB300, one issuing warp
+// streamed ~34 GB/s into a CTA's ring whatever the ring depth, two warps ~51.
+// Each warp runs the loop over all items and skips the other kind.  The physical pages
 // of the split's boxes (one box = min(page_size, 128) rows of one page) are
 // read from the block table in windows of 32 boxes, one box per lane, and the
 // next window is read while the current one is in use: no table read waits in
-// front of a copy.  When a window comes into use its entries are checked and,
-// for an e4m3 cache, the descales of its pages are prefetched into L2 for the
-// softmax warps.  Lane 0 waits for free ring slots; one lane per (box, 64-column
-// chunk) issues the tile's copies together; the keys and values of a tile use
-// the same pages.  Item i (K_j = 2j, V_j = 2j + 1)
+// front of a copy.  When a window comes into use its entries are checked; for
+// an e4m3 cache each tile's descales are prefetched into L2 with its copy.
+// Lane 0 waits for free ring slots; one lane per (box, 64-column chunk) issues
+// the tile's copies together; the keys and values of a tile use the same pages.  Item i (K_j = 2j, V_j = 2j + 1)
 // goes to ring slot (i + SHIFT) % NSLOT: the first SHIFT slots may start out
 // holding other data, released through their empty barrier like a used slot.
+// load_items[kv] receives the item count the warp reached (its own items are
+// those of parity kv below it).
 template <int NSLOT, int CH, int CHUNK, int TILE, int SHIFT>
 __device__ __forceinline__ void decode_produce(const CUtensorMap* tmK, const CUtensorMap* tmV,
                                                uint8_t* sKV, uint64_t* kv_full, uint64_t* kv_empty,
                                                const DecKParams& kp, const int* table, int j0,
                                                int nK, int len, int hk, int lane, const Abort& ab,
-                                               int* load_items_sh) {
+                                               int kv_own, int* load_items) {
   const int nbox = DBN / kp.box_rows;       // divides 32, so windows start at tile starts
   const int nboxes = nK * nbox;
   // box 32 w + lane lies in the split and the sequence
@@ -121,11 +127,6 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap* tmK, const CUt
       atomicCAS(kp.status, 0, kDevBadSeqlens);
       return kp.num_pages;
     }
-    if (kp.k_descale) {
-      const size_t at = static_cast<size_t>(pg) * kp.H_kv + hk;
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(kp.k_descale + at));
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(kp.v_descale + at));
-    }
     return pg;
   };
   int win = take(load_window(0), 0);
@@ -139,6 +140,10 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap* tmK, const CUt
       win_next = load_window(wcur + 1);
     }
     for (int kv = 0; kv < 2; ++kv) {
+      if (kv != kv_own) {
+        ++it;
+        continue;
+      }
       const int slot = (it + SHIFT) % NSLOT;
       const int use = (it + SHIFT) / NSLOT;
       int go = 1;
@@ -160,11 +165,27 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap* tmK, const CUt
         const int tok = (j0 + j) * DBN + x * kp.box_rows;
         tma_load_4d(dst + c * CHUNK + x * kp.box_rows * 128, kv ? tmV : tmK, &kv_full[slot], c * 64,
                     tok & (kp.page_size - 1), hk, phys);
+        if (kp.k_descale && c == 0 && phys < kp.num_pages) {
+          // the tile's descales, into L2 a ring's depth before the softmax
+          // warps read them (a whole block-table window ahead they were
+          // evicted again by the stream of keys and values)
+          const size_t at = static_cast<size_t>(phys) * kp.H_kv + hk;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"((kv ? kp.v_descale : kp.k_descale) + at));
+        }
       }
       ++it;
     }
   }
-  if (lane == 0) *load_items_sh = it;
+  if (lane == 0) load_items[kv_own] = it;
+}
+
+// After an abort: wait (bounded) for the copies a producer warp still has in
+// flight, the last NSLOT items it may have issued.
+template <int NSLOT, int SHIFT, typename Parity>
+__device__ __forceinline__ void decode_drain_items(uint64_t* kv_full, int issued, int kv_own,
+                                                   Parity parity) {
+  for (int i = issued - 1; i >= 0 && i >= issued - NSLOT; --i)
+    if ((i & 1) == kv_own) mbar_wait_drain(&kv_full[(i + SHIFT) % NSLOT], parity(i));
 }
 
 template <int D, bool FP16>
@@ -190,7 +211,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
-  __shared__ int load_items_sh;
+  __shared__ int load_items_sh[2];
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -229,7 +250,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     }
     mbar_init(&drain_bar, 1);
     abort_sh = 0;
-    load_items_sh = 0;
+    load_items_sh[0] = load_items_sh[1] = 0;
     fence_mbar_init();
   }
   if (warp == C::MMA_WARP) {
@@ -242,9 +263,10 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
   const uint32_t tmem = tmem_base_sh;
   const Abort ab{&abort_sh, kp.status};
 
-  if (warp == C::LOAD_WARP) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp == C::LOAD_WARP || warp == C::LOAD_V_WARP) {
+    // ------------------------------------------------------------ producers
+    const int kv_own = warp == C::LOAD_WARP ? 0 : 1;
+    if (lane == 0 && kv_own == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
@@ -255,7 +277,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     }
     decode_produce<NSLOT, C::CH, C::CHUNK, C::TILE, 0>(
         &tmK, &tmV, sKV, kv_full, kv_empty, kp, kp.block_table + static_cast<size_t>(b) * kp.max_pages,
-        j0, nK, len, hk, lane, ab, &load_items_sh);
+        j0, nK, len, hk, lane, ab, kv_own, load_items_sh);
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
@@ -425,11 +447,11 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   if (abort_sh) {
-    if (warp == C::LOAD_WARP && lane == 0) {
-      mbar_wait_drain(&q_full, 0);
-      const int issued = load_items_sh;
-      for (int s = 0; s < NSLOT && s < issued; ++s)
-        mbar_wait_drain(&kv_full[s], ((issued - 1 - s) / NSLOT) & 1);
+    if ((warp == C::LOAD_WARP || warp == C::LOAD_V_WARP) && lane == 0) {
+      const int kv_own = warp == C::LOAD_WARP ? 0 : 1;
+      if (kv_own == 0) mbar_wait_drain(&q_full, 0);
+      decode_drain_items<NSLOT, 0>(kv_full, load_items_sh[kv_own], kv_own,
+                                   [](int i) -> uint32_t { return (i / NSLOT) & 1u; });
     }
     if (warp == C::MMA_WARP && lane == 0) {
       mma_commit(&drain_bar);
@@ -513,9 +535,10 @@ struct Dec8Cfg {
   static constexpr int SHIFT = 2;                    // ring slots the query tile occupies first
   static constexpr int SMEM = 1024 + TILE8 + NSLOT * TILE8;
   static_assert(Q16 == SHIFT * TILE8, "query staging must fill whole ring slots");
-  static constexpr int THREADS = 6 * 32;
-  static constexpr int LOAD_WARP = 4;
+  static constexpr int THREADS = 7 * 32;
+  static constexpr int LOAD_WARP = 4;      // keys (and the query tile)
   static constexpr int MMA_WARP = 5;
+  static constexpr int LOAD_V_WARP = 6;    // values
   __host__ __device__ static constexpr uint32_t S_COL(int buf) { return 128u * buf; }
   static constexpr uint32_t O_COL = 256;
   static_assert(NSLOT >= 6, "ring too short");
@@ -547,7 +570,7 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
-  __shared__ int load_items_sh;
+  __shared__ int load_items_sh[2];
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -586,7 +609,7 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
     }
     mbar_init(&drain_bar, 1);
     abort_sh = 0;
-    load_items_sh = 0;
+    load_items_sh[0] = load_items_sh[1] = 0;
     fence_mbar_init();
   }
   if (warp == C::MMA_WARP) {
@@ -607,9 +630,10 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
     return static_cast<uint32_t>((i + C::SHIFT) / NSLOT - (slot < C::SHIFT ? 1 : 0)) & 1u;
   };
 
-  if (warp == C::LOAD_WARP) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp == C::LOAD_WARP || warp == C::LOAD_V_WARP) {
+    // ------------------------------------------------------------ producers
+    const int kv_own = warp == C::LOAD_WARP ? 0 : 1;
+    if (lane == 0 && kv_own == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
@@ -618,8 +642,8 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
       for (int c = 0; c < 2; ++c)
         tma_load_3d(sQ + c * C::CHUNK16, &tmQ, &q_full, c * 64, hk * kp.group * kp.n_q, b);
     }
-    decode_produce<NSLOT, 1, 0, C::TILE8, 2>(&tmK, &tmV, sKV, kv_full, kv_empty, kp, table, j0, nK,
-                                             len, hk, lane, ab, &load_items_sh);
+    decode_produce<NSLOT, 1, 0, C::TILE8, C::SHIFT>(&tmK, &tmV, sKV, kv_full, kv_empty, kp, table, j0,
+                                                    nK, len, hk, lane, ab, kv_own, load_items_sh);
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
@@ -906,11 +930,10 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   if (abort_sh) {
-    if (warp == C::LOAD_WARP && lane == 0) {
-      mbar_wait_drain(&q_full, 0);
-      const int issued = load_items_sh;
-      for (int i = issued - 1; i >= 0 && i >= issued - NSLOT; --i)
-        mbar_wait_drain(&kv_full[(i + C::SHIFT) % NSLOT], full_parity(i));
+    if ((warp == C::LOAD_WARP || warp == C::LOAD_V_WARP) && lane == 0) {
+      const int kv_own = warp == C::LOAD_WARP ? 0 : 1;
+      if (kv_own == 0) mbar_wait_drain(&q_full, 0);
+      decode_drain_items<NSLOT, C::SHIFT>(kv_full, load_items_sh[kv_own], kv_own, full_parity);
     }
     if (warp == C::MMA_WARP && lane == 0) {
       mma_commit(&drain_bar);
@@ -922,6 +945,544 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// ============================================ e4m3 cache, keys on M ====
+// A decode step has few query rows per key/value head (R = G * n_q).  With
+// R <= 16 the products run transposed, the keys of a tile on the MMA's M side
+// and the query rows on N = 16:
+//     S^T (128 keys x 16) = K_j Q8^T,      O^T (d x 16) += V_j^T P'^T,
+// so each softmax thread holds the scores of one key for every query row and
+// computes NC (>= R, a power of two <= 16) exponentials per tile, where the
+// rows-on-M kernel computes 128 per thread for 128 padded rows.  The row
+// maximum becomes a reduction over the 128 key threads (a column-transposing
+// warp exchange, then the four warps' partial maxima through shared memory and
+// an mbarrier), the row sums stay per thread until the end, and the weights go
+// to shared memory as the B operand of the P V product.  Numerics are those of
+// the rows-on-M kernel: the same query quantiser, the exact running maximum of
+// y = s + log2(dv) per row, P' = 2^(y - m) in e4m3 against raw value codes,
+// and row sums of P' / dv.
+struct Dec8TCfg {
+  static constexpr int D = 128;
+  static constexpr int NQ = 16;                  // MMA N: query rows, padded
+  static constexpr int TILE8 = DBN * D;          // e4m3 key or value tile, 16 KB
+  static constexpr int Q8_OFF = 0;               // e4m3 query rows, 16 x 128 B
+  static constexpr int P_OFF = 2048;             // two e4m3 P'^T tiles, 16 x 128 B each
+  static constexpr int Q16_OFF = 6144;           // 16-bit query rows: two 64-column chunks
+  static constexpr int CHUNK16 = NQ * 128;
+  static constexpr int RING_OFF = 10240;
+  static constexpr int NSLOT_FIT = (kSmemLimit - 2048 - RING_OFF) / TILE8;
+  static constexpr int NSLOT = NSLOT_FIT > 13 ? 13 : NSLOT_FIT;
+  static constexpr int SMEM = 1024 + RING_OFF + NSLOT * TILE8;
+  static constexpr int THREADS = 8 * 32;
+  static constexpr int LOAD_WARP = 4;      // keys (and the query rows)
+  static constexpr int MMA_WARP = 5;       // P V products (and the TMEM allocation)
+  static constexpr int LOAD_V_WARP = 6;    // values
+  static constexpr int MMA_S_WARP = 7;     // score products
+  __host__ __device__ static constexpr uint32_t S_COL(int buf) { return 16u * buf; }
+  static constexpr uint32_t O_COL = 32;
+  static constexpr uint32_t TMEM_COLS = 64;
+  static_assert(NSLOT >= 6, "ring too short");
+  static_assert(Q16_OFF + 2 * CHUNK16 <= RING_OFF, "staging overlaps the ring");
+};
+
+// Reduce NC per-lane values over the 32 lanes of a warp, column by column.
+// While more than one column is left, each exchange round halves the columns a
+// lane keeps: it keeps one half, sends the other to its partner and combines
+// what it receives; the remaining rounds combine a single column.  Returns the
+// warp total of column *col (every lane ends with some column; 32 / NC lanes
+// share each).
+// One exchange round at lane distance STEP with W columns left (rounds with
+// W = 1 combine the single column), then the next round.
+template <int NC, int W, int STEP, typename Op>
+__device__ __forceinline__ float col_reduce_round(float (&cur)[NC], int lane, Op op, int& c) {
+  if constexpr (STEP == 0) {
+    return cur[0];
+  } else if constexpr (W > 1) {
+    constexpr int H = W / 2;
+    const bool hi = (lane & STEP) != 0;
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+      const float send = hi ? cur[i] : cur[i + H];
+      const float keep = hi ? cur[i + H] : cur[i];
+      cur[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, STEP));
+    }
+    if (hi) c += H;
+    return col_reduce_round<NC, H, STEP / 2>(cur, lane, op, c);
+  } else {
+    cur[0] = op(cur[0], __shfl_xor_sync(0xffffffffu, cur[0], STEP));
+    return col_reduce_round<NC, 1, STEP / 2>(cur, lane, op, c);
+  }
+}
+
+// Reduce NC per-lane values over the 32 lanes of a warp, column by column.
+// While more than one column is left, each exchange round halves the columns a
+// lane keeps: it keeps one half, sends the other to its partner and combines
+// what it receives; the remaining rounds combine a single column.  Returns the
+// warp total of column *col (every lane ends with some column; 32 / NC lanes
+// share each).
+template <int NC, typename Op>
+__device__ __forceinline__ float warp_col_reduce(const float (&v)[NC], int lane, Op op, int* col) {
+  float cur[NC];
+#pragma unroll
+  for (int i = 0; i < NC; ++i) cur[i] = v[i];
+  int c = 0;
+  const float r = col_reduce_round<NC, NC, 16>(cur, lane, op, c);
+  *col = c;
+  return r;
+}
+
+struct AddOp {
+  __device__ float operator()(float a, float b) const { return a + b; }
+};
+
+__device__ __forceinline__ void st_shared_u8(uint32_t saddr, uint32_t v) {
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+
+template <bool FP16, int NC>
+__global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
+    decode_fp8_keys_kernel(const __grid_constant__ CUtensorMap tmQ,
+                           const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV, const DecKParams kp) {
+  using C = Dec8TCfg;
+  constexpr int D = C::D;
+  constexpr int NSLOT = C::NSLOT;
+  static_assert(NC == 4 || NC == 8 || NC == 16, "columns per softmax thread");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ8 = smem + C::Q8_OFF;
+  uint8_t* sP = smem + C::P_OFF;
+  uint8_t* sQ16 = smem + C::Q16_OFF;
+  uint8_t* sKV = smem + C::RING_OFF;
+
+  __shared__ __align__(8) uint64_t q_full;
+  __shared__ __align__(8) uint64_t q8_full;
+  __shared__ __align__(8) uint64_t kv_full[NSLOT];
+  __shared__ __align__(8) uint64_t kv_empty[NSLOT];
+  __shared__ __align__(8) uint64_t s_full[2];
+  __shared__ __align__(8) uint64_t p_full[2];
+  __shared__ __align__(8) uint64_t red_full[2];
+  __shared__ __align__(8) uint64_t fin_bar;
+  __shared__ __align__(8) uint64_t o_full;
+  __shared__ __align__(8) uint64_t drain_bar[2];
+  __shared__ __align__(16) float red_sh[2][4 * NC];   // per-warp column maxima, by tile parity
+  __shared__ __align__(16) float fin_sh[4 * NC];      // per-warp row sums
+  __shared__ float cq_sh[C::NQ];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ int load_items_sh[2];
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int t = threadIdx.x;   // softmax threads: key t of a tile, d index t of O^T
+  const int split = blockIdx.x;
+  const int hk = blockIdx.y;
+  const int b = blockIdx.z;
+  const int len = kp.seq_lens[b];
+  if (len < 0 || len > kp.max_pages * kp.page_size) {
+    if (threadIdx.x == 0) atomicCAS(kp.status, 0, kDevBadSeqlens);
+    return;
+  }
+  const int ntiles = (len + DBN - 1) / DBN;
+  const int j0 = split * kp.tiles_per_split;
+  const int nK = max(0, min(ntiles, j0 + kp.tiles_per_split) - j0);
+  // the R rows of this key/value head are contiguous in [B, H, n_q]
+  const size_t prow0 = (static_cast<size_t>(b) * kp.H + static_cast<size_t>(hk) * kp.group) * kp.n_q;
+  if (nK == 0) {
+    if (t < kp.rows_real) kp.lse_part[(prow0 + t) * kp.splits + split] = -INFINITY;
+    return;
+  }
+  const int total_items = 2 * nK;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&q_full, 1);
+    mbar_init(&q8_full, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&red_full[i], 128);
+    }
+    mbar_init(&fin_bar, 128);
+    mbar_init(&o_full, 1);
+    for (int sl = 0; sl < NSLOT; ++sl) {
+      mbar_init(&kv_full[sl], 1);
+      mbar_init(&kv_empty[sl], 1);
+    }
+    mbar_init(&drain_bar[0], 1);
+    mbar_init(&drain_bar[1], 1);
+    abort_sh = 0;
+    load_items_sh[0] = load_items_sh[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+  const Abort ab{&abort_sh, kp.status};
+  const int* table = kp.block_table + static_cast<size_t>(b) * kp.max_pages;
+  auto full_parity = [](int i) -> uint32_t { return static_cast<uint32_t>(i / NSLOT) & 1u; };
+
+  if (warp == C::LOAD_WARP || warp == C::LOAD_V_WARP) {
+    // ------------------------------------------------------------ producers
+    const int kv_own = warp == C::LOAD_WARP ? 0 : 1;
+    if (lane == 0 && kv_own == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(&q_full, 2 * C::CHUNK16);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        tma_load_3d(sQ16 + c * C::CHUNK16, &tmQ, &q_full, c * 64, hk * kp.rows_real, b);
+    }
+    decode_produce<NSLOT, 1, 0, C::TILE8, 0>(&tmK, &tmV, sKV, kv_full, kv_empty, kp, table, j0, nK,
+                                             len, hk, lane, ab, kv_own, load_items_sh);
+  } else if (warp == C::MMA_WARP || warp == C::MMA_S_WARP) {
+    // ------------------------------------------------------------ MMA issue
+    // Two issuing threads: the score products and the P V products.  Issuing
+    // a product or a commit costs the issuing thread tens to a hundred cycles
+    // (measured), which with one thread for both bounded the tile rate.
+    //  * S(j) waits for K_j and for P V(j - 2) (so the softmax has read S(j - 2)
+    //    from the same TMEM buffer and P V(j - 2) has read the P'^T tile that
+    //    the softmax of tile j overwrites); one commit on s_full[j % 2].
+    //  * P V(j) waits for V_j and the softmax's P'(j); one commit on the value
+    //    slot's empty barrier, whose phase also tells the softmax (rescale of
+    //    O^T) and the score issuer that P V(j) has landed.  Key slots are
+    //    released by the softmax once it has seen S(j).
+    auto v_done_parity = [](int jj) -> uint32_t { return static_cast<uint32_t>((2 * jj + 1) / NSLOT) & 1u; };
+    if (lane == 0 && warp == C::MMA_S_WARP) {
+      constexpr uint32_t idS = idesc_e4m3(128, C::NQ, false, false);
+      const uint64_t qdesc = sdesc_sw128(smem_u32(sQ8), 16, 1024);           // B: query rows, K-major
+      const uint64_t kdesc0 = sdesc_sw128(smem_u32(sKV), 16, 1024);          // A: keys, K-major
+      bool ok = mbar_wait(&q8_full, 0, ab, kDevTimeoutMma);
+      for (int jj = 0; jj < nK && ok; ++jj) {
+        const int item = 2 * jj;
+        const int slot = item % NSLOT;
+        if (!(ok = mbar_wait(&kv_full[slot], full_parity(item), ab, kDevTimeoutMma))) break;
+        if (jj >= 2 &&
+            !(ok = mbar_wait(&kv_empty[(2 * jj - 3) % NSLOT], v_done_parity(jj - 2), ab, kDevTimeoutMma)))
+          break;
+        tc_fence_after_sync();
+        const uint64_t kdesc = opaque(sdesc_add(kdesc0, slot * C::TILE8));
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk)
+          mma_f8_ss(tmem + C::S_COL(jj & 1), sdesc_add(kdesc, kk * 32), sdesc_add(qdesc, kk * 32), idS,
+                    kk > 0 ? 1u : 0u);
+        mma_commit(&s_full[jj & 1]);
+      }
+    } else if (lane == 0) {
+      constexpr uint32_t idPV = idesc_e4m3(128, C::NQ, true, false);
+      const uint64_t pdesc0 = sdesc_sw128(smem_u32(sP), 16, 1024);           // B: P'^T rows, K-major
+      const uint64_t vdesc0 = sdesc_sw128(smem_u32(sKV), C::TILE8, 1024);    // A: V^T, MN-major
+      bool ok = true;
+      for (int j = 0; j < nK && ok; ++j) {
+        const int item = 2 * j + 1;
+        const int slot = item % NSLOT;
+        if (!(ok = mbar_wait(&kv_full[slot], full_parity(item), ab, kDevTimeoutMma))) break;
+        const uint64_t vdesc = opaque(sdesc_add(vdesc0, slot * C::TILE8));
+        if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1, ab, kDevTimeoutMma))) break;
+        tc_fence_after_sync();
+        const uint64_t pdesc = sdesc_add(pdesc0, (j & 1) * C::CHUNK16);
+#pragma unroll
+        for (int kk = 0; kk < DBN / 32; ++kk)
+          mma_f8_ss(tmem + C::O_COL, sdesc_add(vdesc, kk * 32 * 128), sdesc_add(pdesc, kk * 32), idPV,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&kv_empty[slot]);   // every use of a value slot gets its phase
+        if (j == nK - 1) mma_commit(&o_full);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    bool ok = true;
+    // ---- quantise the query rows: 8 threads per row, 16 columns each
+    {
+      const int qn = t >> 3, qp = t & 7;
+      if (__any_sync(0xffffffffu, !mbar_wait(&q_full, 0, ab, kDevTimeoutSoftmax))) {
+        ok = false;
+      } else {
+        float x[16];
+        const uint8_t* src = sQ16 + (qp >> 2) * C::CHUNK16 + qn * 128;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int unit = 2 * (qp & 3) + u;
+          const uint4 w = *reinterpret_cast<const uint4*>(src + ((unit ^ (qn & 7)) << 4));
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float2 f;
+            if (FP16) f = __half22float2(*reinterpret_cast<const __half2*>(&ws[e]));
+            else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
+            x[8 * u + 2 * e] = f.x;
+            x[8 * u + 2 * e + 1] = f.y;
+          }
+        }
+        if (kp.signs) {
+          // x -> (x o signs) H_d / sqrt(d): butterflies of span 1..8 inside the
+          // thread, 16..64 between the lanes t ^ 1, t ^ 2, t ^ 4 of the row
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 sg = __ldg(reinterpret_cast<const float4*>(kp.signs + 16 * qp + i));
+            x[i] *= sg.x;
+            x[i + 1] *= sg.y;
+            x[i + 2] *= sg.z;
+            x[i + 3] *= sg.w;
+          }
+#pragma unroll
+          for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if ((i & h) == 0) {
+                const float a = x[i], bb = x[i + h];
+                x[i] = a + bb;
+                x[i + h] = a - bb;
+              }
+#pragma unroll
+          for (int h = 1; h < 8; h <<= 1) {
+            const bool upper = (qp & h) != 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float o = __shfl_xor_sync(0xffffffffu, x[i], h);
+              x[i] = upper ? o - x[i] : x[i] + o;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] *= 0.08838834764831845f;   // 1 / sqrt(128)
+        }
+        float am = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(x[i]));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+        const bool real = qn < kp.rows_real;
+        // descale = amax / 448, code = e4m3(x / descale) with the quotient
+        // rounded as an IEEE float32 division (the block quantiser's rule)
+        const float dq = (real && am > 0.f) ? __fdiv_rn(am, 448.f) : 1.f;
+        const float yq = __fdiv_rn(1.f, dq);
+        uint32_t wq[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          wq[e] = real ? cvt_pack_e4m3x4(div_by_recip(x[4 * e], dq, yq), div_by_recip(x[4 * e + 1], dq, yq),
+                                         div_by_recip(x[4 * e + 2], dq, yq), div_by_recip(x[4 * e + 3], dq, yq))
+                       : 0u;
+        st_shared_v4(smem_u32(sQ8 + qn * 128 + ((qp ^ (qn & 7)) << 4)), wq[0], wq[1], wq[2], wq[3]);
+        if (qp == 0) cq_sh[qn] = real ? kp.scale_log2 * dq : 0.f;
+        // both P'^T tiles start zero: rows at or past NC are never written
+        st_shared_v4(smem_u32(sP + t * 32), 0u, 0u, 0u, 0u);
+        st_shared_v4(smem_u32(sP + t * 32 + 16), 0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+        mbar_arrive(&q8_full);
+      }
+    }
+    float cq[NC];     // scale * log2(e) * dq of each query row (0: padding)
+    int vend[NC];     // keys [0, vend) visible to each query row (0: padding)
+    float m_ref[NC];  // running maximum of y = s + log2(dv), log2 units
+    float lsum[NC];   // this thread's share of the row sums of 2^(s - m_ref)
+    if (ok && __any_sync(0xffffffffu, !mbar_wait(&q8_full, 0, ab, kDevTimeoutSoftmax))) ok = false;
+#pragma unroll
+    for (int n = 0; n < NC; ++n) {
+      cq[n] = cq_sh[n];
+      const int tq = n % kp.n_q;
+      vend[n] = n < kp.rows_real ? (kp.causal ? min(len, len - kp.n_q + tq + 1) : len) : 0;
+      m_ref[n] = -INFINITY;
+      lsum[n] = 0.f;
+    }
+    // ---- descales of this thread's key, fetched two tiles ahead (its
+    // block-table entry two tiles before that)
+    auto page_of = [&](int jj) -> int {
+      const int tok = (j0 + jj) * DBN + t;
+      if (jj >= nK || tok >= len) return -1;
+      return __ldg(table + (tok >> kp.page_shift));   // range-checked when used
+    };
+    auto dk_of = [&](int ph) -> float {
+      return (ph < 0 || ph >= kp.num_pages) ? 1.f : __ldg(kp.k_descale + static_cast<size_t>(ph) * kp.H_kv + hk);
+    };
+    auto dv_of = [&](int ph) -> float {
+      return (ph < 0 || ph >= kp.num_pages) ? 1.f : __ldg(kp.v_descale + static_cast<size_t>(ph) * kp.H_kv + hk);
+    };
+    int ph3 = page_of(3), ph4 = page_of(4);
+    int ph = page_of(0);
+    float dk_cur = dk_of(ph), dv_cur = dv_of(ph);
+    ph = page_of(1);
+    float dk1 = dk_of(ph), dv1 = dv_of(ph);
+    ph = page_of(2);
+    float dk2 = dk_of(ph), dv2 = dv_of(ph);
+
+    for (int j = 0; j < nK && ok; ++j) {
+      const float lgv = lg2_dec(dv_cur);
+      float inv_dv;
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv_dv) : "f"(dv_cur));
+      float coef[NC];
+#pragma unroll
+      for (int n = 0; n < NC; ++n) coef[n] = cq[n] * dk_cur;
+      if (__any_sync(0xffffffffu, !mbar_wait(&s_full[j & 1], (j >> 1) & 1, ab, kDevTimeoutSoftmax))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t sr[16];
+      tmem_ld16(tmem + lane_addr + C::S_COL(j & 1), sr);
+      // S(j) has completed: K_j's slot is free
+      if (t == 0 && 2 * j + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j) % NSLOT]);
+      tmem_ld_wait();
+      const int key = (j0 + j) * DBN + t;
+      float y[NC];
+#pragma unroll
+      for (int n = 0; n < NC; ++n)
+        y[n] = key < vend[n] ? fmaf(__uint_as_float(sr[n]), coef[n], lgv) : -INFINITY;
+      // column maxima over the tile's 128 keys: per warp, then across warps
+      float wmax[NC];
+#pragma unroll
+      for (int n = 0; n < NC; ++n) asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(wmax[n]) : "f"(y[n]));
+      if (lane == 0) {
+#pragma unroll
+        for (int n = 0; n < NC; n += 4)
+          *reinterpret_cast<float4*>(&red_sh[j & 1][warp * NC + n]) =
+              make_float4(wmax[n], wmax[n + 1], wmax[n + 2], wmax[n + 3]);
+      }
+      mbar_arrive(&red_full[j & 1]);
+      if (__any_sync(0xffffffffu, !mbar_wait(&red_full[j & 1], (j >> 1) & 1, ab, kDevTimeoutSoftmax))) {
+        ok = false;
+        break;
+      }
+      // The reference follows the running maximum exactly (no lazy slack), so
+      // the largest weight of a row is exactly 1, which e4m3 holds exactly.
+      float alpha[NC];
+      bool grew = false;
+#pragma unroll
+      for (int n4 = 0; n4 < NC; n4 += 4) {
+        float4 r4[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) r4[w] = *reinterpret_cast<const float4*>(&red_sh[j & 1][w * NC + n4]);
+        const float mt[4] = {fmaxf(fmaxf(r4[0].x, r4[1].x), fmaxf(r4[2].x, r4[3].x)),
+                             fmaxf(fmaxf(r4[0].y, r4[1].y), fmaxf(r4[2].y, r4[3].y)),
+                             fmaxf(fmaxf(r4[0].z, r4[1].z), fmaxf(r4[2].z, r4[3].z)),
+                             fmaxf(fmaxf(r4[0].w, r4[1].w), fmaxf(r4[2].w, r4[3].w))};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int n = n4 + i;
+          alpha[n] = 1.f;
+          if (mt[i] > m_ref[n]) {
+            alpha[n] = ex2_approx(m_ref[n] - mt[i]);   // 0 while m_ref = -inf
+            m_ref[n] = mt[i];
+            grew = true;
+          }
+        }
+      }
+      // weights P' = 2^(y - m) <= 1, e4m3 codes into row n of P'^T (key t)
+      float pw[NC];
+#pragma unroll
+      for (int n = 0; n < NC; ++n) {
+        const float off = (m_ref[n] == -INFINITY ? 0.f : -m_ref[n]) + lgv;
+        pw[n] = key < vend[n] ? ex2_approx(fmaf(__uint_as_float(sr[n]), coef[n], off)) : 0.f;
+        lsum[n] = fmaf(pw[n], inv_dv, lsum[n] * alpha[n]);
+      }
+      const uint32_t pbase = smem_u32(sP + (j & 1) * C::CHUNK16) + (t & 15);
+#pragma unroll
+      for (int n = 0; n < NC; n += 2) {
+        uint16_t pr;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pr) : "f"(pw[n + 1]), "f"(pw[n]));
+        st_shared_u8(pbase + n * 128 + ((((t >> 4) ^ n) & 7) << 4), pr & 0xFFu);
+        st_shared_u8(pbase + (n + 1) * 128 + ((((t >> 4) ^ (n + 1)) & 7) << 4), pr >> 8);
+      }
+      if (j > 0 && __any_sync(0xffffffffu, grew)) {
+        // rescale O^T by alpha once P V(j - 1) has landed (the phase of its
+        // value slot's empty barrier)
+        if (__any_sync(0xffffffffu, !mbar_wait(&kv_empty[(2 * j - 1) % NSLOT],
+                                               static_cast<uint32_t>((2 * j - 1) / NSLOT) & 1u, ab,
+                                               kDevTimeoutSoftmax))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        uint32_t o[16];
+        tmem_ld16(tmem + lane_addr + C::O_COL, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int n = 0; n < NC; ++n) o[n] = __float_as_uint(__uint_as_float(o[n]) * alpha[n]);
+        tmem_st16(tmem + lane_addr + C::O_COL, o);
+        tmem_st_wait();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(&p_full[j & 1]);
+      // advance the descale pipeline
+      dk_cur = dk1;
+      dv_cur = dv1;
+      dk1 = dk2;
+      dv1 = dv2;
+      dk2 = dk_of(ph3);
+      dv2 = dv_of(ph3);
+      ph3 = ph4;
+      ph4 = page_of(j + 5);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && !__any_sync(0xffffffffu, !mbar_wait(&o_full, 0, ab, kDevTimeoutEpilogue))) {
+      tc_fence_after_sync();
+      uint32_t o[16];
+      tmem_ld16(tmem + lane_addr + C::O_COL, o);
+      tmem_ld_wait();
+      int col;
+      const float wsum = warp_col_reduce<NC>(lsum, lane, AddOp{}, &col);
+      fin_sh[warp * NC + col] = wsum;
+      mbar_arrive(&fin_bar);
+      if (!__any_sync(0xffffffffu, !mbar_wait(&fin_bar, 0, ab, kDevTimeoutEpilogue))) {
+#pragma unroll
+        for (int n = 0; n < NC; ++n) {
+          if (n >= kp.rows_real) break;
+          const float l = ((fin_sh[n] + fin_sh[NC + n]) + fin_sh[2 * NC + n]) + fin_sh[3 * NC + n];
+          const float inv_l = l > 0.f ? 1.f / l : 0.f;
+          const size_t pr = (prow0 + n) * kp.splits + split;
+          kp.o_part[pr * D + t] = __uint_as_float(o[n]) * inv_l;
+          if (t == 0) kp.lse_part[pr] = l > 0.f ? (m_ref[n] + lg2_dec(l)) * 0.69314718055994530942f : -INFINITY;
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (abort_sh) {
+    if ((warp == C::LOAD_WARP || warp == C::LOAD_V_WARP) && lane == 0) {
+      const int kv_own = warp == C::LOAD_WARP ? 0 : 1;
+      if (kv_own == 0) mbar_wait_drain(&q_full, 0);
+      decode_drain_items<NSLOT, 0>(kv_full, load_items_sh[kv_own], kv_own, full_parity);
+    }
+    if ((warp == C::MMA_WARP || warp == C::MMA_S_WARP) && lane == 0) {
+      uint64_t* bar = &drain_bar[warp == C::MMA_WARP ? 0 : 1];
+      mma_commit(bar);
+      mbar_wait_drain(bar, 0);
+    }
+    __syncthreads();
+  }
+  if (warp == C::MMA_WARP) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <bool FP16, int NC>
+attn_status_t launch_decode_fp8_keys(const DecodeParams& p, const DecKParams& kp, const DecodeSplits& sp,
+                                     const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+  using C = Dec8TCfg;
+  auto kern = decode_fp8_keys_kernel<FP16, NC>;
+  attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), C::SMEM);
+  if (s != ATTN_OK) return s;
+  CUtensorMap tq;
+  // Q: {d, H * n_q rows, B}, boxes of 16 rows: the R rows of head hk from row hk * R
+  if ((s = make_tmap_3d(&tq, p.q, 2, C::D, static_cast<uint64_t>(p.H) * p.n_q, p.B, 64, C::NQ)) != ATTN_OK)
+    return s;
+  kern<<<dim3(sp.splits, p.H_kv, p.B), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, kp);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "FP8 decode split kernel launch");
+  return ATTN_OK;
 }
 
 template <bool FP16>
@@ -952,9 +1513,18 @@ attn_status_t launch_decode_fp8_t(const DecodeParams& p, cudaStream_t stream) {
                 p.max_pages,   p.page_size, box_rows, p.num_pages,
                 sp.splits,     sp.tiles_per_split, p.causal, p.scale * 1.4426950408889634f,
                 p.k_descale,   p.v_descale, p.signs, p.H_kv, shift};
-  kern<<<dim3(sp.splits, p.H_kv, p.B), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, kp);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail_cuda(e, "FP8 decode split kernel launch");
+  const int rows_real = (p.H / p.H_kv) * p.n_q;
+  if (rows_real <= Dec8TCfg::NQ) {
+    s = rows_real <= 4   ? launch_decode_fp8_keys<FP16, 4>(p, kp, sp, tk, tv, stream)
+        : rows_real <= 8 ? launch_decode_fp8_keys<FP16, 8>(p, kp, sp, tk, tv, stream)
+                         : launch_decode_fp8_keys<FP16, 16>(p, kp, sp, tk, tv, stream);
+    if (s != ATTN_OK) return s;
+  } else {
+    kern<<<dim3(sp.splits, p.H_kv, p.B), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, kp);
+    const cudaError_t e0 = cudaGetLastError();
+    if (e0 != cudaSuccess) return fail_cuda(e0, "FP8 decode split kernel launch");
+  }
+  cudaError_t e = cudaSuccess;
   const long long rows = static_cast<long long>(p.B) * p.H * p.n_q;
   decode_combine_kernel<128, FP16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
       p.o_part, p.lse_part, static_cast<uint16_t*>(p.o), p.lse, rows, sp.splits);

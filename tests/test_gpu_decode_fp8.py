@@ -46,7 +46,7 @@ def _cache(seed, lens, page_size, H_kv, spread=True):
 
 
 def _run(attn, lens, page_size, H, H_kv, n_q, causal, signs=None, dtype="bf16", seed=80,
-         max_seqlen=None, spread=True):
+         max_seqlen=None, spread=True, light=False):
     kc, vc, table = _cache(seed, lens, page_size, H_kv, spread)
     k8, kd = oracle.quantize_paged_cache(kc, signs)
     v8, vd = oracle.quantize_paged_cache(vc)
@@ -71,9 +71,11 @@ def _run(attn, lens, page_size, H, H_kv, n_q, causal, signs=None, dtype="bf16", 
     q8, qd = oracle.quantize_e4m3_blocks(qt, block_rows=1)
     q_used = oracle.dequantize_e4m3_blocks(q8, qd, block_rows=1)
     ref_used = oracle.attention_decode_paged_fp8(q_used, k8, v8, kd, vd, table, lens, scale, causal)
-    ref_exact = oracle.attention_decode_paged_fp8(q64, k8, v8, kd, vd, table, lens, scale, causal,
-                                                  signs)
-    ref_float, _ = oracle.attention_decode_paged(q64, kc, vc, table, lens, scale, causal)
+    ref_exact = ref_float = None
+    if not light:
+        ref_exact = oracle.attention_decode_paged_fp8(q64, k8, v8, kd, vd, table, lens, scale, causal,
+                                                      signs)
+        ref_float, _ = oracle.attention_decode_paged(q64, kc, vc, table, lens, scale, causal)
     # sum_j P_ij^2 V_j^2 of the query the kernel multiplies
     kdq = oracle.dequantize_paged_cache(k8, kd)
     vdq = oracle.dequantize_paged_cache(v8, vd)
@@ -89,7 +91,7 @@ def _run(attn, lens, page_size, H, H_kv, n_q, causal, signs=None, dtype="bf16", 
 def _check(o, lse, ref_used, ref_exact, ref_float, spread, bar):
     got = o.float().cpu().numpy().astype(np.float64)
     lse_c = lse.cpu().numpy().astype(np.float64)
-    (ro, rl), (eo, _) = ref_used, ref_exact
+    ro, rl = ref_used
     seen = np.isfinite(rl)
     assert np.array_equal(np.isfinite(lse_c), seen)
     assert np.all(np.isfinite(got))
@@ -98,6 +100,9 @@ def _check(o, lse, ref_used, ref_exact, ref_float, spread, bar):
     assert np.abs(diff).max() <= 0.25 * max(1.0, float(np.abs(ro).max()))
     np.testing.assert_allclose(lse_c[seen], rl[seen], atol=2e-3)
     assert np.all(got[~seen] == 0)
+    if ref_exact is None:
+        return
+    eo = ref_exact[0]
     total = np.sqrt(np.mean((got - eo) ** 2))
     storage = np.sqrt(np.mean((eo - ref_float) ** 2))
     assert total <= 1.5 * storage, (total, storage)
@@ -114,6 +119,28 @@ def test_page_sizes(attn, page_size, causal):
 @pytest.mark.parametrize("H,H_kv,n_q", [(32, 8, 1), (8, 1, 4), (4, 4, 1), (16, 2, 16)])
 def test_heads_and_query_tokens(attn, H, H_kv, n_q):
     _check(*_run(attn, [300, 1025, 64], 32, H, H_kv, n_q, True, seed=81))
+
+
+@pytest.mark.parametrize("H,H_kv,n_q", [(32, 2, 1), (12, 2, 2), (6, 2, 5), (34, 2, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_query_rows_per_head(attn, H, H_kv, n_q, causal):
+    # G n_q = 16, 12 and 15 query rows per key/value head run with the keys on
+    # the MMA's M side and 16 query columns per softmax thread; 17 rows run
+    # with the query rows on M
+    _check(*_run(attn, [300, 1025, 64], 64, H, H_kv, n_q, causal, seed=92))
+
+
+def test_transformed_keys_sixteen_rows(attn):
+    signs = workloads.random_signs(8, D)
+    _check(*_run(attn, [200, 700], 128, 32, 2, 1, True, signs=signs, seed=93))
+
+
+def test_timed_config_full_size(attn):
+    """The benchmark's decode step at full size: 16 sequences of 8192 cached
+    tokens, H = 32 query heads on H_kv = 8 (4 query rows per key/value head),
+    pages of 256 in a seeded random order, one query token, causal: every
+    output row and LSE against the oracle, within the kernel's own error bar."""
+    _check(*_run(attn, [8192] * 16, 256, 32, 8, 1, True, seed=94, light=True))
 
 
 @pytest.mark.parametrize("page_size", [16, 256])
