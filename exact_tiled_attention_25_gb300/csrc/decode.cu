@@ -1293,8 +1293,12 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
       m_ref[n] = -INFINITY;
       lsum[n] = 0.f;
     }
-    // ---- descales of this thread's key, fetched two tiles ahead (its
-    // block-table entry two tiles before that)
+    // ---- descales of this thread's key.  U register sets, one per tile
+    // residue mod U, with the loop unrolled by U: a tile's descales are loaded
+    // U tiles before use and its block-table entry U tiles before that, and no
+    // register copy waits on a load in flight (with one set rotated by copies,
+    // the copy stalled on the load a tile later).  U = 2 for 16 columns, where
+    // three copies of the larger loop body ran slower.
     auto page_of = [&](int jj) -> int {
       const int tok = (j0 + jj) * DBN + t;
       if (jj >= nK || tok >= len) return -1;
@@ -1306,15 +1310,13 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
     auto dv_of = [&](int ph) -> float {
       return (ph < 0 || ph >= kp.num_pages) ? 1.f : __ldg(kp.v_descale + static_cast<size_t>(ph) * kp.H_kv + hk);
     };
-    int ph3 = page_of(3), ph4 = page_of(4);
-    int ph = page_of(0);
-    float dk_cur = dk_of(ph), dv_cur = dv_of(ph);
-    ph = page_of(1);
-    float dk1 = dk_of(ph), dv1 = dv_of(ph);
-    ph = page_of(2);
-    float dk2 = dk_of(ph), dv2 = dv_of(ph);
+    constexpr int U = NC >= 16 ? 2 : 3;
+    float dk0 = dk_of(page_of(0)), dv0 = dv_of(page_of(0));
+    float dk1 = dk_of(page_of(1)), dv1 = dv_of(page_of(1));
+    float dk2 = U > 2 ? dk_of(page_of(2)) : 1.f, dv2 = U > 2 ? dv_of(page_of(2)) : 1.f;
+    int ph0 = page_of(U), ph1 = page_of(U + 1), ph2 = U > 2 ? page_of(U + 2) : -1;
 
-    for (int j = 0; j < nK && ok; ++j) {
+    auto tile_step = [&](const int j, float& dk_cur, float& dv_cur, int& ph_next) -> bool {
       const float lgv = lg2_dec(dv_cur);
       float inv_dv;
       asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv_dv) : "f"(dv_cur));
@@ -1322,8 +1324,7 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
 #pragma unroll
       for (int n = 0; n < NC; ++n) coef[n] = cq[n] * dk_cur;
       if (__any_sync(0xffffffffu, !mbar_wait(&s_full[j & 1], (j >> 1) & 1, ab, kDevTimeoutSoftmax))) {
-        ok = false;
-        break;
+        return false;
       }
       tc_fence_after_sync();
       uint32_t sr[16];
@@ -1348,8 +1349,7 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
       }
       mbar_arrive(&red_full[j & 1]);
       if (__any_sync(0xffffffffu, !mbar_wait(&red_full[j & 1], (j >> 1) & 1, ab, kDevTimeoutSoftmax))) {
-        ok = false;
-        break;
+        return false;
       }
       // The reference follows the running maximum exactly (no lazy slack), so
       // the largest weight of a row is exactly 1, which e4m3 holds exactly.
@@ -1397,8 +1397,7 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
         if (__any_sync(0xffffffffu, !mbar_wait(&kv_empty[(2 * j - 1) % NSLOT],
                                                static_cast<uint32_t>((2 * j - 1) / NSLOT) & 1u, ab,
                                                kDevTimeoutSoftmax))) {
-          ok = false;
-          break;
+          return false;
         }
         tc_fence_after_sync();
         uint32_t o[16];
@@ -1412,15 +1411,20 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before_sync();
       mbar_arrive(&p_full[j & 1]);
-      // advance the descale pipeline
-      dk_cur = dk1;
-      dv_cur = dv1;
-      dk1 = dk2;
-      dv1 = dv2;
-      dk2 = dk_of(ph3);
-      dv2 = dv_of(ph3);
-      ph3 = ph4;
-      ph4 = page_of(j + 5);
+      // descales of tile j + U (same register set), block-table entry of tile j + 2 U
+      dk_cur = dk_of(ph_next);
+      dv_cur = dv_of(ph_next);
+      ph_next = page_of(j + 2 * U);
+      return true;
+    };
+    for (int j = 0; j < nK && ok; j += U) {
+      if (!(ok = tile_step(j, dk0, dv0, ph0)) || j + 1 >= nK) break;
+      if constexpr (U == 2) {
+        ok = tile_step(j + 1, dk1, dv1, ph1);
+      } else {
+        if (!(ok = tile_step(j + 1, dk1, dv1, ph1)) || j + 2 >= nK) break;
+        ok = tile_step(j + 2, dk2, dv2, ph2);
+      }
     }
     // ------------------------------------------------------------ epilogue
     if (ok && !__any_sync(0xffffffffu, !mbar_wait(&o_full, 0, ab, kDevTimeoutEpilogue))) {
