@@ -962,6 +962,7 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
 // the rows-on-M kernel: the same query quantiser, the exact running maximum of
 // y = s + log2(dv) per row, P' = 2^(y - m) in e4m3 against raw value codes,
 // and row sums of P' / dv.
+template <int CW>   // softmax warps per key quarter (each takes NC / CW query columns)
 struct Dec8TCfg {
   static constexpr int D = 128;
   static constexpr int NQ = 16;                  // MMA N: query rows, padded
@@ -974,11 +975,12 @@ struct Dec8TCfg {
   static constexpr int NSLOT_FIT = (kSmemLimit - 2048 - RING_OFF) / TILE8;
   static constexpr int NSLOT = NSLOT_FIT > 13 ? 13 : NSLOT_FIT;
   static constexpr int SMEM = 1024 + RING_OFF + NSLOT * TILE8;
-  static constexpr int THREADS = 8 * 32;
-  static constexpr int LOAD_WARP = 4;      // keys (and the query rows)
-  static constexpr int MMA_WARP = 5;       // P V products (and the TMEM allocation)
-  static constexpr int LOAD_V_WARP = 6;    // values
-  static constexpr int MMA_S_WARP = 7;     // score products
+  static constexpr int SOFTMAX_WARPS = 4 * CW;
+  static constexpr int THREADS = (SOFTMAX_WARPS + 4) * 32;
+  static constexpr int LOAD_WARP = SOFTMAX_WARPS;         // keys (and the query rows)
+  static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;      // P V products (and the TMEM allocation)
+  static constexpr int LOAD_V_WARP = SOFTMAX_WARPS + 2;   // values
+  static constexpr int MMA_S_WARP = SOFTMAX_WARPS + 3;    // score products
   __host__ __device__ static constexpr uint32_t S_COL(int buf) { return 16u * buf; }
   static constexpr uint32_t O_COL = 32;
   static constexpr uint32_t TMEM_COLS = 64;
@@ -986,12 +988,6 @@ struct Dec8TCfg {
   static_assert(Q16_OFF + 2 * CHUNK16 <= RING_OFF, "staging overlaps the ring");
 };
 
-// Reduce NC per-lane values over the 32 lanes of a warp, column by column.
-// While more than one column is left, each exchange round halves the columns a
-// lane keeps: it keeps one half, sends the other to its partner and combines
-// what it receives; the remaining rounds combine a single column.  Returns the
-// warp total of column *col (every lane ends with some column; 32 / NC lanes
-// share each).
 // One exchange round at lane distance STEP with W columns left (rounds with
 // W = 1 combine the single column), then the next round.
 template <int NC, int W, int STEP, typename Op>
@@ -1036,19 +1032,34 @@ struct AddOp {
   __device__ float operator()(float a, float b) const { return a + b; }
 };
 
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 16) tmem_ld16(taddr, r);
+  else if constexpr (N == 8) tmem_ld8(taddr, r);
+  else tmem_ld4(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+  if constexpr (N == 16) tmem_st16(taddr, r);
+  else if constexpr (N == 8) tmem_st_x8(taddr, r);
+  else tmem_st4(taddr, r);
+}
+
 __device__ __forceinline__ void st_shared_u8(uint32_t saddr, uint32_t v) {
   asm volatile("st.shared.u8 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
 }
 
-template <bool FP16, int NC>
-__global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
+template <bool FP16, int NC, int CW>
+__global__ void __launch_bounds__(Dec8TCfg<CW>::THREADS, 1)
     decode_fp8_keys_kernel(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const DecKParams kp) {
-  using C = Dec8TCfg;
+  using C = Dec8TCfg<CW>;
   constexpr int D = C::D;
   constexpr int NSLOT = C::NSLOT;
-  static_assert(NC == 4 || NC == 8 || NC == 16, "columns per softmax thread");
+  constexpr int NCW = NC / CW;   // query columns of one softmax thread
+  static_assert(NC == 4 || NC == 8 || NC == 16, "query columns");
+  static_assert(NCW == 4 || NCW == 8 || NCW == 16, "columns per softmax thread");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1067,8 +1078,8 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
   __shared__ __align__(8) uint64_t fin_bar;
   __shared__ __align__(8) uint64_t o_full;
   __shared__ __align__(8) uint64_t drain_bar[2];
-  __shared__ __align__(16) float red_sh[2][4 * NC];   // per-warp column maxima, by tile parity
-  __shared__ __align__(16) float fin_sh[4 * NC];      // per-warp row sums
+  __shared__ __align__(16) float red_sh[2][4 * NC];   // [parity][key quarter][column]: maxima
+  __shared__ __align__(16) float fin_sh[4 * NC];      // [key quarter][column]: row sums
   __shared__ float cq_sh[C::NQ];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -1076,7 +1087,10 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int t = threadIdx.x;   // softmax threads: key t of a tile, d index t of O^T
+  // softmax threads: key t of a tile and d index t of O^T (the warp's TMEM lane
+  // quarter), query columns [cg NCW, (cg + 1) NCW)
+  const int t = (warp & 3) * 32 + lane;
+  const int cg = warp >> 2;
   const int split = blockIdx.x;
   const int hk = blockIdx.y;
   const int b = blockIdx.z;
@@ -1091,7 +1105,7 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
   // the R rows of this key/value head are contiguous in [B, H, n_q]
   const size_t prow0 = (static_cast<size_t>(b) * kp.H + static_cast<size_t>(hk) * kp.group) * kp.n_q;
   if (nK == 0) {
-    if (t < kp.rows_real) kp.lse_part[(prow0 + t) * kp.splits + split] = -INFINITY;
+    if (threadIdx.x < kp.rows_real) kp.lse_part[(prow0 + threadIdx.x) * kp.splits + split] = -INFINITY;
     return;
   }
   const int total_items = 2 * nK;
@@ -1101,10 +1115,10 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
     mbar_init(&q8_full, 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
-      mbar_init(&red_full[i], 128);
+      mbar_init(&p_full[i], 32 * C::SOFTMAX_WARPS);
+      mbar_init(&red_full[i], 32 * C::SOFTMAX_WARPS);
     }
-    mbar_init(&fin_bar, 128);
+    mbar_init(&fin_bar, 32 * C::SOFTMAX_WARPS);
     mbar_init(&o_full, 1);
     for (int sl = 0; sl < NSLOT; ++sl) {
       mbar_init(&kv_full[sl], 1);
@@ -1198,10 +1212,11 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
-    // ---- quantise the query rows: 8 threads per row, 16 columns each
-    {
+    // ---- quantise the query rows: 8 threads per row, 16 columns each (the
+    // first four softmax warps)
+    if (cg == 0) {
       const int qn = t >> 3, qp = t & 7;
       if (__any_sync(0xffffffffu, !mbar_wait(&q_full, 0, ab, kDevTimeoutSoftmax))) {
         ok = false;
@@ -1280,16 +1295,17 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
         mbar_arrive(&q8_full);
       }
     }
-    float cq[NC];     // scale * log2(e) * dq of each query row (0: padding)
-    int vend[NC];     // keys [0, vend) visible to each query row (0: padding)
-    float m_ref[NC];  // running maximum of y = s + log2(dv), log2 units
-    float lsum[NC];   // this thread's share of the row sums of 2^(s - m_ref)
+    float cq[NCW];     // scale * log2(e) * dq of each query row (0: padding)
+    int vend[NCW];     // keys [0, vend) visible to each query row (0: padding)
+    float m_ref[NCW];  // running maximum of y = s + log2(dv), log2 units
+    float lsum[NCW];   // this thread's share of the row sums of 2^(s - m_ref)
     if (ok && __any_sync(0xffffffffu, !mbar_wait(&q8_full, 0, ab, kDevTimeoutSoftmax))) ok = false;
 #pragma unroll
-    for (int n = 0; n < NC; ++n) {
-      cq[n] = cq_sh[n];
-      const int tq = n % kp.n_q;
-      vend[n] = n < kp.rows_real ? (kp.causal ? min(len, len - kp.n_q + tq + 1) : len) : 0;
+    for (int n = 0; n < NCW; ++n) {
+      const int nc = cg * NCW + n;
+      cq[n] = cq_sh[nc];
+      const int tq = nc % kp.n_q;
+      vend[n] = nc < kp.rows_real ? (kp.causal ? min(len, len - kp.n_q + tq + 1) : len) : 0;
       m_ref[n] = -INFINITY;
       lsum[n] = 0.f;
     }
@@ -1310,7 +1326,7 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
     auto dv_of = [&](int ph) -> float {
       return (ph < 0 || ph >= kp.num_pages) ? 1.f : __ldg(kp.v_descale + static_cast<size_t>(ph) * kp.H_kv + hk);
     };
-    constexpr int U = NC >= 16 ? 2 : 3;
+    constexpr int U = NCW >= 16 ? 2 : 3;
     float dk0 = dk_of(page_of(0)), dv0 = dv_of(page_of(0));
     float dk1 = dk_of(page_of(1)), dv1 = dv_of(page_of(1));
     float dk2 = U > 2 ? dk_of(page_of(2)) : 1.f, dv2 = U > 2 ? dv_of(page_of(2)) : 1.f;
@@ -1320,31 +1336,31 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
       const float lgv = lg2_dec(dv_cur);
       float inv_dv;
       asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv_dv) : "f"(dv_cur));
-      float coef[NC];
+      float coef[NCW];
 #pragma unroll
-      for (int n = 0; n < NC; ++n) coef[n] = cq[n] * dk_cur;
+      for (int n = 0; n < NCW; ++n) coef[n] = cq[n] * dk_cur;
       if (__any_sync(0xffffffffu, !mbar_wait(&s_full[j & 1], (j >> 1) & 1, ab, kDevTimeoutSoftmax))) {
         return false;
       }
       tc_fence_after_sync();
-      uint32_t sr[16];
-      tmem_ld16(tmem + lane_addr + C::S_COL(j & 1), sr);
+      uint32_t sr[NCW];
+      tmem_ld_cols<NCW>(tmem + lane_addr + C::S_COL(j & 1) + cg * NCW, sr);
       // S(j) has completed: K_j's slot is free
-      if (t == 0 && 2 * j + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j) % NSLOT]);
+      if (threadIdx.x == 0 && 2 * j + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j) % NSLOT]);
       tmem_ld_wait();
       const int key = (j0 + j) * DBN + t;
-      float y[NC];
+      float y[NCW];
 #pragma unroll
-      for (int n = 0; n < NC; ++n)
+      for (int n = 0; n < NCW; ++n)
         y[n] = key < vend[n] ? fmaf(__uint_as_float(sr[n]), coef[n], lgv) : -INFINITY;
       // column maxima over the tile's 128 keys: per warp, then across warps
-      float wmax[NC];
+      float wmax[NCW];
 #pragma unroll
-      for (int n = 0; n < NC; ++n) asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(wmax[n]) : "f"(y[n]));
+      for (int n = 0; n < NCW; ++n) asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(wmax[n]) : "f"(y[n]));
       if (lane == 0) {
 #pragma unroll
-        for (int n = 0; n < NC; n += 4)
-          *reinterpret_cast<float4*>(&red_sh[j & 1][warp * NC + n]) =
+        for (int n = 0; n < NCW; n += 4)
+          *reinterpret_cast<float4*>(&red_sh[j & 1][(warp & 3) * NC + cg * NCW + n]) =
               make_float4(wmax[n], wmax[n + 1], wmax[n + 2], wmax[n + 3]);
       }
       mbar_arrive(&red_full[j & 1]);
@@ -1353,13 +1369,14 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
       }
       // The reference follows the running maximum exactly (no lazy slack), so
       // the largest weight of a row is exactly 1, which e4m3 holds exactly.
-      float alpha[NC];
+      float alpha[NCW];
       bool grew = false;
 #pragma unroll
-      for (int n4 = 0; n4 < NC; n4 += 4) {
+      for (int n4 = 0; n4 < NCW; n4 += 4) {
         float4 r4[4];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) r4[w] = *reinterpret_cast<const float4*>(&red_sh[j & 1][w * NC + n4]);
+        for (int w = 0; w < 4; ++w)
+          r4[w] = *reinterpret_cast<const float4*>(&red_sh[j & 1][w * NC + cg * NCW + n4]);
         const float mt[4] = {fmaxf(fmaxf(r4[0].x, r4[1].x), fmaxf(r4[2].x, r4[3].x)),
                              fmaxf(fmaxf(r4[0].y, r4[1].y), fmaxf(r4[2].y, r4[3].y)),
                              fmaxf(fmaxf(r4[0].z, r4[1].z), fmaxf(r4[2].z, r4[3].z)),
@@ -1376,20 +1393,21 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
         }
       }
       // weights P' = 2^(y - m) <= 1, e4m3 codes into row n of P'^T (key t)
-      float pw[NC];
+      float pw[NCW];
 #pragma unroll
-      for (int n = 0; n < NC; ++n) {
+      for (int n = 0; n < NCW; ++n) {
         const float off = (m_ref[n] == -INFINITY ? 0.f : -m_ref[n]) + lgv;
         pw[n] = key < vend[n] ? ex2_approx(fmaf(__uint_as_float(sr[n]), coef[n], off)) : 0.f;
         lsum[n] = fmaf(pw[n], inv_dv, lsum[n] * alpha[n]);
       }
       const uint32_t pbase = smem_u32(sP + (j & 1) * C::CHUNK16) + (t & 15);
 #pragma unroll
-      for (int n = 0; n < NC; n += 2) {
+      for (int n = 0; n < NCW; n += 2) {
+        const int nc = cg * NCW + n;
         uint16_t pr;
         asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pr) : "f"(pw[n + 1]), "f"(pw[n]));
-        st_shared_u8(pbase + n * 128 + ((((t >> 4) ^ n) & 7) << 4), pr & 0xFFu);
-        st_shared_u8(pbase + (n + 1) * 128 + ((((t >> 4) ^ (n + 1)) & 7) << 4), pr >> 8);
+        st_shared_u8(pbase + nc * 128 + ((((t >> 4) ^ nc) & 7) << 4), pr & 0xFFu);
+        st_shared_u8(pbase + (nc + 1) * 128 + ((((t >> 4) ^ (nc + 1)) & 7) << 4), pr >> 8);
       }
       if (j > 0 && __any_sync(0xffffffffu, grew)) {
         // rescale O^T by alpha once P V(j - 1) has landed (the phase of its
@@ -1400,12 +1418,12 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
           return false;
         }
         tc_fence_after_sync();
-        uint32_t o[16];
-        tmem_ld16(tmem + lane_addr + C::O_COL, o);
+        uint32_t o[NCW];
+        tmem_ld_cols<NCW>(tmem + lane_addr + C::O_COL + cg * NCW, o);
         tmem_ld_wait();
 #pragma unroll
-        for (int n = 0; n < NC; ++n) o[n] = __float_as_uint(__uint_as_float(o[n]) * alpha[n]);
-        tmem_st16(tmem + lane_addr + C::O_COL, o);
+        for (int n = 0; n < NCW; ++n) o[n] = __float_as_uint(__uint_as_float(o[n]) * alpha[n]);
+        tmem_st_cols<NCW>(tmem + lane_addr + C::O_COL + cg * NCW, o);
         tmem_st_wait();
       }
       fence_proxy_async_smem();
@@ -1429,20 +1447,21 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
     // ------------------------------------------------------------ epilogue
     if (ok && !__any_sync(0xffffffffu, !mbar_wait(&o_full, 0, ab, kDevTimeoutEpilogue))) {
       tc_fence_after_sync();
-      uint32_t o[16];
-      tmem_ld16(tmem + lane_addr + C::O_COL, o);
+      uint32_t o[NCW];
+      tmem_ld_cols<NCW>(tmem + lane_addr + C::O_COL + cg * NCW, o);
       tmem_ld_wait();
       int col;
-      const float wsum = warp_col_reduce<NC>(lsum, lane, AddOp{}, &col);
-      fin_sh[warp * NC + col] = wsum;
+      const float wsum = warp_col_reduce<NCW>(lsum, lane, AddOp{}, &col);
+      fin_sh[(warp & 3) * NC + cg * NCW + col] = wsum;
       mbar_arrive(&fin_bar);
       if (!__any_sync(0xffffffffu, !mbar_wait(&fin_bar, 0, ab, kDevTimeoutEpilogue))) {
 #pragma unroll
-        for (int n = 0; n < NC; ++n) {
-          if (n >= kp.rows_real) break;
-          const float l = ((fin_sh[n] + fin_sh[NC + n]) + fin_sh[2 * NC + n]) + fin_sh[3 * NC + n];
+        for (int n = 0; n < NCW; ++n) {
+          const int nc = cg * NCW + n;
+          if (nc >= kp.rows_real) break;
+          const float l = ((fin_sh[nc] + fin_sh[NC + nc]) + fin_sh[2 * NC + nc]) + fin_sh[3 * NC + nc];
           const float inv_l = l > 0.f ? 1.f / l : 0.f;
-          const size_t pr = (prow0 + n) * kp.splits + split;
+          const size_t pr = (prow0 + nc) * kp.splits + split;
           kp.o_part[pr * D + t] = __uint_as_float(o[n]) * inv_l;
           if (t == 0) kp.lse_part[pr] = l > 0.f ? (m_ref[n] + lg2_dec(l)) * 0.69314718055994530942f : -INFINITY;
         }
@@ -1472,11 +1491,11 @@ __global__ void __launch_bounds__(Dec8TCfg::THREADS, 1)
   }
 }
 
-template <bool FP16, int NC>
+template <bool FP16, int NC, int CW>
 attn_status_t launch_decode_fp8_keys(const DecodeParams& p, const DecKParams& kp, const DecodeSplits& sp,
                                      const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-  using C = Dec8TCfg;
-  auto kern = decode_fp8_keys_kernel<FP16, NC>;
+  using C = Dec8TCfg<CW>;
+  auto kern = decode_fp8_keys_kernel<FP16, NC, CW>;
   attn_status_t s = set_smem(reinterpret_cast<const void*>(kern), C::SMEM);
   if (s != ATTN_OK) return s;
   CUtensorMap tq;
@@ -1518,10 +1537,12 @@ attn_status_t launch_decode_fp8_t(const DecodeParams& p, cudaStream_t stream) {
                 sp.splits,     sp.tiles_per_split, p.causal, p.scale * 1.4426950408889634f,
                 p.k_descale,   p.v_descale, p.signs, p.H_kv, shift};
   const int rows_real = (p.H / p.H_kv) * p.n_q;
-  if (rows_real <= Dec8TCfg::NQ) {
-    s = rows_real <= 4   ? launch_decode_fp8_keys<FP16, 4>(p, kp, sp, tk, tv, stream)
-        : rows_real <= 8 ? launch_decode_fp8_keys<FP16, 8>(p, kp, sp, tk, tv, stream)
-                         : launch_decode_fp8_keys<FP16, 16>(p, kp, sp, tk, tv, stream);
+  if (rows_real <= Dec8TCfg<1>::NQ) {
+    // up to 4 query rows: one softmax warp per key quarter; more: two, each
+    // taking half of the query columns
+    s = rows_real <= 4   ? launch_decode_fp8_keys<FP16, 4, 1>(p, kp, sp, tk, tv, stream)
+        : rows_real <= 8 ? launch_decode_fp8_keys<FP16, 8, 2>(p, kp, sp, tk, tv, stream)
+                         : launch_decode_fp8_keys<FP16, 16, 2>(p, kp, sp, tk, tv, stream);
     if (s != ATTN_OK) return s;
   } else {
     kern<<<dim3(sp.splits, p.H_kv, p.B), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, kp);
