@@ -42,10 +42,10 @@ WORKLOAD = "attention step (bf16 fwd + bf16 bwd + fp8 pre-pass + fp8 fwd), B=2 H
 # kernel's source files when the capture was taken; once they change, the
 # figure no longer describes the kernel and the line reports traffic as null.
 NCU_TRAFFIC = {
-    "fwd_bf16": {"bytes": 247_716_608, "src": "533a5703aca929b9"},      # 201.4 MB read + 46.3 MB write
-    "bwd_bf16": {"bytes": 623_137_536, "src": "ce67d0247e0c40db"},      # 405.0 MB read + 218.1 MB write
-    "fwd_fp8": {"bytes": 130_528_512, "src": "95917a811a77b3f6"},       # 100.8 MB read + 29.7 MB write
-    "fp8_prepass": {"bytes": 268_293_120, "src": "95917a811a77b3f6"},   # 201.4 MB read + 66.9 MB write
+    "fwd_bf16": {"bytes": 247_644_928, "src": "a3d36cc3c3bb3716"},      # 201.4 MB read + 46.2 MB write
+    "bwd_bf16": {"bytes": 622_878_976, "src": "b46ee46459be4a33"},      # 404.9 MB read + 217.9 MB write
+    "fwd_fp8": {"bytes": 130_680_064, "src": "e93c6ffab6bcc688"},       # 100.8 MB read + 29.9 MB write
+    "fp8_prepass": {"bytes": 268_097_280, "src": "e93c6ffab6bcc688"},   # 201.4 MB read + 66.7 MB write
 }
 KERNEL_SOURCES = {"fwd_bf16": "fwd.cu", "bwd_bf16": "bwd.cu", "fwd_fp8": "fp8.cu",
                   "fp8_prepass": "fp8.cu"}
@@ -842,6 +842,23 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_decode_only(args):
+    """The paged decode lines alone, as one JSON line (not the bench contract's
+    line: no step is timed)."""
+    import torch
+    import exact_tiled_attention_25_gb300 as attn
+    attn.load_library()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    out = run_decode(torch, attn, dev, stream, args.steps, args.warmup)
+    out.update(run_decode_fp8(torch, attn, dev, stream, args.steps, args.warmup))
+    assert attn.attn_get_device_status() == 0, attn.attn_last_error()
+    hbm = peaks()["hbm_gbs"]
+    for v in out.values():
+        v["frac_hbm"] = round(v["gbs"] / hbm, 3)
+    print(json.dumps({"decode": out, "hbm_peak_gbs": hbm}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -853,6 +870,9 @@ def main():
     ap.add_argument("--no-sweep", dest="sweep", action="store_false",
                     help="skip the head-dimension sweep")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the paged decode lines (BF16 and e4m3 caches) and print them; "
+                         "the profiling captures of the decode kernels use this")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -863,6 +883,9 @@ def main():
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.decode_only:
+        run_decode_only(args)
+        return
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
