@@ -49,10 +49,17 @@ def assert_fwd_close(o_gpu, lse_gpu, o_ref, lse_ref, max_abs=FWD_MAX_ABS, rmse=F
 def rel_rmse(g_gpu, g_ref, floor=1e-4):
     """RMSE(g - g_ref) / RMS(g_ref).  The denominator is floored at `floor`
     because some gradients are exactly zero (e.g. dQ and dK with a single key),
-    where only float32 rounding residue remains on the GPU."""
-    g = g_gpu.float().cpu().numpy().astype(np.float64)
+    where only float32 rounding residue remains on the GPU.  The floor applies
+    only there: a reference with RMS below it must be zero up to float64
+    rounding (RMS < 1e-9), otherwise the floor could hide a real error and the
+    call fails."""
+    g = g_gpu.float().cpu().numpy().astype(np.float64) if hasattr(g_gpu, "float") else np.asarray(
+        g_gpu, dtype=np.float64)
     assert np.all(np.isfinite(g))
-    return float(np.sqrt(np.mean((g - g_ref) ** 2)) / max(np.sqrt(np.mean(g_ref ** 2)), floor))
+    rms_ref = float(np.sqrt(np.mean(g_ref ** 2)))
+    assert rms_ref >= floor or rms_ref < 1e-9, (
+        f"reference RMS {rms_ref:.3g} is below the floor {floor:g} but not zero")
+    return float(np.sqrt(np.mean((g - g_ref) ** 2)) / max(rms_ref, floor))
 
 
 def guarded(shape, dtype, fill):
