@@ -94,6 +94,18 @@ __global__ void __launch_bounds__(256)
   float4 s4 = make_float4(1.f, 1.f, 1.f, 1.f);
   if (hadamard) s4 = reinterpret_cast<const float4*>(signs)[lane];
   const float inv_sqrt_d = 0.08838834764831845f;   // 1 / sqrt(128)
+  // bfloat16 rows are small enough (8 bytes per lane) to have all 16 of the
+  // warp's loads in flight before the first transform
+  uint2 raw[BF16IN ? 16 : 1];
+  if constexpr (BF16IN) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int row = blk * 128 + warp * 16 + r;
+      raw[r] = row < nrows ? __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(src) + row0 +
+                                                                 row * rstride) + lane)
+                           : make_uint2(0u, 0u);
+    }
+  }
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = blk * 128 + warp * 16 + r;
@@ -101,8 +113,7 @@ __global__ void __launch_bounds__(256)
     if (row < nrows) {
       if constexpr (BF16IN) {
         // four bfloat16 values; each is the upper half of its float32
-        const uint2 w = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(src) + row0 +
-                                                        row * rstride)[lane];
+        const uint2 w = raw[r];
         v = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
                         __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
       } else {
