@@ -604,14 +604,17 @@ __global__ void __launch_bounds__(THREADS8, 1)
     const float* vdesc = kp.v_descale + static_cast<size_t>(kvp) * kp.nblk;
     float dv_max = 0.f;
     for (int b = 0; b < (N + BN - 1) / BN; ++b) dv_max = fmaxf(dv_max, vdesc[b]);
+    const float inv_dv_max = 1.f / dv_max;
     const float c_q = (my_nK > 0) ? kp.scale_log2 * kp.q_descale[static_cast<size_t>(bh) * kp.nblk + qt] : 0.f;
     float m_ref = -INFINITY;   // in log2 units of the scaled scores
     float l = 0.f;             // this half's share of the row sum
     bool ok = true;
     for (int j = 0; j < my_nK; ++j) {
       const float cj = c_q * kdesc[j];
-      const float ratio = vdesc[j] / dv_max;              // in (0, 1]
+      const float ratio = vdesc[j] * inv_dv_max;          // in (0, 1]
       const float lg_ratio = lg2_approx8(ratio);
+      float inv_ratio;
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv_ratio) : "f"(ratio));
       // A warp that gives up (decided for the whole warp: the TMEM loads below
       // are warp-collective) still arrives at this step's pair barrier, where
       // its partner may be waiting; the partner then fails its next wait too,
@@ -692,7 +695,7 @@ __global__ void __launch_bounds__(THREADS8, 1)
         tmem_st_x8(tS + c0 * 8, pk);
       }
       const uint64_t acc = fadd2(acc0, acc1);
-      l += (lo2(acc) + hi2(acc)) / ratio;                   // sum of the unscaled P
+      l = fmaf(lo2(acc) + hi2(acc), inv_ratio, l);          // sum of the unscaled P
       // Rescale this half's columns of O (this step's P V product is issued
       // only after the arrive below; the previous one finished before S_t(j)).
       if (j > 0 && __any_sync(0xffffffffu, need)) {
