@@ -954,10 +954,12 @@ __global__ void __launch_bounds__(Dec8Cfg::THREADS, 1)
 //     S^T (128 keys x 16) = K_j Q8^T,      O^T (d x 16) += V_j^T P'^T,
 // so each softmax thread holds the scores of one key for every query row and
 // computes NC (>= R, a power of two <= 16) exponentials per tile, where the
-// rows-on-M kernel computes 128 per thread for 128 padded rows.  The row
-// maximum becomes a reduction over the 128 key threads (a column-transposing
-// warp exchange, then the four warps' partial maxima through shared memory and
-// an mbarrier), the row sums stay per thread until the end, and the weights go
+// rows-on-M kernel computes 128 per thread for 128 padded rows (with more than
+// 4 rows, CW = 2 softmax warps share a key quarter, each taking half of the
+// columns).  The row maximum becomes a reduction over the 128 key threads
+// (redux.sync per warp, then the four key quarters' partial maxima through
+// shared memory and an mbarrier), the row sums stay per thread until the
+// epilogue (one column-transposing warp exchange there), and the weights go
 // to shared memory as the B operand of the P V product.  Numerics are those of
 // the rows-on-M kernel: the same query quantiser, the exact running maximum of
 // y = s + log2(dv) per row, P' = 2^(y - m) in e4m3 against raw value codes,
