@@ -626,8 +626,8 @@ def run_decode(torch, attn, dev, stream, steps=20, warmup=3):
 
 def run_decode_fp8(torch, attn, dev, stream, steps=20, warmup=3):
     """Paged decode over an e4m3 cache at the shape of run_decode: random codes
-    with a random descale per (page, head); n_q = 1, 2 and 4, and n_q = 1 with
-    the key transform.  GB/s of algorithmic bytes: the cached codes read once, the
+    with a random descale per (page, head); n_q = 1, 2, 4 and 8, and n_q = 1
+    with the key transform.  GB/s of algorithmic bytes: the cached codes read once, the
     descales, Q and O."""
     Bq, L, h, hkv, d, ps = 16, 8192, 32, 8, 128, 256
     npg = Bq * L // ps
@@ -639,7 +639,7 @@ def run_decode_fp8(torch, attn, dev, stream, steps=20, warmup=3):
     lens = torch.full((Bq,), L, dtype=torch.int32, device=dev)
     signs = torch.where(torch.rand(d, generator=g, device=dev) < 0.5, -1.0, 1.0).float()
     out = {}
-    for n_q, sg in ((1, None), (2, None), (4, None), (1, signs)):
+    for n_q, sg in ((1, None), (2, None), (4, None), (8, None), (1, signs)):
         q = torch.randn((Bq, h, n_q, d), generator=g, device=dev).to(torch.bfloat16)
         o = torch.empty_like(q)
         lse = torch.empty((Bq, h, n_q), dtype=torch.float32, device=dev)

@@ -121,12 +121,13 @@ def test_heads_and_query_tokens(attn, H, H_kv, n_q):
     _check(*_run(attn, [300, 1025, 64], 32, H, H_kv, n_q, True, seed=81))
 
 
-@pytest.mark.parametrize("H,H_kv,n_q", [(32, 2, 1), (12, 2, 2), (6, 2, 5), (34, 2, 1)])
+@pytest.mark.parametrize("H,H_kv,n_q", [(32, 2, 1), (12, 2, 2), (6, 2, 5), (34, 2, 1), (40, 2, 1),
+                                         (64, 2, 1), (16, 2, 4), (66, 2, 1)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_query_rows_per_head(attn, H, H_kv, n_q, causal):
     # G n_q = 16, 12 and 15 query rows per key/value head run with the keys on
-    # the MMA's M side and 16 query columns per softmax thread; 17 rows run
-    # with the query rows on M
+    # the MMA's M side and N = 16; 17, 20, 32 (as 16 query heads x 2 tokens and
+    # as 8 x 4) and 33 rows with the query rows on M
     _check(*_run(attn, [300, 1025, 64], 64, H, H_kv, n_q, causal, seed=92))
 
 
