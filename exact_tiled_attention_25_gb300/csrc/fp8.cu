@@ -89,11 +89,14 @@ __global__ void __launch_bounds__(256)
   const int lane = threadIdx.x % 32;
   __shared__ float warp_max[8];
 
-  float4 x[16];   // 16 rows per warp, 4 columns per lane
+  // 16 rows per warp, 4 columns per lane, as two packed float32 pairs
+  // (columns 4 lane, 4 lane + 1 and 4 lane + 2, 4 lane + 3)
+  uint64_t x01[16], x23[16];
   float amax = 0.f;
   float4 s4 = make_float4(1.f, 1.f, 1.f, 1.f);
   if (hadamard) s4 = reinterpret_cast<const float4*>(signs)[lane];
   const float inv_sqrt_d = 0.08838834764831845f;   // 1 / sqrt(128)
+  const uint64_t isd2 = pack2(inv_sqrt_d, inv_sqrt_d);
   // bfloat16 rows are small enough (8 bytes per lane) to have all 16 of the
   // warp's loads in flight before the first transform
   uint2 raw[BF16IN ? 16 : 1];
@@ -106,6 +109,12 @@ __global__ void __launch_bounds__(256)
                            : make_uint2(0u, 0u);
     }
   }
+  // The sign diagonal of M on bfloat16 inputs: multiplying by -1 flips the
+  // sign bit, done while widening.
+  const uint32_t sgx = (!ROPE && BF16IN && s4.x < 0.f) ? 0x80000000u : 0u;
+  const uint32_t sgy = (!ROPE && BF16IN && s4.y < 0.f) ? 0x80000000u : 0u;
+  const uint32_t sgz = (!ROPE && BF16IN && s4.z < 0.f) ? 0x80000000u : 0u;
+  const uint32_t sgw = (!ROPE && BF16IN && s4.w < 0.f) ? 0x80000000u : 0u;
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = blk * 128 + warp * 16 + r;
@@ -114,8 +123,8 @@ __global__ void __launch_bounds__(256)
       if constexpr (BF16IN) {
         // four bfloat16 values; each is the upper half of its float32
         const uint2 w = raw[r];
-        v = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                        __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+        v = make_float4(__uint_as_float((w.x << 16) ^ sgx), __uint_as_float((w.x & 0xffff0000u) ^ sgy),
+                        __uint_as_float((w.y << 16) ^ sgz), __uint_as_float((w.y & 0xffff0000u) ^ sgw));
       } else {
         v = reinterpret_cast<const float4*>(static_cast<const float*>(src) + row0 + row * rstride)[lane];
       }
@@ -135,28 +144,37 @@ __global__ void __launch_bounds__(256)
       v = make_float4(fmaf(sg * ox, sn.x, v.x * c4.x), fmaf(sg * oy, sn.y, v.y * c4.y),
                       fmaf(sg * oz, sn.z, v.z * c4.z), fmaf(sg * ow, sn.w, v.w * c4.w));
     }
+    uint64_t p01 = pack2(v.x, v.y), p23 = pack2(v.z, v.w);
     if (hadamard) {
-      v.x *= s4.x; v.y *= s4.y; v.z *= s4.z; v.w *= s4.w;
+      if (ROPE || !BF16IN) {
+        p01 = fmul2(p01, pack2(s4.x, s4.y));
+        p23 = fmul2(p23, pack2(s4.z, s4.w));
+      }
       // stages of span 1 and 2 inside the lane (columns 4*lane .. 4*lane+3)
-      float a = v.x + v.y, b = v.x - v.y, c = v.z + v.w, e = v.z - v.w;
-      v = make_float4(a + c, b + e, a - c, b - e);
-      // stages of span 4 .. 64 across lanes (lane distance 1 .. 16)
+      const float a = lo2(p01) + hi2(p01), b = lo2(p01) - hi2(p01);
+      const float c = lo2(p23) + hi2(p23), e = lo2(p23) - hi2(p23);
+      p01 = pack2(a + c, b + e);
+      p23 = pack2(a - c, b - e);
+      // stages of span 4 .. 64 across lanes (lane distance 1 .. 16): the lane
+      // with bit m set takes partner - own, the other own + partner, both as
+      // one fused multiply-add by +-1 (exact as the add or subtract)
 #pragma unroll
       for (int m = 1; m < 32; m <<= 1) {
-        const float ox = __shfl_xor_sync(0xffffffffu, v.x, m);
-        const float oy = __shfl_xor_sync(0xffffffffu, v.y, m);
-        const float oz = __shfl_xor_sync(0xffffffffu, v.z, m);
-        const float ow = __shfl_xor_sync(0xffffffffu, v.w, m);
-        if (lane & m) {
-          v = make_float4(ox - v.x, oy - v.y, oz - v.z, ow - v.w);
-        } else {
-          v = make_float4(v.x + ox, v.y + oy, v.z + oz, v.w + ow);
-        }
+        const float ox = __shfl_xor_sync(0xffffffffu, lo2(p01), m);
+        const float oy = __shfl_xor_sync(0xffffffffu, hi2(p01), m);
+        const float oz = __shfl_xor_sync(0xffffffffu, lo2(p23), m);
+        const float ow = __shfl_xor_sync(0xffffffffu, hi2(p23), m);
+        const float sg = (lane & m) ? -1.f : 1.f;
+        const uint64_t sg2 = pack2(sg, sg);
+        p01 = ffma2(sg2, p01, pack2(ox, oy));
+        p23 = ffma2(sg2, p23, pack2(oz, ow));
       }
-      v.x *= inv_sqrt_d; v.y *= inv_sqrt_d; v.z *= inv_sqrt_d; v.w *= inv_sqrt_d;
+      p01 = fmul2(p01, isd2);
+      p23 = fmul2(p23, isd2);
     }
-    x[r] = v;
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    x01[r] = p01;
+    x23[r] = p23;
+    amax = fmax3(amax, fmax3(fabsf(lo2(p01)), fabsf(hi2(p01)), fabsf(lo2(p23))), fabsf(hi2(p23)));
   }
 
   float descale;
@@ -177,15 +195,20 @@ __global__ void __launch_bounds__(256)
     descale = bmax > 0.f ? __fdiv_rn(bmax, kE4m3Max) : 1.f;
     if (threadIdx.x == 0) desc[static_cast<size_t>(bh) * nblk + blk] = descale;
   }
-  // code = e4m3(x / descale), the quotient rounded as an IEEE division would
+  // code = e4m3(x / descale), the quotient rounded as an IEEE division would:
+  // q0 = x y with y = 1 / descale, then q0 + (x - descale q0) y (the steps of
+  // div_by_recip on packed pairs)
   const float rdesc = __fdiv_rn(1.f, descale);
+  const uint64_t y2 = pack2(rdesc, rdesc);
+  const uint64_t nb2 = pack2(-descale, -descale);
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = blk * 128 + warp * 16 + r;
     if (row < nrows) {
-      const float4 v = x[r];
-      const uint32_t packed = cvt_pack_e4m3x4(div_by_recip(v.x, descale, rdesc), div_by_recip(v.y, descale, rdesc),
-                                              div_by_recip(v.z, descale, rdesc), div_by_recip(v.w, descale, rdesc));
+      const uint64_t q01 = fmul2(x01[r], y2), q23 = fmul2(x23[r], y2);
+      const uint64_t c01 = ffma2(ffma2(nb2, q01, x01[r]), y2, q01);
+      const uint64_t c23 = ffma2(ffma2(nb2, q23, x23[r]), y2, q23);
+      const uint32_t packed = cvt_pack_e4m3x4(lo2(c01), hi2(c01), lo2(c23), hi2(c23));
       reinterpret_cast<uint32_t*>(dst + row0 + row * rstride)[lane] = packed;
     }
   }
