@@ -44,8 +44,8 @@ WORKLOAD = "attention step (bf16 fwd + bf16 bwd + fp8 pre-pass + fp8 fwd), B=2 H
 NCU_TRAFFIC = {
     "fwd_bf16": {"bytes": 247_644_928, "src": "a3d36cc3c3bb3716"},      # 201.4 MB read + 46.2 MB write
     "bwd_bf16": {"bytes": 622_878_976, "src": "b46ee46459be4a33"},      # 404.9 MB read + 217.9 MB write
-    "fwd_fp8": {"bytes": 130_450_176, "src": "180a2ffba3a70c03"},       # 100.7 MB read + 29.7 MB write
-    "fp8_prepass": {"bytes": 270_585_344, "src": "180a2ffba3a70c03"},   # 201.4 MB read + 69.2 MB write
+    "fwd_fp8": {"bytes": 130_427_392, "src": "db186e3e96a3d4be"},       # 100.7 MB read + 29.7 MB write
+    "fp8_prepass": {"bytes": 270_648_832, "src": "db186e3e96a3d4be"},   # 201.4 MB read + 69.3 MB write
 }
 KERNEL_SOURCES = {"fwd_bf16": "fwd.cu", "bwd_bf16": "bwd.cu", "fwd_fp8": "fp8.cu",
                   "fp8_prepass": "fp8.cu"}

@@ -33,6 +33,40 @@ constexpr int kSmemLimit = 232448;
 constexpr float kE4m3Max = 448.f;
 
 // ============================================================== pre-pass ====
+// Walsh-Hadamard butterfly (unnormalised) of a 128-value row held by a warp as
+// 32 lanes x 4 values, packed as (columns 4 lane, 4 lane + 1) and (4 lane + 2,
+// 4 lane + 3): the stages of span 1 and 2 inside the lane, then those of span
+// 4 .. 64 across lanes (lane distance 1 .. 16), where the lane with bit m set
+// takes partner - own and the other own + partner, both as one fused
+// multiply-add by +-1 (exactly the add or the subtract).
+__device__ __forceinline__ void wht128_row(uint64_t& p01, uint64_t& p23, int lane) {
+  const float a = lo2(p01) + hi2(p01), b = lo2(p01) - hi2(p01);
+  const float c = lo2(p23) + hi2(p23), e = lo2(p23) - hi2(p23);
+  p01 = pack2(a + c, b + e);
+  p23 = pack2(a - c, b - e);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const float ox = __shfl_xor_sync(0xffffffffu, lo2(p01), m);
+    const float oy = __shfl_xor_sync(0xffffffffu, hi2(p01), m);
+    const float oz = __shfl_xor_sync(0xffffffffu, lo2(p23), m);
+    const float ow = __shfl_xor_sync(0xffffffffu, hi2(p23), m);
+    const float sg = (lane & m) ? -1.f : 1.f;
+    const uint64_t sg2 = pack2(sg, sg);
+    p01 = ffma2(sg2, p01, pack2(ox, oy));
+    p23 = ffma2(sg2, p23, pack2(oz, ow));
+  }
+}
+
+// code = e4m3(x / descale) for four values (two packed pairs), each quotient
+// rounded as an IEEE division would: q0 = x y with y = 1 / descale, then
+// q0 + (x - descale q0) y (the steps of div_by_recip on packed pairs).
+__device__ __forceinline__ uint32_t quantise4(uint64_t x01, uint64_t x23, uint64_t y2, uint64_t nb2) {
+  const uint64_t q01 = fmul2(x01, y2), q23 = fmul2(x23, y2);
+  const uint64_t c01 = ffma2(ffma2(nb2, q01, x01), y2, q01);
+  const uint64_t c23 = ffma2(ffma2(nb2, q23, x23), y2, q23);
+  return cvt_pack_e4m3x4(lo2(c01), hi2(c01), lo2(c23), hi2(c23));
+}
+
 // Mode: 0 = fused block mode (amax + quantise), 1 = block amax only (into
 // descale), 2 = quantise with the descale already in place.  PACKED (mode 0):
 // sequences packed back to back, [total, heads, d]; N is the longest sequence
@@ -150,25 +184,7 @@ __global__ void __launch_bounds__(256)
         p01 = fmul2(p01, pack2(s4.x, s4.y));
         p23 = fmul2(p23, pack2(s4.z, s4.w));
       }
-      // stages of span 1 and 2 inside the lane (columns 4*lane .. 4*lane+3)
-      const float a = lo2(p01) + hi2(p01), b = lo2(p01) - hi2(p01);
-      const float c = lo2(p23) + hi2(p23), e = lo2(p23) - hi2(p23);
-      p01 = pack2(a + c, b + e);
-      p23 = pack2(a - c, b - e);
-      // stages of span 4 .. 64 across lanes (lane distance 1 .. 16): the lane
-      // with bit m set takes partner - own, the other own + partner, both as
-      // one fused multiply-add by +-1 (exact as the add or subtract)
-#pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const float ox = __shfl_xor_sync(0xffffffffu, lo2(p01), m);
-        const float oy = __shfl_xor_sync(0xffffffffu, hi2(p01), m);
-        const float oz = __shfl_xor_sync(0xffffffffu, lo2(p23), m);
-        const float ow = __shfl_xor_sync(0xffffffffu, hi2(p23), m);
-        const float sg = (lane & m) ? -1.f : 1.f;
-        const uint64_t sg2 = pack2(sg, sg);
-        p01 = ffma2(sg2, p01, pack2(ox, oy));
-        p23 = ffma2(sg2, p23, pack2(oz, ow));
-      }
+      wht128_row(p01, p23, lane);
       p01 = fmul2(p01, isd2);
       p23 = fmul2(p23, isd2);
     }
@@ -195,22 +211,14 @@ __global__ void __launch_bounds__(256)
     descale = bmax > 0.f ? __fdiv_rn(bmax, kE4m3Max) : 1.f;
     if (threadIdx.x == 0) desc[static_cast<size_t>(bh) * nblk + blk] = descale;
   }
-  // code = e4m3(x / descale), the quotient rounded as an IEEE division would:
-  // q0 = x y with y = 1 / descale, then q0 + (x - descale q0) y (the steps of
-  // div_by_recip on packed pairs)
   const float rdesc = __fdiv_rn(1.f, descale);
   const uint64_t y2 = pack2(rdesc, rdesc);
   const uint64_t nb2 = pack2(-descale, -descale);
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int row = blk * 128 + warp * 16 + r;
-    if (row < nrows) {
-      const uint64_t q01 = fmul2(x01[r], y2), q23 = fmul2(x23[r], y2);
-      const uint64_t c01 = ffma2(ffma2(nb2, q01, x01[r]), y2, q01);
-      const uint64_t c23 = ffma2(ffma2(nb2, q23, x23[r]), y2, q23);
-      const uint32_t packed = cvt_pack_e4m3x4(lo2(c01), hi2(c01), lo2(c23), hi2(c23));
-      reinterpret_cast<uint32_t*>(dst + row0 + row * rstride)[lane] = packed;
-    }
+    if (row < nrows)
+      reinterpret_cast<uint32_t*>(dst + row0 + row * rstride)[lane] = quantise4(x01[r], x23[r], y2, nb2);
   }
 }
 
@@ -297,24 +305,13 @@ __global__ void __launch_bounds__(256)
                         fmaf(sg * o.z, sn.z, v.z * c.z), fmaf(sg * o.w, sn.w, v.w * c.w));
       }
       if (hadamard) {
-        v.x *= s4.x; v.y *= s4.y; v.z *= s4.z; v.w *= s4.w;
-        // stages of span 1 and 2 inside the lane (columns 4*lane .. 4*lane+3)
-        float a = v.x + v.y, b = v.x - v.y, c = v.z + v.w, e = v.z - v.w;
-        v = make_float4(a + c, b + e, a - c, b - e);
-        // stages of span 4 .. 64 across lanes (lane distance 1 .. 16)
-#pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-          const float ox = __shfl_xor_sync(0xffffffffu, v.x, m);
-          const float oy = __shfl_xor_sync(0xffffffffu, v.y, m);
-          const float oz = __shfl_xor_sync(0xffffffffu, v.z, m);
-          const float ow = __shfl_xor_sync(0xffffffffu, v.w, m);
-          if (lane & m) {
-            v = make_float4(ox - v.x, oy - v.y, oz - v.z, ow - v.w);
-          } else {
-            v = make_float4(v.x + ox, v.y + oy, v.z + oz, v.w + ow);
-          }
-        }
-        v.x *= inv_sqrt_d; v.y *= inv_sqrt_d; v.z *= inv_sqrt_d; v.w *= inv_sqrt_d;
+        uint64_t p01 = fmul2(pack2(v.x, v.y), pack2(s4.x, s4.y));
+        uint64_t p23 = fmul2(pack2(v.z, v.w), pack2(s4.z, s4.w));
+        wht128_row(p01, p23, lane);
+        const uint64_t isd2 = pack2(inv_sqrt_d, inv_sqrt_d);
+        p01 = fmul2(p01, isd2);
+        p23 = fmul2(p23, isd2);
+        v = make_float4(lo2(p01), hi2(p01), lo2(p23), hi2(p23));
       }
       if (rotate || hadamard) {
         __syncwarp();                                 // partners read before the write-back
@@ -343,14 +340,15 @@ __global__ void __launch_bounds__(256)
     if (threadIdx.x == 0) desc[static_cast<size_t>(bh) * nblk + blk] = descale;
   }
   const float rdesc = __fdiv_rn(1.f, descale);
+  const uint64_t y2 = pack2(rdesc, rdesc);
+  const uint64_t nb2 = pack2(-descale, -descale);
 #pragma unroll 4
   for (int r = 0; r < 16; ++r) {
     const int lr = warp * 16 + r;
     if (lr >= rows) break;
     const float4 v = reinterpret_cast<const float4*>(sblk + lr * D)[lane];
-    const uint32_t packed = cvt_pack_e4m3x4(div_by_recip(v.x, descale, rdesc), div_by_recip(v.y, descale, rdesc),
-                                            div_by_recip(v.z, descale, rdesc), div_by_recip(v.w, descale, rdesc));
-    reinterpret_cast<uint32_t*>(dst + (static_cast<size_t>(bh) * N + blk * QROWS + lr) * D)[lane] = packed;
+    reinterpret_cast<uint32_t*>(dst + (static_cast<size_t>(bh) * N + blk * QROWS + lr) * D)[lane] =
+        quantise4(pack2(v.x, v.y), pack2(v.z, v.w), y2, nb2);
   }
 }
 
