@@ -70,6 +70,12 @@ struct FwdCfg {
   __host__ __device__ static constexpr uint32_t P_COL(int kk) {
     return 64u * static_cast<uint32_t>(kk / 4) + 8u * static_cast<uint32_t>(kk % 4);
   }
+  // With a ring of two stages (d = 256: 64 KB tiles) the next K or V tile can
+  // load only into the stage just read, so the MMA thread hands each stage back
+  // by a commit right after the products that read it; with deeper rings the
+  // softmax does it when it sees S(j) complete, which keeps commits off the
+  // MMA thread.
+  static constexpr bool COMMIT_RELEASE = (NSLOT == 2);
   static_assert(NSLOT >= 2, "need at least two ring stages");
   static_assert(O_COL(NQ - 1) + D <= 512, "TMEM overflow");
   static_assert(S_COL(NQ - 1) + 128 <= 256, "S region overflow");
@@ -276,6 +282,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ_>::THREADS, 1)
               mma_f16_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + C::P_COL(kk),
                          sdesc_add(vdesc, kk * 16 * 128), idPV, (j - 1 > 0 || kk > 0) ? 1u : 0u);
             if (j - 1 == nK[t] - 1) mma_commit(&o_full[t]);
+            if (C::COMMIT_RELEASE && t == t_rel && itV + NSLOT < total_items) mma_commit(&kv_empty[slotV]);
           }
           if (j < nK[t]) {
             // S_t(j) = Q_t K_j^T
@@ -293,6 +300,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ_>::THREADS, 1)
                          kk > 0 ? 1u : 0u);
             }
             mma_commit(&s_full[t]);
+            if (C::COMMIT_RELEASE && t == t_rel && itK + NSLOT < total_items) mma_commit(&kv_empty[slotK]);
           }
         }
         if (!ok) break;
@@ -330,7 +338,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ_>::THREADS, 1)
         break;
       }
       tc_fence_after_sync();
-      if (t == t_rel && h == 0 && r == 0) {
+      if (!C::COMMIT_RELEASE && t == t_rel && h == 0 && r == 0) {
         // release only slots the producer refills
         if (2 * j + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j) % NSLOT]);
         if (j >= 1 && 2 * j - 1 + NSLOT < total_items) mbar_arrive(&kv_empty[(2 * j - 1) % NSLOT]);
