@@ -54,9 +54,16 @@ struct FwdCfg {
   static constexpr int TILE_BYTES = BM * D * 2;      // a Q, K or V tile
   // row-statistics exchange between the two warps of a row (static shared memory)
   static constexpr int XCH_BYTES = 2 * NQ * 2 * 128 * 4;
-  static constexpr int NSLOT_FIT = (kSmemLimit - 2048 - XCH_BYTES - NQ * TILE_BYTES) / TILE_BYTES;
+  // d = 256: S (128 columns) and O (256) leave 128 TMEM columns, enough for the
+  // query tile (128 rows x 256 bf16) as the A operand of S.  Q then needs no
+  // shared memory of its own (it is staged once through the last ring stage),
+  // and the ring gets a third 64 KB stage.
+  static constexpr bool Q_IN_TMEM = (D == 256 && NQ == 1);
+  static constexpr uint32_t Q_COL = 128;
+  static constexpr int Q_SMEM = Q_IN_TMEM ? 0 : NQ * TILE_BYTES;
+  static constexpr int NSLOT_FIT = (kSmemLimit - 2048 - XCH_BYTES - Q_SMEM) / TILE_BYTES;
   static constexpr int NSLOT = NSLOT_FIT > 6 ? 6 : NSLOT_FIT;
-  static constexpr int SMEM_BYTES = 1024 + NQ * TILE_BYTES + NSLOT * TILE_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + Q_SMEM + NSLOT * TILE_BYTES;
   // Two softmax warpgroups per query tile: each row of S is split between two
   // warps (key columns [0, 64) and [64, 128)).
   static constexpr int NUM_SOFTMAX_WARPS = 8 * NQ;
@@ -75,8 +82,9 @@ struct FwdCfg {
   // by a commit right after the products that read it; with deeper rings the
   // softmax does it when it sees S(j) complete, which keeps commits off the
   // MMA thread.
-  static constexpr bool COMMIT_RELEASE = (NSLOT == 2);
+  static constexpr bool COMMIT_RELEASE = (TILE_BYTES >= 65536);
   static_assert(NSLOT >= 2, "need at least two ring stages");
+  static_assert(!Q_IN_TMEM || (S_COL(0) + 128 <= Q_COL && Q_COL + D / 2 <= O_COL(0)), "TMEM overflow (Q)");
   static_assert(O_COL(NQ - 1) + D <= 512, "TMEM overflow");
   static_assert(S_COL(NQ - 1) + 128 <= 256, "S region overflow");
 };
@@ -114,8 +122,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ_>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sKV = smem + NQ * C::TILE_BYTES;
+  uint8_t* sKV = smem + C::Q_SMEM;
+  // Q tiles: their own region, or (Q in tensor memory) staged in the last ring stage
+  uint8_t* sQ = C::Q_IN_TMEM ? sKV + (NSLOT - 1) * C::TILE_BYTES : smem;
 
   __shared__ __align__(8) uint64_t q_full[NQ];
   __shared__ __align__(8) uint64_t kv_full[NSLOT];
@@ -124,6 +133,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ_>::THREADS, 1)
   __shared__ __align__(8) uint64_t p_full[NQ];
   __shared__ __align__(8) uint64_t o_full[NQ];
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t q_moved;   // Q in tensor memory: its staging stage is free
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ int load_items_sh;
@@ -182,6 +192,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ_>::THREADS, 1)
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(&drain_bar, 1);
+    mbar_init(&q_moved, 32 * C::NUM_SOFTMAX_WARPS);
     abort_sh = 0;
     load_items_sh = 0;
     fence_mbar_init();
@@ -231,6 +242,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ_>::THREADS, 1)
             ok = false;
             break;
           }
+          // the last stage holds Q until the softmax warps have copied it to tensor memory
+          if (C::Q_IN_TMEM && it == NSLOT - 1 && !mbar_wait(&q_moved, 0, ab, kDevTimeoutLoad)) {
+            ok = false;
+            break;
+          }
           mbar_arrive_expect_tx(&kv_full[slot], C::TILE_BYTES);
           uint8_t* dst = sKV + slot * C::TILE_BYTES;
 #pragma unroll
@@ -258,7 +274,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ_>::THREADS, 1)
       bool ok = true;
 #pragma unroll
       for (int t = 0; t < NQ; ++t)
-        if (ok && nK[t] > 0) ok = mbar_wait(&q_full[t], 0, ab, kDevTimeoutMma);
+        if (ok && nK[t] > 0)
+          ok = C::Q_IN_TMEM ? mbar_wait(&q_moved, 0, ab, kDevTimeoutMma) : mbar_wait(&q_full[t], 0, ab, kDevTimeoutMma);
       for (int j = 0; j <= nKmax && ok; ++j) {
         const int itK = 2 * j;          // ring item of K_j
         const int itV = 2 * j - 1;      // ring item of V_{j-1}
@@ -296,8 +313,12 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ_>::THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32;
-              mma_f16_ss(tmem + C::S_COL(t), sdesc_add(qdesc, off), sdesc_add(kdesc, off), idS,
-                         kk > 0 ? 1u : 0u);
+              if constexpr (C::Q_IN_TMEM)
+                mma_f16_ts(tmem + C::S_COL(t), tmem + C::Q_COL + 8u * kk, sdesc_add(kdesc, off), idS,
+                           kk > 0 ? 1u : 0u);
+              else
+                mma_f16_ss(tmem + C::S_COL(t), sdesc_add(qdesc, off), sdesc_add(kdesc, off), idS,
+                           kk > 0 ? 1u : 0u);
             }
             mma_commit(&s_full[t]);
             if (C::COMMIT_RELEASE && t == t_rel && itK + NSLOT < total_items) mma_commit(&kv_empty[slotK]);
@@ -327,7 +348,39 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ_>::THREADS, 1)
     float m_ref = -INFINITY;
     float l = 0.f;                       // this half's share of the row sum
     bool ok = true;
-    for (int j = 0; j < my_nK; ++j) {
+    if constexpr (C::Q_IN_TMEM) {
+      // Copy this warp's half of its rows of Q (d in [128 h, 128 h + 128): chunks
+      // 2h, 2h + 1 of the 128-byte-swizzled tile) into tensor memory, two bf16 per
+      // column, then hand the staging stage back.  Every softmax thread arrives
+      // at q_moved (the producer and the MMA thread wait on it).
+      if (my_nK > 0) {
+        if (__any_sync(0xffffffffu, !mbar_wait(&q_full[t], 0, ab, kDevTimeoutSoftmax))) {
+          ok = false;
+        } else {
+          const uint8_t* qrow = sQ + t * C::TILE_BYTES + r * 128;
+          const uint32_t tQ = tmem + lane_addr + C::Q_COL + (D / 4) * h;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const uint8_t* chunk = qrow + (2 * h + cc) * C::CHUNK_BYTES;
+            uint32_t w[32];
+#pragma unroll
+            for (int pc = 0; pc < 8; ++pc) {
+              const uint4 v = *reinterpret_cast<const uint4*>(chunk + ((pc ^ (r & 7)) * 16));
+              w[4 * pc] = v.x;
+              w[4 * pc + 1] = v.y;
+              w[4 * pc + 2] = v.z;
+              w[4 * pc + 3] = v.w;
+            }
+            tmem_st32(tQ + 32 * cc, w);
+          }
+          tmem_st_wait();
+        }
+      }
+      fence_proxy_async_smem();   // the reads above come before the stage's next copy
+      tc_fence_before_sync();
+      mbar_arrive(&q_moved);
+    }
+    for (int j = 0; ok && j < my_nK; ++j) {
       // A warp that gives up (decided for the whole warp: the TMEM loads below
       // are warp-collective) still arrives at this step's pair barrier, where
       // its partner may be waiting; the partner then fails its next wait too,
