@@ -11,7 +11,9 @@
 //  * One CTA owns NQ query tiles of 128 rows (NQ = 2 for d <= 128, 1 for
 //    d = 256).  Scores S_t and output accumulators O_t live in tensor memory
 //    (TMEM); the probabilities P_t are written back over S_t as 16-bit values
-//    and fed to the P V product straight from TMEM.
+//    and fed to the P V product straight from TMEM.  At d = 256 the query tile
+//    sits in TMEM too (the A operand of S), which leaves shared memory for a
+//    third K/V stage.
 //  * Warp roles: one TMA producer warp, one MMA warp whose elected thread
 //    issues every tcgen05.mma, and two softmax warpgroups per query tile: a
 //    warp owns 32 rows (one TMEM lane quarter) and one half of the key
