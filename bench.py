@@ -42,7 +42,7 @@ WORKLOAD = "attention step (bf16 fwd + bf16 bwd + fp8 pre-pass + fp8 fwd), B=2 H
 # kernel's source files when the capture was taken; once they change, the
 # figure no longer describes the kernel and the line reports traffic as null.
 NCU_TRAFFIC = {
-    "fwd_bf16": {"bytes": 247_720_704, "src": "b00e1a845695e5b4"},      # 201.4 MB read + 46.3 MB write
+    "fwd_bf16": {"bytes": 247_944_960, "src": "4556e39afb1bcd95"},      # 201.4 MB read + 46.5 MB write
     "bwd_bf16": {"bytes": 622_878_976, "src": "b46ee46459be4a33"},      # 404.9 MB read + 217.9 MB write
     "fwd_fp8": {"bytes": 130_427_392, "src": "db186e3e96a3d4be"},       # 100.7 MB read + 29.7 MB write
     "fp8_prepass": {"bytes": 270_648_832, "src": "db186e3e96a3d4be"},   # 201.4 MB read + 69.3 MB write
