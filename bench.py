@@ -44,8 +44,8 @@ WORKLOAD = "attention step (bf16 fwd + bf16 bwd + fp8 pre-pass + fp8 fwd), B=2 H
 NCU_TRAFFIC = {
     "fwd_bf16": {"bytes": 247_944_960, "src": "4556e39afb1bcd95"},      # 201.4 MB read + 46.5 MB write
     "bwd_bf16": {"bytes": 622_878_976, "src": "b46ee46459be4a33"},      # 404.9 MB read + 217.9 MB write
-    "fwd_fp8": {"bytes": 130_427_392, "src": "db186e3e96a3d4be"},       # 100.7 MB read + 29.7 MB write
-    "fp8_prepass": {"bytes": 270_648_832, "src": "db186e3e96a3d4be"},   # 201.4 MB read + 69.3 MB write
+    "fwd_fp8": {"bytes": 130_313_728, "src": "75a2b568ddb5cc49"},       # 100.7 MB read + 29.6 MB write
+    "fp8_prepass": {"bytes": 270_740_992, "src": "75a2b568ddb5cc49"},   # 201.4 MB read + 69.4 MB write
 }
 KERNEL_SOURCES = {"fwd_bf16": "fwd.cu", "bwd_bf16": "bwd.cu", "fwd_fp8": "fp8.cu",
                   "fp8_prepass": "fp8.cu"}
@@ -304,7 +304,8 @@ def run_ours(args, rank, world):
                            "timed alone, well under a second, at full clocks); fp8 = 2x bf16")
 
     e2e = run_e2e(args, torch, attn, dev, stream, step_parts, causal, scale, q, k, v, do, signs, rope)
-    ablation = run_ablation(torch, attn, stream, causal, scale, q, k, v) if args.sweep else None
+    ablation = (run_ablation(torch, attn, stream, causal, scale, q, k, v, args.exp2_eighths)
+                if args.sweep else None)
     sweep = run_sweep(torch, attn, dev, stream, causal) if args.sweep else None
     fp8_acc = run_fp8_accuracy(torch, attn, dev) if args.sweep else None
     launches = sum(l for _, _, _, l in step_parts) * args.steps
@@ -486,7 +487,7 @@ def time_call(torch, stream, fn, steps=20, warmup=3):
     return a.elapsed_time(b) / steps
 
 
-def run_ablation(torch, attn, stream, causal, scale, q, k, v):
+def run_ablation(torch, attn, stream, causal, scale, q, k, v, exp2_eighths=(2,)):
     """The forward pipeline ablation on the timed workload: the default schedule
     (two query tiles per CTA alternating on the tensor core, lazy rescaling)
     against one query tile per CTA (nothing fills the tensor core while a
@@ -503,11 +504,15 @@ def run_ablation(torch, attn, stream, causal, scale, q, k, v):
                                             o=o, lse=lse, stream=stream)
         ms = time_call(torch, stream, fn)
         out[name] = {"ms": round(ms, 4), "tflops": round(flop / (ms * 1e-3) / 1e12, 1)}
-    # FP8 forward with a quarter of its exponentials on the FMA pipe
+    # FP8 forward: the library's default (one eighth of the exponentials on the FMA
+    # pipe for non-causal batches), all on the MUFU unit, and k eighths (--exp2-eighths)
     signs = torch.where(torch.arange(q.shape[-1], device=q.device) % 3 == 0, -1.0, 1.0).float()
     (q8, k8, v8), (qs, ks, vs) = attn.attn_fp8_quantize_bf16(q, k, v, signs, stream=stream)
     o8 = torch.empty_like(q)
-    for name, sched in (("fp8_default", 0), ("fp8_exp2_poly_quarter", attn.ATTN_SCHED_EXP2_POLY)):
+    names = {1: "eighth", 2: "quarter", 3: "three_eighths", 4: "half"}
+    variants = ([("fp8_default", 0), ("fp8_exp2_none", attn.ATTN_SCHED_EXP2_NONE)] +
+                [(f"fp8_exp2_poly_{names[e]}", attn.ATTN_SCHED_EXP2_EIGHTHS(e)) for e in exp2_eighths])
+    for name, sched in variants:
         fn = lambda: attn.attn_fwd_fp8_schedule(q8, k8, v8, qs, ks, vs, sched, causal=causal,
                                                 softmax_scale=scale, o=o8, lse=lse, stream=stream)
         ms = time_call(torch, stream, fn)
@@ -870,6 +875,9 @@ def main():
     ap.add_argument("--no-sweep", dest="sweep", action="store_false",
                     help="skip the head-dimension sweep")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--exp2-eighths", type=int, nargs="+", default=[2], choices=[1, 2, 3, 4],
+                    help="shares (in eighths) of the FP8 forward's exponentials evaluated on the FMA "
+                         "pipe in the ablation entries (default: a quarter)")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the paged decode lines (BF16 and e4m3 caches) and print them; "
                          "the profiling captures of the decode kernels use this")

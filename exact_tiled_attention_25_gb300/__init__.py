@@ -33,6 +33,13 @@ ATTN_SCHED_DEFAULT = 0
 ATTN_SCHED_ONE_TILE = 1
 ATTN_SCHED_EAGER_RESCALE = 2
 ATTN_SCHED_EXP2_POLY = 4
+ATTN_SCHED_EXP2_NONE = 8
+
+
+def ATTN_SCHED_EXP2_EIGHTHS(k: int) -> int:
+    """Schedule value for k of every 8 FP8-forward exponentials on the FMA pipe (k = 1..4)."""
+    return ATTN_SCHED_EXP2_POLY | (int(k) << 8)
+
 
 __all__ = ["AttnError", "attn_fwd", "attn_fwd_schedule", "attn_fwd_gqa", "attn_fwd_varlen", "attn_bwd",
            "attn_bwd_gqa", "attn_bwd_varlen", "attn_bwd_varlen_workspace_size",
@@ -536,7 +543,8 @@ def attn_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, causal: bool = Fal
 def attn_fwd_fp8_schedule(q8, k8, v8, q_descale, k_descale, v_descale, schedule: int,
                           causal: bool = False, softmax_scale: float | None = None, o=None,
                           lse=None, stream=None):
-    """attn_fwd_fp8 with a schedule variant (0 or ATTN_SCHED_EXP2_POLY), for measurement."""
+    """attn_fwd_fp8 with a schedule variant (0 = attn_fwd_fp8, ATTN_SCHED_EXP2_NONE,
+    ATTN_SCHED_EXP2_POLY or ATTN_SCHED_EXP2_EIGHTHS(k)), for measurement."""
     lib = _lib.load()
     B, H, N, d = _shape4(q8, "q8")
     for t, n in ((k8, "k8"), (v8, "v8")):

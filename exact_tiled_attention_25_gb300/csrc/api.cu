@@ -613,13 +613,19 @@ attn_status_t attn_fwd_fp8_schedule(const uint8_t* q8, const uint8_t* k8, const 
   if (!q_descale || !k_descale || !v_descale)
     return fail(ATTN_ERR_INVALID_ARG, "null descale pointer");
   if ((s = check_scale(softmax_scale)) != ATTN_OK) return s;
-  if (schedule != 0 && schedule != ATTN_SCHED_EXP2_POLY)
-    return fail(ATTN_ERR_INVALID_ARG, "schedule must be 0 or ATTN_SCHED_EXP2_POLY");
+  // 0, ATTN_SCHED_EXP2_NONE, or ATTN_SCHED_EXP2_POLY with an optional share of 1..4
+  // eighths in bits 8..11
+  const int eighths = (schedule >> 8) & 15;
+  if (schedule != 0 && schedule != ATTN_SCHED_EXP2_NONE &&
+      ((schedule & ~(15 << 8)) != ATTN_SCHED_EXP2_POLY || eighths > 4))
+    return fail(ATTN_ERR_INVALID_ARG,
+                "schedule must be 0, ATTN_SCHED_EXP2_NONE, ATTN_SCHED_EXP2_POLY or "
+                "ATTN_SCHED_EXP2_EIGHTHS(1..4)");
   if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
   if ((s = check_device()) != ATTN_OK) return s;
   Fp8FwdParams p{q8, k8, v8, q_descale, k_descale, v_descale, o, lse, B, H, N, d, causal,
                  softmax_scale, H};
-  p.exp2_poly = schedule == ATTN_SCHED_EXP2_POLY ? 1 : 0;
+  p.exp2_poly = schedule == 0 ? -1 : schedule == ATTN_SCHED_EXP2_NONE ? 0 : (eighths == 0 ? 2 : eighths);
   return launch_fwd_fp8(p, stream);
 }
 

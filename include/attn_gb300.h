@@ -89,9 +89,16 @@ enum {
                                     runs, the tensor core has no second tile to work on */
   ATTN_SCHED_EAGER_RESCALE = 2,  /* rescale the output accumulator whenever the row max
                                     grows, instead of only when it grows by more than 2^8 */
-  ATTN_SCHED_EXP2_POLY = 4       /* FP8 forward only: a quarter of the exponentials on the
-                                    FMA pipe (a fitted cubic) instead of the MUFU unit */
+  ATTN_SCHED_EXP2_POLY = 4,      /* FP8 forward only: part of the exponentials on the FMA
+                                    pipe (a fitted cubic) instead of the MUFU unit; the
+                                    share is set in eighths by ATTN_SCHED_EXP2_EIGHTHS,
+                                    a quarter when none is given */
+  ATTN_SCHED_EXP2_NONE = 8       /* FP8 forward only: every exponential on the MUFU unit */
 };
+
+/* The FMA-pipe share of the FP8 forward's exponentials, k of every 8 (k = 1..4), as a
+   schedule value: ATTN_SCHED_EXP2_POLY with k in bits 8..11. */
+#define ATTN_SCHED_EXP2_EIGHTHS(k) (ATTN_SCHED_EXP2_POLY | ((k) << 8))
 
 /*
  * attn_fwd_schedule -- attn_fwd with a schedule variant.  `schedule` is a
@@ -491,11 +498,15 @@ attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* 
 
 /*
  * attn_fwd_fp8_schedule -- attn_fwd_fp8 with a schedule variant, for
- * measurement.  `schedule` is 0 (exactly attn_fwd_fp8) or ATTN_SCHED_EXP2_POLY:
- * a quarter of each softmax thread's exponentials are evaluated on the FMA
- * pipe by range reduction and a cubic (relative error <= 1.1e-4, below the
- * e4m3 rounding of P) instead of by the MUFU unit.  Other values return
- * ATTN_ERR_INVALID_ARG.  Arguments, layout and errors as attn_fwd_fp8.
+ * measurement.  `schedule` is 0 (exactly attn_fwd_fp8, which evaluates one
+ * eighth of the exponentials on the FMA pipe for non-causal batches and none
+ * for causal ones), ATTN_SCHED_EXP2_NONE (every exponential on the
+ * MUFU unit), ATTN_SCHED_EXP2_POLY or ATTN_SCHED_EXP2_EIGHTHS(k), k = 1..4: k of
+ * every 8 of each softmax thread's exponentials (a quarter for
+ * ATTN_SCHED_EXP2_POLY alone) are evaluated on the FMA pipe by range reduction
+ * and a cubic (relative error <= 1.1e-4, below the e4m3 rounding of P) instead
+ * of by the MUFU unit.  Other values return ATTN_ERR_INVALID_ARG.  Arguments,
+ * layout and errors as attn_fwd_fp8.
  * Source: "FlashAttention-3: Hopper Asynchrony and FP8 Attention", section
  * "Why This Exists" (FP8 doubles the matrix-multiply rate but not the rate of
  * exponentials).

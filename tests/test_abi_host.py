@@ -276,3 +276,15 @@ def test_fp8_quantize_ex_validates(lib):
                           (dict(cu=18, total=300), 1, "cu_seqlens"), (dict(cu=16, total=0), 1, ">= 1")):
         assert call(**kw) == code, kw
         assert why.lower() in lib.attn_last_error().decode().lower(), (kw, lib.attn_last_error())
+
+
+def test_fp8_schedule_validates_the_exp2_share(lib):
+    """attn_fwd_fp8_schedule takes 0, ATTN_SCHED_EXP2_NONE, ATTN_SCHED_EXP2_POLY or
+    ATTN_SCHED_EXP2_EIGHTHS(1..4) and rejects anything else before touching the GPU."""
+    import exact_tiled_attention_25_gb300 as attn
+    args = (16, 16, 16, 16, 16, 16, 16, 16, 1, 1, 128, 128, 0, 0.1)
+    for bad in (1, 2, 12, attn.ATTN_SCHED_EXP2_NONE | (1 << 8), attn.ATTN_SCHED_EXP2_EIGHTHS(5),
+                attn.ATTN_SCHED_EXP2_EIGHTHS(15), attn.ATTN_SCHED_EXP2_POLY | (1 << 12)):
+        assert lib.attn_fwd_fp8_schedule(*args, bad, None) == 1, bad
+        assert b"schedule" in lib.attn_last_error()
+    assert attn.ATTN_SCHED_EXP2_EIGHTHS(2) == attn.ATTN_SCHED_EXP2_POLY | (2 << 8)

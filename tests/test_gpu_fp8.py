@@ -292,18 +292,22 @@ def test_exp2_polynomial_error_on_the_gpu(attn):
     assert np.all(yp[xf == 0.0] == 1.0)
 
 
+@pytest.mark.parametrize("eighths", ["none", 0, 1, 3, 4])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [129, 640])
-def test_fp8_exp2_poly_variant_matches_dequantised_oracle(attn, N, causal):
-    """The forward with a quarter of its exponentials on the FMA pipe computes
-    the same attention (the polynomial's error is far below the e4m3 rounding of P)."""
+def test_fp8_exp2_poly_variant_matches_dequantised_oracle(attn, N, causal, eighths):
+    """The forward with none or part of its exponentials on the FMA pipe (a quarter
+    for ATTN_SCHED_EXP2_POLY alone, else k eighths) computes the same attention as
+    the library's default (the polynomial's error is far below the e4m3 rounding of P)."""
     B, H, d = 1, 2, 128
     q, k, v = workloads.normal_with_outliers(60 + N, (B, H, N, d), 3)
     signs = workloads.random_signs(5, d)
     gq, gk, gv = (torch.from_numpy(x).to(dev()) for x in (q, k, v))
     (q8, k8, v8), (qd, kd, vd) = attn.attn_fp8_quantize(gq, gk, gv,
                                                         hadamard_signs=torch.from_numpy(signs).to(dev()))
-    o, lse = attn.attn_fwd_fp8_schedule(q8, k8, v8, qd, kd, vd, attn.ATTN_SCHED_EXP2_POLY,
+    sched = (attn.ATTN_SCHED_EXP2_NONE if eighths == "none" else
+             attn.ATTN_SCHED_EXP2_POLY if eighths == 0 else attn.ATTN_SCHED_EXP2_EIGHTHS(eighths))
+    o, lse = attn.attn_fwd_fp8_schedule(q8, k8, v8, qd, kd, vd, sched,
                                         causal=causal, softmax_scale=1 / np.sqrt(d))
     o0, _ = attn.attn_fwd_fp8(q8, k8, v8, qd, kd, vd, causal=causal, softmax_scale=1 / np.sqrt(d))
     check_status(attn)
