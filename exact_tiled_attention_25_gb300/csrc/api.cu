@@ -625,7 +625,8 @@ attn_status_t attn_fwd_fp8_schedule(const uint8_t* q8, const uint8_t* k8, const 
   if ((s = check_device()) != ATTN_OK) return s;
   Fp8FwdParams p{q8, k8, v8, q_descale, k_descale, v_descale, o, lse, B, H, N, d, causal,
                  softmax_scale, H};
-  p.exp2_poly = schedule == 0 ? -1 : schedule == ATTN_SCHED_EXP2_NONE ? 0 : (eighths == 0 ? 2 : eighths);
+  // the kernels count the share in sixteenths
+  p.exp2_poly = schedule == 0 ? -1 : schedule == ATTN_SCHED_EXP2_NONE ? 0 : 2 * (eighths == 0 ? 2 : eighths);
   return launch_fwd_fp8(p, stream);
 }
 

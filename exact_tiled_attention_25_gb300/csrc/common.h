@@ -108,7 +108,7 @@ struct Fp8FwdParams {
   int H_kv;   // heads of K and V (H % H_kv == 0)
   const int* cu_seqlens = nullptr;   // packed batch: device [B + 1] offsets (N = longest)
   int total = 0;                     // packed batch: tokens
-  int exp2_poly = -1;                // eighths of the exponentials on the FMA pipe (0..4); -1: the library's choice
+  int exp2_poly = -1;                // sixteenths of the exponentials on the FMA pipe (0, 1, 2, 4, 6, 8); -1: the library's choice
 };
 
 attn_status_t launch_fwd(const FwdParams& p, cudaStream_t stream);

@@ -422,12 +422,13 @@ __device__ __forceinline__ float lg2_approx8(float x) {
 // descales [B, heads, ceil(max_seqlen / 128)] per sequence's 128-row blocks, O
 // [total, H, d], LSE [H, total]; kp.N is the longest sequence; query and key
 // tiles are read at the sequence's first token by 4-D tensor maps.
-// POLY (0..4): of every eight 4-key groups of a softmax thread, POLY (spread
-// out: group i when i POLY mod 8 < POLY) are evaluated by exp2_poly2 on the
-// FMA pipe instead of the MUFU unit.  One eighth measured a little faster than
-// none on fixed-length non-causal batches and is the library's choice there; a
-// quarter or more measured slower (each emulated exponential takes several issue
-// slots, and the softmax is bound by instruction issue, not by the MUFU rate).
+// POLY (0..8): of the sixteen 4-key groups of a softmax thread's step, POLY
+// (spread out: group g when g POLY mod 16 < POLY) are evaluated by exp2_poly2 on
+// the FMA pipe instead of the MUFU unit.  One sixteenth measured a little faster
+// than none or one eighth on non-causal batches and is the library's choice
+// there; three sixteenths or more measured slower (each emulated exponential
+// takes several issue slots, and the softmax is bound by instruction issue, not
+// by the MUFU rate).
 template <bool CAUSAL, bool PACKED, int POLY = 0>
 __global__ void __launch_bounds__(THREADS8, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -697,7 +698,7 @@ __global__ void __launch_bounds__(THREADS8, 1)
           const uint64_t y0 = ffma2(pack2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), cc, nn);
           const uint64_t y1 = ffma2(pack2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), cc, nn);
           float p0, p1, p2, p3;
-          if (POLY > 0 && ((i * POLY) % 8) < POLY) {
+          if (POLY > 0 && (((c0 * 8 + i) * POLY) % 16) < POLY) {
             const uint64_t e0 = exp2_poly2(lo2(y0), hi2(y0));
             const uint64_t e1 = exp2_poly2(lo2(y1), hi2(y1));
             p0 = lo2(e0);
@@ -944,11 +945,11 @@ attn_status_t launch_fwd_fp8(const Fp8FwdParams& p, cudaStream_t stream) {
   if (p.d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 path supports d = 128");
   if (p.N > 65535 * 256 || p.H > 65535 || p.B > 65535)
     return fail(ATTN_ERR_UNSUPPORTED, "grid dimension limit exceeded");
-  // The library's share of exponentials on the FMA pipe: one eighth for
-  // non-causal batches (measured 1731 -> 1766 TFLOP/s at B = 2, H = 16,
-  // N = 8192; causal unchanged, a quarter or more slower), none for causal ones.
-  // Packed batches take the same choice, so one packed sequence gives the bits
-  // of the fixed-length call.
+  // The library's share of exponentials on the FMA pipe (in sixteenths): one
+  // sixteenth for non-causal batches (at B = 2, H = 16, N = 8192: 1732 TFLOP/s
+  // with none, 1765 with one eighth, 1777 with one sixteenth; causal unchanged;
+  // three sixteenths or more slower), none for causal ones.  Packed batches take
+  // the same choice, so one packed sequence gives the bits of the fixed-length call.
   const int poly = p.exp2_poly >= 0 ? p.exp2_poly : (p.causal ? 0 : 1);
   if (p.cu_seqlens) {
     if (poly == 0)
@@ -960,9 +961,10 @@ attn_status_t launch_fwd_fp8(const Fp8FwdParams& p, cudaStream_t stream) {
     case 0: break;
     case 1: return p.causal ? launch_fwd_fp8_t<true, false, 1>(p, stream) : launch_fwd_fp8_t<false, false, 1>(p, stream);
     case 2: return p.causal ? launch_fwd_fp8_t<true, false, 2>(p, stream) : launch_fwd_fp8_t<false, false, 2>(p, stream);
-    case 3: return p.causal ? launch_fwd_fp8_t<true, false, 3>(p, stream) : launch_fwd_fp8_t<false, false, 3>(p, stream);
     case 4: return p.causal ? launch_fwd_fp8_t<true, false, 4>(p, stream) : launch_fwd_fp8_t<false, false, 4>(p, stream);
-    default: return fail(ATTN_ERR_INVALID_ARG, "exp2 share must be 0..4 eighths");
+    case 6: return p.causal ? launch_fwd_fp8_t<true, false, 6>(p, stream) : launch_fwd_fp8_t<false, false, 6>(p, stream);
+    case 8: return p.causal ? launch_fwd_fp8_t<true, false, 8>(p, stream) : launch_fwd_fp8_t<false, false, 8>(p, stream);
+    default: return fail(ATTN_ERR_INVALID_ARG, "exp2 share must be 0, 1, 2, 4, 6 or 8 sixteenths");
   }
   return p.causal ? launch_fwd_fp8_t<true, false>(p, stream) : launch_fwd_fp8_t<false, false>(p, stream);
 }

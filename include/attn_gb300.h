@@ -499,7 +499,7 @@ attn_status_t attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* 
 /*
  * attn_fwd_fp8_schedule -- attn_fwd_fp8 with a schedule variant, for
  * measurement.  `schedule` is 0 (exactly attn_fwd_fp8, which evaluates one
- * eighth of the exponentials on the FMA pipe for non-causal batches and none
+ * sixteenth of the exponentials on the FMA pipe for non-causal batches and none
  * for causal ones), ATTN_SCHED_EXP2_NONE (every exponential on the
  * MUFU unit), ATTN_SCHED_EXP2_POLY or ATTN_SCHED_EXP2_EIGHTHS(k), k = 1..4: k of
  * every 8 of each softmax thread's exponentials (a quarter for
